@@ -1,0 +1,175 @@
+/*
+ * kvpool -- a shared, asymmetrically quantized KV-cache pool for multi-agent
+ * decode on one GB300 GPU (sm_103a).
+ *
+ * The method (PolyKV: A Shared Asymmetrically-Compressed KV Cache Pool for
+ * Multi-Agent LLM Inference, gist.science summary, section 2): the full KV
+ * state of a shared document is computed once, compressed, and stored as ONE
+ * write-once / read-many object that every agent reads (section 2.A,
+ * SharedKVPool / PooledAgent). Keys are quantised per tensor to int8; values
+ * are rotated per head-vector by the fast Walsh-Hadamard transform and mapped
+ * to Lloyd-Max centroids for N(0,1), 3 bits by default (section 2.B). The
+ * CoMixKV article (zicq.com, "CoMixKV ... Qwen3显存降低32.08%") gives 2 to 4
+ * bits per layer and keeps the most recent states at native precision; here
+ * each layer has its own V bit width in {2, 3, 4} and every agent may bring a
+ * private bf16 recent-token tail to attention.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Return value: KVPOOL_OK (0) or a negative KVPOOL_ERR_* code. Argument and
+ *    state errors are reported synchronously and enqueue nothing.
+ *  - Errors found by a kernel (a non-finite K maximum or V norm, an expired
+ *    bounded wait) are recorded in a device status word. They are sticky and
+ *    are returned (and cleared) by kvpool_status().
+ *  - All device work is asynchronous on the caller's stream (`stream` is a
+ *    cudaStream_t passed as void*; NULL is the legacy default stream). Device
+ *    pointers passed in must stay valid until that work completes; the library
+ *    keeps no caller pointer after a call returns.
+ *  - The pool owns all of its device memory, allocated once by
+ *    kvpool_create(); compress, attend and decompress allocate nothing.
+ *  - bf16 tensors are raw IEEE bfloat16 bit patterns, row-major, contiguous,
+ *    16-byte aligned. head_dim is 64 or 128.
+ *  - After a layer is compressed its pool bytes are read-only, so concurrent
+ *    kvpool_attend / kvpool_decompress calls on different streams are safe.
+ *    A single pool must not be compressed from two host threads at once.
+ */
+#ifndef KVPOOL_H
+#define KVPOOL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum {
+    KVPOOL_OK = 0,
+    KVPOOL_ERR_INVALID_ARG = -1, /* null pointer, bad size, layer out of range  */
+    KVPOOL_ERR_STATE = -2,       /* write-once violated / layer not compressed   */
+    KVPOOL_ERR_CUDA = -3,        /* a CUDA runtime call or launch failed         */
+    KVPOOL_ERR_OOM = -4,         /* device allocation failed in kvpool_create    */
+    KVPOOL_ERR_NONFINITE = -5,   /* K maximum or a V norm was Inf/NaN (device)   */
+    KVPOOL_ERR_TIMEOUT = -6,     /* a bounded device wait expired (device)       */
+    KVPOOL_ERR_UNSUPPORTED = -7  /* no sm_103a device, or a shape not supported  */
+};
+
+typedef struct kvpool kvpool_t;
+
+/* A private recent-token tail per agent, kept at bf16 (CoMixKV article,
+ * incremental quantisation: recent states stay at native precision). Agent a
+ * attends over the pool followed by its first len[a] tail tokens, in one
+ * softmax. */
+typedef struct {
+    const void* K;      /* bf16 [agents][kv_heads][T_max][head_dim], device    */
+    const void* V;      /* bf16 [agents][kv_heads][T_max][head_dim], device    */
+    const int32_t* len; /* int32 [agents], device, each in [0, T_max]          */
+    int T_max;          /* capacity of the tail buffers, >= 0                  */
+} kvpool_tail_t;
+
+/* Device-side view of one compressed layer (for inspection and tests). The
+ * token axis is padded to `ctx_padded`; padding is zero and never read as a
+ * token. Pointers stay owned by the pool. */
+typedef struct {
+    const int8_t* kq;      /* int8 [kv_heads][ctx_padded][head_dim]            */
+    const uint8_t* vcodes; /* uint8 [kv_heads][ctx_padded][head_dim*bits/8]    */
+    const float* vnorm;    /* float [kv_heads][ctx_padded]                     */
+    const float* kscale;   /* one float: the layer's K scale s = max|K| / 127  */
+    int ctx;
+    int ctx_padded;
+    int bits;
+    int compressed;        /* 1 once kvpool_compress succeeded for the layer   */
+} kvpool_layer_view_t;
+
+/* Create a pool for `layers` layers of a shared context of `ctx` tokens with
+ * `kv_heads` KV heads of size `head_dim` (64 or 128). bits_per_layer: host
+ * array [layers] of V bit widths, each 2, 3 or 4 (NULL: 3 for every layer).
+ * max_rows: the most query rows that may share one KV head in kvpool_attend
+ * (agents x GQA group), 1..1024 (0: 512); it sizes the attention scratch.
+ * Allocates all device memory on the current device. Source: PolyKV summary,
+ * section 2.A (one shared object, O(1) in the number of agents). */
+int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
+                  const uint8_t* bits_per_layer, int max_rows);
+
+/* Free all device memory of the pool. Waits for the device first. NULL is a
+ * no-op. */
+void kvpool_destroy(kvpool_t* pool);
+
+/* Write-once encode of one layer. K, V: bf16 [kv_heads][ctx][head_dim], device.
+ * K: s = max|K| / 127 (float32; s = 1 when K is all zero), q = clamp(round-
+ * half-even(k / s), -127, 127). V, per head-vector v: n = |v| (float32,
+ * pairwise tree), u = H v (unnormalised FWHT, stages 1, 2, 4, ...), code_i =
+ * #{ j : u_i > fl(m_j * n) } for the float32 Lloyd-Max midpoints m_j, codes
+ * bit-packed little-endian. Source: PolyKV summary, section 2.B. Returns
+ * KVPOOL_ERR_STATE if the layer was already compressed (see
+ * kvpool_reset_layer). A non-finite K or V norm is reported by kvpool_status
+ * as KVPOOL_ERR_NONFINITE. */
+int kvpool_compress(kvpool_t* pool, int layer, const void* K, const void* V, void* stream);
+
+/* Decode attention of `agents` agents over one compressed layer.
+ * Q: bf16 [agents][q_heads][head_dim], device; q_heads a multiple of
+ * kv_heads; query head h reads KV head h / (q_heads / kv_heads).
+ * tail: NULL for none. out: float32 [agents][q_heads][head_dim], device.
+ * softmax_scale: 0 means 1/sqrt(head_dim).
+ * Every agent's rows attend over the dequantised pool (K = q*s, V = n*H c/d)
+ * followed by the agent's tail tokens, in one softmax. agents * group must not
+ * exceed the pool's max_rows. Source: PolyKV summary, section 2.A (every agent
+ * reads the same pool) and 2.B (dequantisation: centroid lookup + inverse
+ * FWHT). */
+int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_heads,
+                  const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream);
+
+/* Materialise one layer as bf16: K_out = bf16(q*s), V_out_i = bf16(fl(z_i*n)
+ * * (1/d)) with z = FWHT(c[codes]) in float32. K_out, V_out: bf16
+ * [kv_heads][ctx][head_dim], device. This is the per-agent decompression of
+ * the PolyKV summary, section 2.A (each agent injects the decompressed KV into
+ * its own cache). */
+int kvpool_decompress(kvpool_t* pool, int layer, void* K_out, void* V_out, void* stream);
+
+/* Compressed bytes held for the shared context: per layer, int8 K, packed V,
+ * float32 norms and the float32 K scale (padding excluded). Independent of
+ * the number of agents (PolyKV summary, section 4: the pool is O(1) in agents). */
+size_t kvpool_pool_bytes(const kvpool_t* pool);
+
+/* All device bytes the pool allocated (pool with padding, scratch, status). */
+size_t kvpool_device_bytes(const kvpool_t* pool);
+
+/* Synchronise `stream`, then return and clear the device status word
+ * (KVPOOL_OK or the first device-side error recorded). */
+int kvpool_status(kvpool_t* pool, void* stream);
+
+/* Re-arm the write-once guard of one layer so it can be compressed again. */
+int kvpool_reset_layer(kvpool_t* pool, int layer);
+
+/* Fill *view with the device pointers and sizes of one layer. */
+int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view);
+
+/* Copy the stored bytes of one compressed layer, token padding removed, to
+ * caller buffers in host or device memory (any of the four may be NULL):
+ * kq int8 [kv_heads][ctx][head_dim], vcodes uint8 [kv_heads][ctx][head_dim*
+ * bits/8], vnorm float [kv_heads][ctx], kscale one float. Asynchronous on
+ * `stream` (host buffers should be pinned). This is the quantised-cache handoff
+ * of the QKVShare blog (mhpn.cn, section 3.1: the sender packs the quantised
+ * cache with its scales; the receiver loads it instead of recomputing). */
+int kvpool_export_layer(const kvpool_t* pool, int layer, void* kq, void* vcodes, void* vnorm,
+                        void* kscale, void* stream);
+
+/* Load one layer from the four buffers kvpool_export_layer writes (same
+ * kv_heads, ctx, head_dim and bits). Write-once like kvpool_compress:
+ * KVPOOL_ERR_STATE if the layer already holds data. All four are required. */
+int kvpool_import_layer(kvpool_t* pool, int layer, const void* kq, const void* vcodes,
+                        const void* vnorm, const void* kscale, void* stream);
+
+/* Copy the library's float32 Lloyd-Max table for `bits` (2, 3 or 4) to host
+ * arrays: 2^bits centroids (ascending) and 2^bits - 1 midpoints. The library
+ * derives it on the host, once, in double precision. */
+int kvpool_codebook(int bits, float* centroids, float* midpoints);
+
+/* Static description of an error code. */
+const char* kvpool_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVPOOL_H */

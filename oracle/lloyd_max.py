@@ -42,7 +42,7 @@ def _upper_tail(x: float) -> float:
     return 0.5 * math.erfc(x / _SQRT2)
 
 
-def lloyd_max_normal(levels: int, tol: float = 1e-16, max_iter: int = 200000):
+def lloyd_max_normal(levels: int, tol: float = 1e-16, max_iter: int = 20000):
     """Return (centroids, thresholds) in float64 for ``levels`` in {2, 4, 8, 16}.
 
     ``centroids`` is ascending, length ``levels``; ``thresholds`` has the

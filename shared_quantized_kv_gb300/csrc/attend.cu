@@ -1,0 +1,261 @@
+// Decode attention of many agents directly over the shared pool.
+//
+// PolyKV summary, section 2.A: every agent reads the same compressed pool;
+// section 2.B: K = q * s, V = n * H c[codes] / d. Instead of materialising V
+// per agent, the pool is streamed once per step for all agents that share a
+// KV head, and P.V is accumulated in the rotated domain:
+//   sum_t p_t V_t = H (sum_t p_t n_t c[codes_t]) / d,
+// so the inverse FWHT runs once per output row instead of once per token.
+// The private bf16 tail of each agent (CoMixKV article: recent states stay at
+// native precision) joins the same softmax.
+//
+// CUDA-core path (split context):
+//   attend_split: grid (context split, kv head, row block). A CTA walks its
+//     token range in tiles of 32 tokens: K int8 and the V codes are expanded
+//     to float32 in shared memory (V already scaled by its norm), then each
+//     warp runs an online softmax for its rows (lane = token for the logits,
+//     lane = channel for the rotated accumulator). It writes (m, l, acc) per
+//     row for its split.
+//   attend_combine: one CTA per (row, kv head): log-sum-exp merge of the
+//     splits, inverse FWHT / d, the agent's tail tokens, final normalisation.
+#include <cuda_bf16.h>
+#include <math_constants.h>
+
+#include "kvpool_internal.cuh"
+
+namespace kvp {
+namespace {
+
+constexpr int kTileTok = 32;
+constexpr int kRowsPerWarp = 2;
+constexpr int kWarps = 8;
+constexpr int kRowsPerBlock = kRowsPerWarp * kWarps;
+
+__device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+template <int D, int BITS>
+__global__ void __launch_bounds__(kWarps * 32)
+attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ vcodes,
+                    const float* __restrict__ vnorm, const float* __restrict__ kscale, int ctx,
+                    int ctx_pad, const uint16_t* __restrict__ Q, int Hq, int G, int R,
+                    float scale_log2, int tok_per_split, float* __restrict__ part_acc,
+                    float* __restrict__ part_ml, int nsplit, int max_rows, Codebook cb) {
+    constexpr int VB = D * BITS / 8;
+    constexpr uint32_t MASK = (1u << BITS) - 1;
+    constexpr int DPL = D / 32;  // channels per lane
+    __shared__ float Ks[kTileTok][D + 1];
+    __shared__ float Vs[kTileTok][D];
+    __shared__ float Qs[kRowsPerBlock][D];
+    __shared__ float cen[16];
+
+    const int split = blockIdx.x, g = blockIdx.y, rb = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    for (int i = tid; i < kRowsPerBlock * D; i += blockDim.x) {
+        const int rr = i / D, c = i % D, r = rb * kRowsPerBlock + rr;
+        float val = 0.f;
+        if (r < R) {
+            const int a = r / G, j = r % G;
+            val = bf2f(Q[((long long)a * Hq + g * G + j) * D + c]);
+        }
+        Qs[rr][c] = val;
+    }
+    if (tid < 16) cen[tid] = cb.c[tid];
+
+    const float lscale = *kscale * scale_log2;
+    const int t_begin = split * tok_per_split;
+    const int t_end = min(ctx, t_begin + tok_per_split);
+    const int8_t* kbase = kq + (long long)g * ctx_pad * D;
+    const uint8_t* vbase = vcodes + (long long)g * ctx_pad * VB;
+    const float* nbase = vnorm + (long long)g * ctx_pad;
+
+    float m[kRowsPerWarp], l[kRowsPerWarp], acc[kRowsPerWarp][DPL];
+#pragma unroll
+    for (int r = 0; r < kRowsPerWarp; ++r) {
+        m[r] = -CUDART_INF_F;
+        l[r] = 0.f;
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) acc[r][k] = 0.f;
+    }
+    __syncthreads();
+
+    for (int t0 = t_begin; t0 < t_end; t0 += kTileTok) {
+        // K tile: int8 -> float (the scale s joins the logit scale)
+        for (int i = tid; i < kTileTok * D / 16; i += blockDim.x) {
+            const int tt = i / (D / 16), c = i % (D / 16);
+            const uint4 w = *reinterpret_cast<const uint4*>(kbase + (long long)(t0 + tt) * D + c * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                Ks[tt][c * 16 + e] = (float)(int8_t)((ws[e / 4] >> (8 * (e % 4))) & 0xFF);
+        }
+        // V tile: 8 codes at a time -> n_t * c[code]
+        for (int i = tid; i < kTileTok * D / 8; i += blockDim.x) {
+            const int tt = i / (D / 8), gi = i % (D / 8);
+            const uint8_t* p = vbase + (long long)(t0 + tt) * VB + gi * BITS;
+            uint32_t word = 0;
+#pragma unroll
+            for (int b = 0; b < BITS; ++b) word |= (uint32_t)p[b] << (8 * b);
+            const float n = nbase[t0 + tt];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) Vs[tt][gi * 8 + k] = cen[(word >> (BITS * k)) & MASK] * n;
+        }
+        __syncthreads();
+
+        const bool valid = (t0 + lane) < t_end;
+#pragma unroll
+        for (int r4 = 0; r4 < kRowsPerWarp; ++r4) {
+            const int rr = warp * kRowsPerWarp + r4;
+            float dot = 0.f;
+#pragma unroll 16
+            for (int i = 0; i < D; ++i) dot = fmaf(Qs[rr][i], Ks[lane][i], dot);
+            const float lg = valid ? dot * lscale : -CUDART_INF_F;
+            const float mnew = fmaxf(m[r4], warp_max(lg));
+            if (mnew == -CUDART_INF_F) continue;  // warp-uniform
+            const float corr = exp2f(m[r4] - mnew);
+            const float p = exp2f(lg - mnew);
+            l[r4] = l[r4] * corr + warp_sum(p);
+            m[r4] = mnew;
+#pragma unroll
+            for (int k = 0; k < DPL; ++k) acc[r4][k] *= corr;
+#pragma unroll 8
+            for (int tt = 0; tt < kTileTok; ++tt) {
+                const float pt = __shfl_sync(0xffffffffu, p, tt);
+#pragma unroll
+                for (int k = 0; k < DPL; ++k) acc[r4][k] = fmaf(pt, Vs[tt][lane + 32 * k], acc[r4][k]);
+            }
+        }
+        __syncthreads();
+    }
+
+#pragma unroll
+    for (int r4 = 0; r4 < kRowsPerWarp; ++r4) {
+        const int r = rb * kRowsPerBlock + warp * kRowsPerWarp + r4;
+        if (r >= R) continue;
+        const long long base = ((long long)g * nsplit + split) * max_rows + r;
+        if (lane == 0) {
+            part_ml[2 * base] = m[r4];
+            part_ml[2 * base + 1] = l[r4];
+        }
+#pragma unroll
+        for (int k = 0; k < DPL; ++k) part_acc[base * D + lane + 32 * k] = acc[r4][k];
+    }
+}
+
+template <int D>
+__global__ void __launch_bounds__(D)
+attend_combine_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml,
+                      int nsplit, int max_rows, int Hk, int Hq, int G,
+                      const uint16_t* __restrict__ Q, const uint16_t* __restrict__ tK,
+                      const uint16_t* __restrict__ tV, const int32_t* __restrict__ tlen,
+                      int tail_max, float scale_log2, float* __restrict__ out) {
+    __shared__ float x[D];
+    __shared__ float red[D / 32];
+    const int r = blockIdx.x, g = blockIdx.y, i = threadIdx.x;
+    const int a = r / G, h = g * G + r % G;
+
+    // merge the splits (log2 domain)
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < nsplit; ++s) {
+        const long long b = ((long long)g * nsplit + s) * max_rows + r;
+        if (part_ml[2 * b + 1] > 0.f) M = fmaxf(M, part_ml[2 * b]);
+    }
+    float L = 0.f, acc = 0.f;
+    for (int s = 0; s < nsplit; ++s) {
+        const long long b = ((long long)g * nsplit + s) * max_rows + r;
+        const float ls = part_ml[2 * b + 1];
+        if (ls > 0.f) {
+            const float w = exp2f(part_ml[2 * b] - M);
+            L += ls * w;
+            acc += part_acc[b * D + i] * w;
+        }
+    }
+    // inverse rotation: H acc / D
+    x[i] = acc;
+    __syncthreads();
+#pragma unroll
+    for (int hh = 1; hh < D; hh <<= 1) {
+        if (!(i & hh)) {
+            const float u = x[i], v = x[i + hh];
+            x[i] = u + v;
+            x[i + hh] = u - v;
+        }
+        __syncthreads();
+    }
+    const float Opool = x[i] * (1.0f / (float)D);
+
+    // private tail of agent a for kv head g
+    float mt = -CUDART_INF_F, lt = 0.f, Ot = 0.f;
+    if (tK != nullptr) {
+        const int n = min(max(tlen[a], 0), tail_max);  // never read past the tail buffers
+        const float q = bf2f(Q[((long long)a * Hq + h) * D + i]);
+        const long long tb = ((long long)a * Hk + g) * tail_max;
+        for (int t = 0; t < n; ++t) {
+            float part = warp_sum(q * bf2f(tK[(tb + t) * D + i]));
+            if ((i & 31) == 0) red[i / 32] = part;
+            __syncthreads();
+            float dot = 0.f;
+#pragma unroll
+            for (int w = 0; w < D / 32; ++w) dot += red[w];
+            __syncthreads();
+            const float lg = dot * scale_log2;
+            const float mnew = fmaxf(mt, lg);
+            const float corr = exp2f(mt - mnew), p = exp2f(lg - mnew);
+            lt = lt * corr + p;
+            Ot = Ot * corr + p * bf2f(tV[(tb + t) * D + i]);
+            mt = mnew;
+        }
+    }
+    const float Mf = fmaxf(M, mt);
+    const float wp = (L > 0.f) ? exp2f(M - Mf) : 0.f;
+    const float wt = (lt > 0.f) ? exp2f(mt - Mf) : 0.f;
+    out[((long long)a * Hq + h) * D + i] = (Opool * wp + Ot * wt) / (L * wp + lt * wt);
+}
+
+template <int D, int BITS>
+cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const AttendScratch& scr,
+                cudaStream_t st) {
+    const int ntile = (s.ctx + kTileTok - 1) / kTileTok;
+    const int per = (ntile + scr.nsplit - 1) / scr.nsplit;
+    const int tok_per_split = per * kTileTok;
+    const int nsplit = (s.ctx + tok_per_split - 1) / tok_per_split;
+    dim3 grid(nsplit, s.kv_heads, (a.rows + kRowsPerBlock - 1) / kRowsPerBlock);
+    attend_split_kernel<D, BITS><<<grid, kWarps * 32, 0, st>>>(
+        Lb.kq, Lb.vcodes, Lb.vnorm, Lb.kscale, s.ctx, s.ctx_pad, (const uint16_t*)a.Q, a.q_heads,
+        a.group, a.rows, a.scale_log2, tok_per_split, scr.acc, scr.ml, nsplit, scr.max_rows,
+        codebook(BITS));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    attend_combine_kernel<D><<<dim3(a.rows, s.kv_heads), D, 0, st>>>(
+        scr.acc, scr.ml, nsplit, scr.max_rows, s.kv_heads, a.q_heads, a.group,
+        (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len,
+        a.tail_max, a.scale_log2, a.out);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attend(const Shape& s, const LayerBufs& L, const AttendArgs& a,
+                          const AttendScratch& scr, int* status, cudaStream_t st) {
+    (void)status;
+    if (s.head_dim == 64) {
+        if (L.bits == 2) return run<64, 2>(s, L, a, scr, st);
+        if (L.bits == 3) return run<64, 3>(s, L, a, scr, st);
+        return run<64, 4>(s, L, a, scr, st);
+    }
+    if (L.bits == 2) return run<128, 2>(s, L, a, scr, st);
+    if (L.bits == 3) return run<128, 3>(s, L, a, scr, st);
+    return run<128, 4>(s, L, a, scr, st);
+}
+
+}  // namespace kvp

@@ -1,0 +1,397 @@
+// Host side of the C-ABI: argument validation, the write-once state of each
+// layer, the single device allocation of the pool, the library's own
+// Lloyd-Max table, status reporting.
+//
+// Memory layout of a pool (one cudaMalloc, every region 256-byte aligned):
+//   per layer l:  kq     int8  [Hk][ctx_pad][D]
+//                 vcodes uint8 [Hk][ctx_pad][D*bits_l/8]
+//                 vnorm  f32   [Hk][ctx_pad]
+//   kscale f32 [layers], kabsmax u32 [layers] (encode scratch),
+//   status int32, attention split scratch acc f32 [Hk][nsplit][max_rows][D]
+//   and ml f32 [Hk][nsplit][max_rows][2].
+// ctx_pad rounds the token axis up to a multiple of 128 so tiles never leave a
+// layer; the padding is zeroed once and never counted as tokens.
+#include <math.h>
+
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "kvpool_internal.cuh"
+
+// ----------------------------------------------------------- Lloyd-Max table
+namespace kvp {
+namespace {
+
+// N(0,1) density and upper tail (double precision: the table is rounded to
+// float32 in the end).
+double npdf(double x) { return exp(-0.5 * x * x) * 0.3989422804014327; }
+double ntail(double x) { return 0.5 * erfc(x * 0.7071067811865476); }
+
+// Lloyd-Max quantiser for N(0,1) with `levels` (even) outputs. N(0,1) is
+// symmetric, so only the positive half is solved, with cell edges 0 = e_0 <
+// e_1 < ... < e_K = inf (K = levels/2): iterate
+//   y_k = (pdf(e_{k-1}) - pdf(e_k)) / (tail(e_{k-1}) - tail(e_k)),
+//   e_k = (y_k + y_{k+1}) / 2
+// from equally spaced edges on [0, 3] until the edges stop moving.
+void lloyd_max(int levels, double* pos /* K outputs */) {
+    const int K = levels / 2;
+    double e[9];
+    e[0] = 0.0;
+    for (int k = 1; k < K; ++k) e[k] = 3.0 * k / K;
+    double y[8];
+    for (int it = 0; it < 20000; ++it) {
+        for (int k = 0; k < K; ++k) {
+            const double hi_pdf = (k + 1 < K) ? npdf(e[k + 1]) : 0.0;
+            const double hi_tail = (k + 1 < K) ? ntail(e[k + 1]) : 0.0;
+            y[k] = (npdf(e[k]) - hi_pdf) / (ntail(e[k]) - hi_tail);
+        }
+        double moved = 0.0;
+        for (int k = 1; k < K; ++k) {
+            const double ne = 0.5 * (y[k - 1] + y[k]);
+            moved = fmax(moved, fabs(ne - e[k]));
+            e[k] = ne;
+        }
+        if (moved == 0.0) break;
+    }
+    for (int k = 0; k < K; ++k) pos[k] = y[k];
+}
+
+Codebook g_books[5];
+std::once_flag g_books_once;
+
+void build_books() {
+    for (int bits = 2; bits <= 4; ++bits) {
+        Codebook& b = g_books[bits];
+        const int L = 1 << bits, K = L / 2;
+        double pos[8];
+        lloyd_max(L, pos);
+        double c[16];
+        for (int k = 0; k < K; ++k) {
+            c[K + k] = pos[k];
+            c[K - 1 - k] = -pos[k];
+        }
+        for (int k = 0; k < 16; ++k) b.c[k] = (k < L) ? (float)c[k] : 0.0f;
+        for (int k = 0; k < 16; ++k) b.m[k] = (k < L - 1) ? (float)(0.5 * (c[k] + c[k + 1])) : 0.0f;
+        b.levels = L;
+        b.bits = bits;
+    }
+}
+
+}  // namespace
+
+const Codebook& codebook(int bits) {
+    std::call_once(g_books_once, build_books);
+    return g_books[bits];
+}
+
+}  // namespace kvp
+
+// ---------------------------------------------------------------- the pool
+struct kvpool {
+    int layers = 0, kv_heads = 0, head_dim = 0, ctx = 0, ctx_pad = 0, max_rows = 0;
+    int nsplit = 1, device = 0;
+    std::vector<int> bits;
+    std::vector<size_t> off_kq, off_vc, off_vn;
+    std::vector<unsigned char> compressed;
+    unsigned char* base = nullptr;
+    size_t bytes = 0;
+    float* kscale = nullptr;
+    uint32_t* kabsmax = nullptr;
+    int* status = nullptr;
+    float* acc = nullptr;
+    float* ml = nullptr;
+
+    kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
+    kvp::LayerBufs layer(int l) const {
+        return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
+                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + l, bits[l]};
+    }
+};
+
+namespace {
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int map_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return KVPOOL_OK;
+    if (e == cudaErrorMemoryAllocation) return KVPOOL_ERR_OOM;
+    return KVPOOL_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int check_layer(const kvpool* p, int layer) {
+    if (!p || layer < 0 || layer >= p->layers) return KVPOOL_ERR_INVALID_ARG;
+    return KVPOOL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kvpool_codebook(int bits, float* centroids, float* midpoints) {
+    if (bits < 2 || bits > 4) return KVPOOL_ERR_INVALID_ARG;
+    const kvp::Codebook& b = kvp::codebook(bits);
+    for (int k = 0; k < b.levels; ++k) {
+        if (centroids) centroids[k] = b.c[k];
+        if (midpoints && k < b.levels - 1) midpoints[k] = b.m[k];
+    }
+    return KVPOOL_OK;
+}
+
+int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
+                  const uint8_t* bits_per_layer, int max_rows) {
+    if (!out) return KVPOOL_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (layers < 1 || kv_heads < 1 || ctx < 1 || (head_dim != 64 && head_dim != 128))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (max_rows == 0) max_rows = 512;
+    if (max_rows < 1 || max_rows > 1024) return KVPOOL_ERR_INVALID_ARG;
+    if ((long long)kv_heads * ctx > (1LL << 31) / 128) return KVPOOL_ERR_INVALID_ARG;
+    if (bits_per_layer)
+        for (int l = 0; l < layers; ++l)
+            if (bits_per_layer[l] < 2 || bits_per_layer[l] > 4) return KVPOOL_ERR_INVALID_ARG;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return KVPOOL_ERR_UNSUPPORTED;
+    cudaDeviceProp prop;
+    e = cudaGetDeviceProperties(&prop, dev);
+    if (e != cudaSuccess) return map_cuda(e);
+    if (prop.major * 10 + prop.minor != 103) return KVPOOL_ERR_UNSUPPORTED;
+
+    kvpool* p = new (std::nothrow) kvpool;
+    if (!p) return KVPOOL_ERR_OOM;
+    p->layers = layers;
+    p->kv_heads = kv_heads;
+    p->head_dim = head_dim;
+    p->ctx = ctx;
+    p->ctx_pad = (ctx + kvp::kTokenPad - 1) / kvp::kTokenPad * kvp::kTokenPad;
+    p->max_rows = max_rows;
+    p->device = dev;
+    const int ntile = (ctx + 31) / 32;
+    const int want = (2 * prop.multiProcessorCount + kv_heads - 1) / kv_heads;
+    p->nsplit = want < 1 ? 1 : (want > ntile ? ntile : want);
+    p->bits.resize(layers);
+    p->compressed.assign(layers, 0);
+    size_t off = 0;
+    const size_t nvec = (size_t)kv_heads * p->ctx_pad;
+    for (int l = 0; l < layers; ++l) {
+        p->bits[l] = bits_per_layer ? bits_per_layer[l] : 3;
+        p->off_kq.push_back(off);
+        off = align256(off + nvec * head_dim);
+        p->off_vc.push_back(off);
+        off = align256(off + nvec * head_dim * p->bits[l] / 8);
+        p->off_vn.push_back(off);
+        off = align256(off + nvec * 4);
+    }
+    const size_t off_scale = off;
+    off = align256(off + 4 * (size_t)layers);
+    const size_t off_absmax = off;
+    off = align256(off + 4 * (size_t)layers);
+    const size_t off_status = off;
+    off = align256(off + 4);
+    const size_t off_acc = off;
+    off = align256(off + 4 * (size_t)kv_heads * p->nsplit * max_rows * head_dim);
+    const size_t off_ml = off;
+    off = align256(off + 8 * (size_t)kv_heads * p->nsplit * max_rows);
+    p->bytes = off;
+    e = cudaMalloc(reinterpret_cast<void**>(&p->base), p->bytes);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        delete p;
+        return map_cuda(e);
+    }
+    e = cudaMemset(p->base, 0, p->bytes);
+    if (e != cudaSuccess) {
+        cudaFree(p->base);
+        delete p;
+        return map_cuda(e);
+    }
+    p->kscale = reinterpret_cast<float*>(p->base + off_scale);
+    p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
+    p->status = reinterpret_cast<int*>(p->base + off_status);
+    p->acc = reinterpret_cast<float*>(p->base + off_acc);
+    p->ml = reinterpret_cast<float*>(p->base + off_ml);
+    kvp::codebook(2);  // derive the tables now, not inside a stream capture
+    *out = p;
+    return KVPOOL_OK;
+}
+
+void kvpool_destroy(kvpool_t* p) {
+    if (!p) return;
+    cudaDeviceSynchronize();
+    cudaFree(p->base);
+    delete p;
+}
+
+int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!K || !V || !aligned16(K) || !aligned16(V)) return KVPOOL_ERR_INVALID_ARG;
+    if (p->compressed[layer]) return KVPOOL_ERR_STATE;
+    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return map_cuda(e);
+    p->compressed[layer] = 1;
+    return KVPOOL_OK;
+}
+
+int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads,
+                  const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!Q || !out || agents < 1 || q_heads < p->kv_heads || q_heads % p->kv_heads)
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(out)) return KVPOOL_ERR_INVALID_ARG;
+    if (!(softmax_scale >= 0.0f) || isinf(softmax_scale)) return KVPOOL_ERR_INVALID_ARG;
+    const int group = q_heads / p->kv_heads;
+    if ((long long)agents * group > p->max_rows) return KVPOOL_ERR_INVALID_ARG;
+    if (tail && (tail->T_max < 0 || (tail->T_max > 0 && (!tail->K || !tail->V || !tail->len))))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
+    kvp::AttendArgs a;
+    a.Q = Q;
+    a.agents = agents;
+    a.q_heads = q_heads;
+    a.group = group;
+    a.rows = agents * group;
+    const bool has_tail = tail && tail->T_max > 0;
+    a.tailK = has_tail ? tail->K : nullptr;
+    a.tailV = has_tail ? tail->V : nullptr;
+    a.tail_len = has_tail ? tail->len : nullptr;
+    a.tail_max = has_tail ? tail->T_max : 0;
+    a.out = out;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    kvp::AttendScratch scr{p->acc, p->ml, p->nsplit, p->max_rows};
+    cudaError_t e = kvp::launch_attend(p->shape(), p->layer(layer), a, scr, p->status,
+                                       static_cast<cudaStream_t>(stream));
+    return map_cuda(e);
+}
+
+int kvpool_decompress(kvpool_t* p, int layer, void* K_out, void* V_out, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if ((!K_out && !V_out) || !aligned16(K_out) || !aligned16(V_out)) return KVPOOL_ERR_INVALID_ARG;
+    if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
+    return map_cuda(kvp::launch_decompress(p->shape(), p->layer(layer), K_out, V_out,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+size_t kvpool_pool_bytes(const kvpool_t* p) {
+    if (!p) return 0;
+    size_t total = 0;
+    const size_t nvec = (size_t)p->kv_heads * p->ctx;
+    for (int l = 0; l < p->layers; ++l)
+        total += nvec * p->head_dim + nvec * p->head_dim * p->bits[l] / 8 + 4 * nvec + 4;
+    return total;
+}
+
+size_t kvpool_device_bytes(const kvpool_t* p) { return p ? p->bytes : 0; }
+
+int kvpool_status(kvpool_t* p, void* stream) {
+    if (!p) return KVPOOL_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return map_cuda(e);
+    int st = 0;
+    e = cudaMemcpy(&st, p->status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return map_cuda(e);
+    if (st) {
+        e = cudaMemset(p->status, 0, sizeof(int));
+        if (e != cudaSuccess) return map_cuda(e);
+    }
+    if (st & kvp::kStNonfinite) return KVPOOL_ERR_NONFINITE;
+    if (st & kvp::kStTimeout) return KVPOOL_ERR_TIMEOUT;
+    return KVPOOL_OK;
+}
+
+int kvpool_reset_layer(kvpool_t* p, int layer) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    p->compressed[layer] = 0;
+    return KVPOOL_OK;
+}
+
+int kvpool_layer_view(const kvpool_t* p, int layer, kvpool_layer_view_t* v) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!v) return KVPOOL_ERR_INVALID_ARG;
+    const kvp::LayerBufs L = p->layer(layer);
+    v->kq = L.kq;
+    v->vcodes = L.vcodes;
+    v->vnorm = L.vnorm;
+    v->kscale = L.kscale;
+    v->ctx = p->ctx;
+    v->ctx_padded = p->ctx_pad;
+    v->bits = L.bits;
+    v->compressed = p->compressed[layer];
+    return KVPOOL_OK;
+}
+
+namespace {
+
+// Move one layer between the padded pool layout and a dense caller layout.
+int copy_layer(const kvpool* p, int layer, bool to_pool, void* kq, void* vc, void* vn,
+               void* ks, cudaStream_t st) {
+    const kvp::LayerBufs L = p->layer(layer);
+    const size_t rows = (size_t)p->kv_heads;
+    const size_t kw = (size_t)p->ctx * p->head_dim, kp = (size_t)p->ctx_pad * p->head_dim;
+    const size_t vb = (size_t)p->head_dim * L.bits / 8;
+    const size_t vw = (size_t)p->ctx * vb, vp = (size_t)p->ctx_pad * vb;
+    const size_t nw = (size_t)p->ctx * 4, np_ = (size_t)p->ctx_pad * 4;
+    cudaError_t e = cudaSuccess;
+    if (kq && e == cudaSuccess)
+        e = to_pool ? cudaMemcpy2DAsync(L.kq, kp, kq, kw, kw, rows, cudaMemcpyDefault, st)
+                    : cudaMemcpy2DAsync(kq, kw, L.kq, kp, kw, rows, cudaMemcpyDefault, st);
+    if (vc && e == cudaSuccess)
+        e = to_pool ? cudaMemcpy2DAsync(L.vcodes, vp, vc, vw, vw, rows, cudaMemcpyDefault, st)
+                    : cudaMemcpy2DAsync(vc, vw, L.vcodes, vp, vw, rows, cudaMemcpyDefault, st);
+    if (vn && e == cudaSuccess)
+        e = to_pool ? cudaMemcpy2DAsync(L.vnorm, np_, vn, nw, nw, rows, cudaMemcpyDefault, st)
+                    : cudaMemcpy2DAsync(vn, nw, L.vnorm, np_, nw, rows, cudaMemcpyDefault, st);
+    if (ks && e == cudaSuccess)
+        e = to_pool ? cudaMemcpyAsync(L.kscale, ks, 4, cudaMemcpyDefault, st)
+                    : cudaMemcpyAsync(ks, L.kscale, 4, cudaMemcpyDefault, st);
+    return map_cuda(e);
+}
+
+}  // namespace
+
+int kvpool_export_layer(const kvpool_t* p, int layer, void* kq, void* vcodes, void* vnorm,
+                        void* kscale, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
+    return copy_layer(p, layer, false, kq, vcodes, vnorm, kscale, static_cast<cudaStream_t>(stream));
+}
+
+int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcodes,
+                        const void* vnorm, const void* kscale, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!kq || !vcodes || !vnorm || !kscale) return KVPOOL_ERR_INVALID_ARG;
+    if (p->compressed[layer]) return KVPOOL_ERR_STATE;
+    rc = copy_layer(p, layer, true, const_cast<void*>(kq), const_cast<void*>(vcodes),
+                    const_cast<void*>(vnorm), const_cast<void*>(kscale),
+                    static_cast<cudaStream_t>(stream));
+    if (rc == KVPOOL_OK) p->compressed[layer] = 1;
+    return rc;
+}
+
+const char* kvpool_strerror(int code) {
+    switch (code) {
+        case KVPOOL_OK: return "ok";
+        case KVPOOL_ERR_INVALID_ARG: return "invalid argument";
+        case KVPOOL_ERR_STATE: return "layer state: compress is write-once, attend/decompress need a compressed layer";
+        case KVPOOL_ERR_CUDA: return "CUDA runtime error";
+        case KVPOOL_ERR_OOM: return "device allocation failed";
+        case KVPOOL_ERR_NONFINITE: return "non-finite K maximum or V norm";
+        case KVPOOL_ERR_TIMEOUT: return "a bounded device wait expired";
+        case KVPOOL_ERR_UNSUPPORTED: return "unsupported device or shape (needs sm_103)";
+        default: return "unknown error";
+    }
+}
+
+}  // extern "C"

@@ -1,0 +1,72 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kvpool.h"
+
+namespace kvp {
+
+// The token axis of every pool layer is padded to a multiple of this.
+constexpr int kTokenPad = 128;
+
+// Device status bits (kernels OR them in; the host maps them to error codes).
+enum : int { kStNonfinite = 1, kStTimeout = 2 };
+
+// Float32 Lloyd-Max table of one V bit width, passed to kernels by value.
+struct Codebook {
+    float c[16];  // centroids, ascending (levels used)
+    float m[16];  // midpoints (levels - 1 used)
+    int levels;
+    int bits;
+};
+
+// Host: the library's own table for `bits` in {2,3,4} (derived once).
+const Codebook& codebook(int bits);
+
+// Device buffers of one layer.
+struct LayerBufs {
+    int8_t* kq;        // [Hk][ctx_pad][D]
+    uint8_t* vcodes;   // [Hk][ctx_pad][D*bits/8]
+    float* vnorm;      // [Hk][ctx_pad]
+    float* kscale;     // 1 float
+    uint32_t* kabsmax; // 1 word: bf16 bits of max|K| (scratch of the encode)
+    int bits;
+};
+
+struct Shape {
+    int kv_heads, head_dim, ctx, ctx_pad;
+};
+
+// ---- encode (write-once compress of one layer)
+cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
+                          int* status, cudaStream_t st);
+
+// ---- decompress
+cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out,
+                              cudaStream_t st);
+
+// ---- attend
+struct AttendArgs {
+    const void* Q;       // bf16 [A][Hq][D]
+    int agents, q_heads, group, rows;  // rows = agents * group
+    const void* tailK;   // bf16 [A][Hk][T_max][D] or null
+    const void* tailV;
+    const int32_t* tail_len;
+    int tail_max;
+    float* out;          // f32 [A][Hq][D]
+    float scale_log2;    // softmax scale * log2(e)
+};
+
+struct AttendScratch {
+    float* acc;   // [Hk][nsplit][max_rows][D]
+    float* ml;    // [Hk][nsplit][max_rows][2]
+    int nsplit;
+    int max_rows;
+};
+
+cudaError_t launch_attend(const Shape& s, const LayerBufs& L, const AttendArgs& a,
+                          const AttendScratch& scr, int* status, cudaStream_t st);
+
+}  // namespace kvp

@@ -1,0 +1,233 @@
+"""ctypes binding of ``libkvpool.so`` (argument marshalling only).
+
+Every step of the path runs in the library's CUDA kernels; this module only
+turns torch tensors into device pointers and the current torch stream into a
+``cudaStream_t``. There is no fallback: if the library is missing or the
+device is not an sm_103 GPU the calls raise.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libkvpool.so")
+
+OK = 0
+ERRORS = {
+    -1: "INVALID_ARG", -2: "STATE", -3: "CUDA", -4: "OOM", -5: "NONFINITE", -6: "TIMEOUT",
+    -7: "UNSUPPORTED",
+}
+
+
+class KVPoolError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({_lib().kvpool_strerror(code).decode()})")
+
+
+class Tail(ctypes.Structure):
+    _fields_ = [("K", ctypes.c_void_p), ("V", ctypes.c_void_p), ("len", ctypes.c_void_p),
+                ("T_max", ctypes.c_int)]
+
+
+class LayerView(ctypes.Structure):
+    _fields_ = [("kq", ctypes.c_void_p), ("vcodes", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
+                ("kscale", ctypes.c_void_p), ("ctx", ctypes.c_int), ("ctx_padded", ctypes.c_int),
+                ("bits", ctypes.c_int), ("compressed", ctypes.c_int)]
+
+
+_LIB = None
+
+# name -> (restype, argtypes); the C declarations are in include/kvpool.h
+_SIGS = {
+    "kvpool_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]),
+    "kvpool_destroy": (None, [ctypes.c_void_p]),
+    "kvpool_compress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_attend": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_float, ctypes.c_void_p]),
+    "kvpool_decompress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                         ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_pool_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
+    "kvpool_device_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
+    "kvpool_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_reset_layer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "kvpool_layer_view": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.POINTER(LayerView)]),
+    "kvpool_codebook": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_export_layer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
+    "kvpool_import_layer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
+    "kvpool_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+}
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m shared_quantized_kv_gb300.build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = lib
+    return _LIB
+
+
+def lib():
+    """The loaded library (ctypes.CDLL)."""
+    return _lib()
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise KVPoolError(rc, what)
+
+
+def _stream_ptr(stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _dev_ptr(t, dtype, name):
+    import torch
+
+    if t is None:
+        return None
+    if not t.is_cuda or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CUDA tensor of {dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def codebook(bits: int):
+    """The library's float32 (centroids, midpoints) for ``bits`` (host)."""
+    import numpy as np
+
+    c = np.zeros(1 << bits, np.float32)
+    m = np.zeros((1 << bits) - 1, np.float32)
+    _check(_lib().kvpool_codebook(bits, c.ctypes.data, m.ctypes.data), "kvpool_codebook")
+    return c, m
+
+
+class KVPool:
+    """One shared pool (a ``kvpool_t``) on the current CUDA device."""
+
+    def __init__(self, layers, kv_heads, head_dim, ctx, bits=None, max_rows=0):
+        self.layers, self.kv_heads, self.head_dim, self.ctx = layers, kv_heads, head_dim, ctx
+        self.bits = list(bits) if bits is not None else [3] * layers
+        arr = (ctypes.c_uint8 * layers)(*self.bits)
+        h = ctypes.c_void_p()
+        _check(_lib().kvpool_create(ctypes.byref(h), layers, kv_heads, head_dim, ctx,
+                                    ctypes.cast(arr, ctypes.c_void_p), max_rows), "kvpool_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None):
+            _lib().kvpool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def compress(self, layer, K, V, stream=None):
+        import torch
+
+        _check(_lib().kvpool_compress(self._h, layer, _dev_ptr(K, torch.bfloat16, "K"),
+                                      _dev_ptr(V, torch.bfloat16, "V"), _stream_ptr(stream)),
+               "kvpool_compress")
+
+    def attend(self, layer, Q, out=None, tail=None, softmax_scale=0.0, stream=None):
+        """Q: bf16 [agents, q_heads, d]; tail: None or (K, V, lens) with K, V
+        bf16 [agents, kv_heads, T_max, d] and lens int32 [agents] (device).
+        Returns out: float32 [agents, q_heads, d]."""
+        import torch
+
+        A, Hq, d = Q.shape
+        if out is None:
+            out = torch.empty((A, Hq, d), dtype=torch.float32, device=Q.device)
+        tp = None
+        if tail is not None:
+            Kt, Vt, lens = tail
+            self._tail = Tail(_dev_ptr(Kt, torch.bfloat16, "tail K").value,
+                              _dev_ptr(Vt, torch.bfloat16, "tail V").value,
+                              _dev_ptr(lens, torch.int32, "tail len").value, Kt.shape[2])
+            tp = ctypes.byref(self._tail)
+        _check(_lib().kvpool_attend(self._h, layer, _dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, tp,
+                                    _dev_ptr(out, torch.float32, "out"), softmax_scale,
+                                    _stream_ptr(stream)), "kvpool_attend")
+        return out
+
+    def decompress(self, layer, K_out=None, V_out=None, stream=None):
+        import torch
+
+        shape = (self.kv_heads, self.ctx, self.head_dim)
+        dev = torch.device("cuda", torch.cuda.current_device())
+        if K_out is None:
+            K_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        if V_out is None:
+            V_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+        _check(_lib().kvpool_decompress(self._h, layer, _dev_ptr(K_out, torch.bfloat16, "K_out"),
+                                        _dev_ptr(V_out, torch.bfloat16, "V_out"),
+                                        _stream_ptr(stream)), "kvpool_decompress")
+        return K_out, V_out
+
+    def pool_bytes(self) -> int:
+        return int(_lib().kvpool_pool_bytes(self._h))
+
+    def device_bytes(self) -> int:
+        return int(_lib().kvpool_device_bytes(self._h))
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return (and clear) the device status code."""
+        return int(_lib().kvpool_status(self._h, _stream_ptr(stream)))
+
+    def reset_layer(self, layer):
+        _check(_lib().kvpool_reset_layer(self._h, layer), "kvpool_reset_layer")
+
+    def layer_view(self, layer) -> LayerView:
+        v = LayerView()
+        _check(_lib().kvpool_layer_view(self._h, layer, ctypes.byref(v)), "kvpool_layer_view")
+        return v
+
+    def export_layer(self, layer, stream=None):
+        """The layer's stored bytes as device tensors (token padding removed):
+        kq int8 [Hk, ctx, d], vcodes uint8 [Hk, ctx, d*bits/8], vnorm float32
+        [Hk, ctx], kscale float32 [1]."""
+        import torch
+
+        bits = self.bits[layer]
+        dev = torch.device("cuda", torch.cuda.current_device())
+        Hk, T, d = self.kv_heads, self.ctx, self.head_dim
+        kq = torch.empty((Hk, T, d), dtype=torch.int8, device=dev)
+        vc = torch.empty((Hk, T, d * bits // 8), dtype=torch.uint8, device=dev)
+        vn = torch.empty((Hk, T), dtype=torch.float32, device=dev)
+        ks = torch.empty(1, dtype=torch.float32, device=dev)
+        _check(_lib().kvpool_export_layer(self._h, layer, kq.data_ptr(), vc.data_ptr(),
+                                          vn.data_ptr(), ks.data_ptr(), _stream_ptr(stream)),
+               "kvpool_export_layer")
+        return kq, vc, vn, ks
+
+    def import_layer(self, layer, kq, vcodes, vnorm, kscale, stream=None):
+        _check(_lib().kvpool_import_layer(self._h, layer, kq.data_ptr(), vcodes.data_ptr(),
+                                          vnorm.data_ptr(), kscale.data_ptr(),
+                                          _stream_ptr(stream)), "kvpool_import_layer")
+
+    def read_layer(self, layer):
+        """Host numpy copies of one layer's stored bytes (see export_layer)."""
+        kq, vc, vn, ks = self.export_layer(layer)
+        return dict(kq=kq.cpu().numpy(), vcodes=vc.cpu().numpy(), vnorm=vn.cpu().numpy(),
+                    kscale=ks.cpu().numpy()[0])
