@@ -144,6 +144,37 @@ int kvpool_reset_layer(kvpool_t* pool, int layer);
 /* Fill *view with the device pointers and sizes of one layer. */
 int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view);
 
+/* Allocation-free variant of kvpool_attend, for callers that cannot call
+ * cudaMalloc: an engine that reserved all device memory up front and hands
+ * out slices itself (a cudaMalloc would fail or break its accounting), or a
+ * latency-critical caller that cannot afford the device-wide synchronisation
+ * cudaMalloc implies. The pages have no counterpart; this is an interface
+ * convenience only.
+ *
+ * Inputs and outputs are the caller's: one compressed layer in the pool's
+ * layout (as kvpool_layer_view describes it, token axis padded to
+ * ctx_padded = ctx rounded up to a multiple of 128): kq int8
+ * [kv_heads][ctx_padded][head_dim], vcodes uint8 [kv_heads][ctx_padded]
+ * [head_dim*bits/8], vnorm float [kv_heads][ctx_padded], kscale one float;
+ * Q, tail, out, softmax_scale and stream as in kvpool_attend. The result
+ * equals kvpool_attend's on the same layer within float rounding.
+ *
+ * The split-context scratch is a fixed 8 MiB array inside the library, held
+ * by every GPU that loads it until the process exits. A call needs
+ * kv_heads * agents * (q_heads/kv_heads) * (head_dim + 2) * 4 bytes of it
+ * per context split; calls that do not fit even one split (or with more than
+ * 4096 query rows per KV head) return KVPOOL_ERR_INVALID_ARG. The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress with
+ * that device current); make that first call before any stream capture. All
+ * calls share the one array, so calls that overlap on the GPU (different
+ * streams, or other host threads) race and must be serialised by the caller;
+ * every byte a call reads from the array it has written first. Returns
+ * KVPOOL_ERR_UNSUPPORTED on a device other than sm_103. */
+int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, const float* vnorm,
+                          const float* kscale, int kv_heads, int head_dim, int ctx, int bits,
+                          const void* Q, int agents, int q_heads, const kvpool_tail_t* tail,
+                          float* out, float softmax_scale, void* stream);
+
 /* Copy the stored bytes of one compressed layer, token padding removed, to
  * caller buffers in host or device memory (any of the four may be NULL):
  * kq int8 [kv_heads][ctx][head_dim], vcodes uint8 [kv_heads][ctx][head_dim*
