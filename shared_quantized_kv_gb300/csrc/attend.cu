@@ -245,9 +245,8 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
 
 }  // namespace
 
-cudaError_t launch_attend(const Shape& s, const LayerBufs& L, const AttendArgs& a,
-                          const AttendScratch& scr, int* status, cudaStream_t st) {
-    (void)status;
+cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const AttendArgs& a,
+                                const AttendScratch& scr, cudaStream_t st) {
     if (s.head_dim == 64) {
         if (L.bits == 2) return run<64, 2>(s, L, a, scr, st);
         if (L.bits == 3) return run<64, 3>(s, L, a, scr, st);

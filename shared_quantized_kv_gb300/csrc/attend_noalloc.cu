@@ -99,7 +99,8 @@ extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, co
 
     kvp::Shape shape{kv_heads, head_dim, ctx, (ctx + kvp::kTokenPad - 1) / kvp::kTokenPad * kvp::kTokenPad};
     kvp::LayerBufs layer{const_cast<int8_t*>(kq), const_cast<uint8_t*>(vcodes),
-                         const_cast<float*>(vnorm), const_cast<float*>(kscale), nullptr, bits};
+                         const_cast<float*>(vnorm), const_cast<float*>(kscale), nullptr, bits,
+                         nullptr};
     kvp::AttendArgs a;
     a.Q = Q;
     a.agents = agents;
@@ -115,6 +116,6 @@ extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, co
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
     const cudaError_t e =
-        kvp::launch_attend(shape, layer, a, scr, nullptr, static_cast<cudaStream_t>(stream));
+        kvp::launch_attend_split(shape, layer, a, scr, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? KVPOOL_OK : KVPOOL_ERR_CUDA;
 }

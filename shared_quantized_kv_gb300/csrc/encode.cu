@@ -36,7 +36,8 @@ template <int D, int BITS>
 __global__ void __launch_bounds__(kEncThreads)
 encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, int nvec, int ctx,
                      int ctx_pad, uint8_t* __restrict__ vcodes, float* __restrict__ vnorm,
-                     uint32_t* __restrict__ kabsmax, int* __restrict__ status, Codebook cb) {
+                     uint32_t* __restrict__ kabsmax, uint32_t* __restrict__ vnmax,
+                     int* __restrict__ status, Codebook cb) {
     constexpr int CH = D / 8;          // 16-byte chunks per head-vector
     constexpr int ROW = D * 2 + 16;    // padded shared-memory row: conflict-free 16-byte reads
     constexpr int L = 1 << BITS;
@@ -70,7 +71,7 @@ encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, i
     __syncthreads();
 
     const long long v = v0 + tid;
-    if (v >= nvec) return;
+    const bool live = v < nvec;
     const unsigned char* row = srow + tid * ROW;
 
     // 2. norm: sq_i = v_i^2 + v_{i+D/2}^2 (first tree level), then halves
@@ -94,6 +95,10 @@ encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, i
         for (int i = 0; i < w; ++i) s[i] = __fadd_rn(s[i], s[i + w]);
     }
     const float n = __fsqrt_rn(s[0]);
+    // largest norm of the layer (non-negative floats order like their bits)
+    const uint32_t nmax = __reduce_max_sync(0xffffffffu, __float_as_uint(n));
+    if ((tid & 31) == 0 && nmax) atomicMax(vnmax, nmax);
+    if (!live) return;
 
     // 3. FWHT in registers, stages h = 1, 2, ..., D/2, lower index first
     float x[D];
@@ -190,10 +195,12 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     const long long nvec = (long long)s.kv_heads * s.ctx;
     cudaError_t e = cudaMemsetAsync(L.kabsmax, 0, sizeof(uint32_t), st);
     if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
     const unsigned grid_v = (unsigned)((nvec + kEncThreads - 1) / kEncThreads);
     encode_v_kmax_kernel<D, BITS><<<grid_v, kEncThreads, 0, st>>>(
         (const uint4*)K, (const uint4*)V, (int)nvec, s.ctx, s.ctx_pad, L.vcodes, L.vnorm,
-        L.kabsmax, status, codebook(BITS));
+        L.kabsmax, L.vnmax, status, codebook(BITS));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const long long n16 = nvec * D / 16;
@@ -203,7 +210,28 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     return cudaGetLastError();
 }
 
+__global__ void __launch_bounds__(256)
+norm_max_kernel(const float* __restrict__ vnorm, int kv_heads, int ctx, int ctx_pad,
+                uint32_t* __restrict__ vnmax) {
+    uint32_t m = 0;
+    const long long n = (long long)kv_heads * ctx;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long h = i / ctx, t = i - h * ctx;
+        m = max(m, __float_as_uint(fabsf(vnorm[h * ctx_pad + t])));
+    }
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0 && m) atomicMax(vnmax, m);
+}
+
 }  // namespace
+
+cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st);
+    if (e != cudaSuccess) return e;
+    norm_max_kernel<<<64, 256, 0, st>>>(L.vnorm, s.kv_heads, s.ctx, s.ctx_pad, L.vnmax);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
                           int* status, cudaStream_t st) {

@@ -6,12 +6,14 @@
 //   per layer l:  kq     int8  [Hk][ctx_pad][D]
 //                 vcodes uint8 [Hk][ctx_pad][D*bits_l/8]
 //                 vnorm  f32   [Hk][ctx_pad]
-//   kscale f32 [layers], kabsmax u32 [layers] (encode scratch),
-//   status int32, attention split scratch acc f32 [Hk][nsplit][max_rows][D]
-//   and ml f32 [Hk][nsplit][max_rows][2].
+//   kscale f32 [layers], kabsmax u32 [layers] (encode scratch), vnmax u32
+//   [layers] (largest V norm, float bits), status int32.
+// Attention needs no scratch: the CTAs of a cluster merge their context
+// splits through distributed shared memory.
 // ctx_pad rounds the token axis up to a multiple of 128 so tiles never leave a
 // layer; the padding is zeroed once and never counted as tokens.
 #include <math.h>
+#include <string.h>
 
 #include <mutex>
 #include <new>
@@ -57,6 +59,49 @@ void lloyd_max(int levels, double* pos /* K outputs */) {
     for (int k = 0; k < K; ++k) pos[k] = y[k];
 }
 
+// float -> fp16 bits, round to nearest even (normal range; the table values
+// are between 0.1 and 6)
+uint16_t half_bits(float f) {
+    uint32_t x;
+    memcpy(&x, &f, 4);
+    const uint32_t sign = (x >> 16) & 0x8000u;
+    const int e = (int)((x >> 23) & 0xFF) - 127 + 15;
+    uint32_t mant = x & 0x7FFFFFu;
+    if (e <= 0 || e >= 31) return (uint16_t)sign;  // not reached for the table
+    uint32_t h = ((uint32_t)e << 10) | (mant >> 13);
+    const uint32_t rest = mant & 0x1FFFu;
+    if (rest > 0x1000u || (rest == 0x1000u && (h & 1))) ++h;
+    return (uint16_t)(sign | h);
+}
+double half_value(uint16_t h) {
+    const int e = (h >> 10) & 0x1F;
+    const double m = (double)(h & 0x3FF);
+    const double v = ldexp(1.0 + m / 1024.0, e - 15);
+    return (h & 0x8000) ? -v : v;
+}
+
+// Scale lam in [1, 2) minimising the largest relative fp16 rounding error of
+// lam * c over the positive centroids (the table is antisymmetric).
+float pick_lambda(const double* c, int L) {
+    double best = 1e30;
+    float best_lam = 1.0f;
+    for (int i = 0; i < (1 << 20); ++i) {
+        const float lam = 1.0f + (float)i / (float)(1 << 20);
+        double worst = 0.0;
+        for (int k = L / 2; k < L; ++k) {
+            const double v = (double)(float)((double)lam * c[k]);
+            const double e = fabs(half_value(half_bits((float)v)) - (double)lam * c[k]) / ((double)lam * c[k]);
+            if (e > worst) worst = e;
+            if (worst >= best) break;
+        }
+        if (worst < best) {
+            best = worst;
+            best_lam = lam;
+        }
+    }
+    return best_lam;
+}
+
 Codebook g_books[5];
 std::once_flag g_books_once;
 
@@ -75,6 +120,9 @@ void build_books() {
         for (int k = 0; k < 16; ++k) b.m[k] = (k < L - 1) ? (float)(0.5 * (c[k] + c[k + 1])) : 0.0f;
         b.levels = L;
         b.bits = bits;
+        b.lam = pick_lambda(c, L);
+        for (int k = 0; k < 16; ++k)
+            b.c16[k] = (k < L) ? half_bits((float)((double)b.lam * c[k])) : (uint16_t)0;
     }
 }
 
@@ -90,7 +138,7 @@ const Codebook& codebook(int bits) {
 // ---------------------------------------------------------------- the pool
 struct kvpool {
     int layers = 0, kv_heads = 0, head_dim = 0, ctx = 0, ctx_pad = 0, max_rows = 0;
-    int nsplit = 1, device = 0;
+    int device = 0, sm_count = 0;
     std::vector<int> bits;
     std::vector<size_t> off_kq, off_vc, off_vn;
     std::vector<unsigned char> compressed;
@@ -98,14 +146,14 @@ struct kvpool {
     size_t bytes = 0;
     float* kscale = nullptr;
     uint32_t* kabsmax = nullptr;
+    uint32_t* vnmax = nullptr;
     int* status = nullptr;
-    float* acc = nullptr;
-    float* ml = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
-                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + l, bits[l]};
+                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + l, bits[l],
+                vnmax + l};
     }
 };
 
@@ -170,9 +218,7 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     p->ctx_pad = (ctx + kvp::kTokenPad - 1) / kvp::kTokenPad * kvp::kTokenPad;
     p->max_rows = max_rows;
     p->device = dev;
-    const int ntile = (ctx + 31) / 32;
-    const int want = (2 * prop.multiProcessorCount + kv_heads - 1) / kv_heads;
-    p->nsplit = want < 1 ? 1 : (want > ntile ? ntile : want);
+    p->sm_count = prop.multiProcessorCount;
     p->bits.resize(layers);
     p->compressed.assign(layers, 0);
     size_t off = 0;
@@ -190,12 +236,10 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     off = align256(off + 4 * (size_t)layers);
     const size_t off_absmax = off;
     off = align256(off + 4 * (size_t)layers);
+    const size_t off_vnmax = off;
+    off = align256(off + 4 * (size_t)layers);
     const size_t off_status = off;
     off = align256(off + 4);
-    const size_t off_acc = off;
-    off = align256(off + 4 * (size_t)kv_heads * p->nsplit * max_rows * head_dim);
-    const size_t off_ml = off;
-    off = align256(off + 8 * (size_t)kv_heads * p->nsplit * max_rows);
     p->bytes = off;
     e = cudaMalloc(reinterpret_cast<void**>(&p->base), p->bytes);
     if (e != cudaSuccess) {
@@ -211,9 +255,8 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     }
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
+    p->vnmax = reinterpret_cast<uint32_t*>(p->base + off_vnmax);
     p->status = reinterpret_cast<int*>(p->base + off_status);
-    p->acc = reinterpret_cast<float*>(p->base + off_acc);
-    p->ml = reinterpret_cast<float*>(p->base + off_ml);
     kvp::codebook(2);  // derive the tables now, not inside a stream capture
     *out = p;
     return KVPOOL_OK;
@@ -250,6 +293,9 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     if ((long long)agents * group > p->max_rows) return KVPOOL_ERR_INVALID_ARG;
     if (tail && (tail->T_max < 0 || (tail->T_max > 0 && (!tail->K || !tail->V || !tail->len))))
         return KVPOOL_ERR_INVALID_ARG;
+    if (tail && tail->T_max > 0 && (!aligned16(tail->K) || !aligned16(tail->V) ||
+                                    (reinterpret_cast<uintptr_t>(tail->len) & 3)))
+        return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
     kvp::AttendArgs a;
     a.Q = Q;
@@ -265,9 +311,8 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     a.out = out;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
-    kvp::AttendScratch scr{p->acc, p->ml, p->nsplit, p->max_rows};
-    cudaError_t e = kvp::launch_attend(p->shape(), p->layer(layer), a, scr, p->status,
-                                       static_cast<cudaStream_t>(stream));
+    cudaError_t e = kvp::launch_attend_tc(p->shape(), p->layer(layer), a, p->status, p->sm_count,
+                                          static_cast<cudaStream_t>(stream));
     return map_cuda(e);
 }
 
@@ -376,6 +421,8 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
     rc = copy_layer(p, layer, true, const_cast<void*>(kq), const_cast<void*>(vcodes),
                     const_cast<void*>(vnorm), const_cast<void*>(kscale),
                     static_cast<cudaStream_t>(stream));
+    if (rc != KVPOOL_OK) return rc;
+    rc = map_cuda(kvp::launch_norm_max(p->shape(), p->layer(layer), static_cast<cudaStream_t>(stream)));
     if (rc == KVPOOL_OK) p->compressed[layer] = 1;
     return rc;
 }

@@ -20,6 +20,11 @@ struct Codebook {
     float m[16];  // midpoints (levels - 1 used)
     int levels;
     int bits;
+    // Tensor-core operand table: fp16 bits of lam * c[k]. The scale lam in
+    // [1, 2) is chosen so that every lam * c[k] lies as close as possible to
+    // an fp16 value (the attention kernel divides its output by lam).
+    uint16_t c16[16];
+    float lam;
 };
 
 // Host: the library's own table for `bits` in {2,3,4} (derived once).
@@ -33,6 +38,7 @@ struct LayerBufs {
     float* kscale;     // 1 float
     uint32_t* kabsmax; // 1 word: bf16 bits of max|K| (scratch of the encode)
     int bits;
+    uint32_t* vnmax;   // 1 word: float bits of the largest V norm of the layer
 };
 
 struct Shape {
@@ -66,7 +72,15 @@ struct AttendScratch {
     int max_rows;
 };
 
-cudaError_t launch_attend(const Shape& s, const LayerBufs& L, const AttendArgs& a,
-                          const AttendScratch& scr, int* status, cudaStream_t st);
+// CUDA-core split-context attention with partials in `scr` (any device memory).
+cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const AttendArgs& a,
+                                const AttendScratch& scr, cudaStream_t st);
+
+// Tensor-core cluster attention (no scratch memory).
+cudaError_t launch_attend_tc(const Shape& s, const LayerBufs& L, const AttendArgs& a, int* status,
+                             int sm_count, cudaStream_t st);
+
+// Largest V norm of a layer (for layers loaded with kvpool_import_layer).
+cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st);
 
 }  // namespace kvp
