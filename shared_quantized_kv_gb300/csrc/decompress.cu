@@ -6,10 +6,12 @@
 // H / d). This is the per-agent baseline path that direct attention over the
 // pool avoids.
 //
-//   decompress_v: one thread per head-vector: unpack the codes, look the
-//     centroids up in a shared-memory table, FWHT in registers in the encoder's
-//     stage order, V_i = bf16(fl(fl(z_i * n) * (1/d))), 16-byte stores.
-//   decompress_k: K = bf16(fl(q * s)), 16 elements per thread.
+// One kernel, grid (blocks, kv heads):
+//   V blocks: D/32 threads per head-vector, 32 coordinates each: unpack the
+//     slice's codes, look the centroids up in a shared-memory table, FWHT in
+//     the encoder's stage order (h < 32 in registers, h = 32, 64 by
+//     shfl.xor), V_i = bf16(fl(fl(z_i * n) * (1/d))), coalesced 16-byte stores.
+//   K blocks: K = bf16(fl(q * s)), 16 elements per thread.
 #include <cuda_bf16.h>
 
 #include "kvpool_internal.cuh"
@@ -17,52 +19,73 @@
 namespace kvp {
 namespace {
 
+constexpr int kDecThreads = 256;
+
 __device__ __forceinline__ uint32_t bf16_bits(float f) {
     return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// One launch for both halves, grid (blocks, kv heads): the first nbv blocks of
+// each head materialise V (D/32 threads per head-vector), the rest K (16
+// elements per thread).
 template <int D, int BITS>
-__global__ void __launch_bounds__(128)
-decompress_v_kernel(const uint8_t* __restrict__ vcodes, const float* __restrict__ vnorm, int nvec,
-                    int ctx, int ctx_pad, uint4* __restrict__ Vout, Codebook cb) {
+__global__ void __launch_bounds__(kDecThreads)
+decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscale,
+                  const uint8_t* __restrict__ vcodes, const float* __restrict__ vnorm, int ctx,
+                  int ctx_pad, int nbv, uint4* __restrict__ Kout, uint4* __restrict__ Vout,
+                  Codebook cb) {
+    constexpr int TPV = D / 32;
     constexpr int VB = D * BITS / 8;
-    constexpr int NW = VB / 4;
+    constexpr int TB = 4 * BITS;
     constexpr uint32_t MASK = (1u << BITS) - 1;
+    const int tid = threadIdx.x;
+    const long long head = blockIdx.y;
+    if ((int)blockIdx.x >= nbv) {
+        // ---- K = bf16(q * s)
+        const float s = *kscale;
+        const int g = (blockIdx.x - nbv) * kDecThreads + tid;  // 16-element group in the head
+        if (g >= ctx * (D / 16)) return;
+        const int t = g / (D / 16), c = g % (D / 16);
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(kq + (head * ctx_pad + t) * D + c * 16));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int b0 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2))) & 0xFF);
+            const int b1 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2) + 8)) & 0xFF);
+            o[j] = bf16_bits(__fmul_rn((float)b0, s)) | (bf16_bits(__fmul_rn((float)b1, s)) << 16);
+        }
+        uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
+        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        return;
+    }
+    // ---- V = bf16(fl(fl(z * n) * (1/d))), z = FWHT(c[codes])
     __shared__ float cen[16];
-    if (threadIdx.x < 16) cen[threadIdx.x] = cb.c[threadIdx.x];
+    if (tid < 16) cen[tid] = cb.c[tid];
     __syncthreads();
-    const long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (v >= nvec) return;
-    const long long head = v / ctx, t = v - head * ctx;
-    const long long src = head * ctx_pad + t;
-
-    uint32_t words[NW];
-    const uint8_t* in = vcodes + src * VB;
-    if constexpr (VB % 16 == 0) {
+    const int lt = tid % TPV;
+    const int t = blockIdx.x * (kDecThreads / TPV) + tid / TPV;
+    const bool live = t < ctx;
+    const unsigned gmask = 0xffffffffu;
+    const long long src = head * ctx_pad + (live ? t : 0);
+    uint32_t words[BITS + 1];
+    const uint32_t* in = reinterpret_cast<const uint32_t*>(vcodes + src * VB + lt * TB);
 #pragma unroll
-        for (int q = 0; q < VB / 16; ++q) {
-            const uint4 u = __ldg(reinterpret_cast<const uint4*>(in) + q);
-            words[4 * q] = u.x; words[4 * q + 1] = u.y; words[4 * q + 2] = u.z; words[4 * q + 3] = u.w;
-        }
-    } else {
+    for (int w = 0; w < BITS; ++w) words[w] = live ? __ldg(in + w) : 0u;
+    words[BITS] = 0;
+    const float n = live ? __ldg(vnorm + src) : 0.f;
+    float x[32];
 #pragma unroll
-        for (int q = 0; q < VB / 8; ++q) {
-            const uint2 u = __ldg(reinterpret_cast<const uint2*>(in) + q);
-            words[2 * q] = u.x; words[2 * q + 1] = u.y;
-        }
-    }
-    float x[D];
-#pragma unroll
-    for (int i = 0; i < D; ++i) {
+    for (int i = 0; i < 32; ++i) {
         const int bit = i * BITS, w = bit / 32, off = bit % 32;
-        uint32_t code = words[w] >> off;
-        if (off + BITS > 32) code |= words[w + 1] << (32 - off);
-        x[i] = cen[code & MASK];
+        const uint32_t code = __funnelshift_r(words[w], words[w + 1], off) & MASK;
+        x[i] = cen[code];
     }
 #pragma unroll
-    for (int h = 1; h < D; h <<= 1) {
+    for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < D; ++i) {
+        for (int i = 0; i < 32; ++i) {
             if (!(i & h)) {
                 const float a = x[i], b = x[i + h];
                 x[i] = __fadd_rn(a, b);
@@ -70,11 +93,21 @@ decompress_v_kernel(const uint8_t* __restrict__ vcodes, const float* __restrict_
             }
         }
     }
-    const float n = __ldg(vnorm + src);
-    const float inv_d = 1.0f / (float)D;  // a power of two: exact
-    uint4* out = Vout + v * (D / 8);
 #pragma unroll
-    for (int q = 0; q < D / 8; ++q) {
+    for (int h = 32; h < D; h <<= 1) {
+        const int off = h / 32;
+        const bool upper = (lt & off) != 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
+            x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+        }
+    }
+    if (!live) return;
+    const float inv_d = 1.0f / (float)D;  // a power of two: exact
+    uint4* out = Vout + (head * ctx + t) * (D / 8) + lt * 4;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -86,45 +119,16 @@ decompress_v_kernel(const uint8_t* __restrict__ vcodes, const float* __restrict_
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(256)
-decompress_k_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscale, long long n16,
-                    int ctx, int ctx_pad, uint4* __restrict__ Kout) {
-    const float s = *kscale;
-    for (long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x; g < n16;
-         g += (long long)gridDim.x * blockDim.x) {
-        const long long e = g * 16, vec = e / D;
-        const long long head = vec / ctx, t = vec - head * ctx;
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(kq + (head * ctx_pad + t) * D + (e % D)));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        uint32_t o[8];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int b0 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2))) & 0xFF);
-            const int b1 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2) + 8)) & 0xFF);
-            o[j] = bf16_bits(__fmul_rn((float)b0, s)) | (bf16_bits(__fmul_rn((float)b1, s)) << 16);
-        }
-        Kout[2 * g] = make_uint4(o[0], o[1], o[2], o[3]);
-        Kout[2 * g + 1] = make_uint4(o[4], o[5], o[6], o[7]);
-    }
-}
-
 template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& L, void* K_out, void* V_out, cudaStream_t st) {
-    const long long nvec = (long long)s.kv_heads * s.ctx;
-    if (V_out) {
-        decompress_v_kernel<D, BITS><<<(unsigned)((nvec + 127) / 128), 128, 0, st>>>(
-            L.vcodes, L.vnorm, (int)nvec, s.ctx, s.ctx_pad, (uint4*)V_out, codebook(BITS));
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-    }
-    if (K_out) {
-        const long long n16 = nvec * D / 16;
-        decompress_k_kernel<D><<<(unsigned)((n16 + 255) / 256), 256, 0, st>>>(
-            L.kq, L.kscale, n16, s.ctx, s.ctx_pad, (uint4*)K_out);
-        return cudaGetLastError();
-    }
-    return cudaSuccess;
+    constexpr int VPB = kDecThreads / (D / 32);
+    const int nbv = V_out ? (s.ctx + VPB - 1) / VPB : 0;
+    const int nbk = K_out ? (s.ctx * (D / 16) + kDecThreads - 1) / kDecThreads : 0;
+    if (nbv + nbk == 0) return cudaSuccess;
+    decompress_kernel<D, BITS><<<dim3(nbv + nbk, s.kv_heads), kDecThreads, 0, st>>>(
+        L.kq, L.kscale, L.vcodes, L.vnorm, s.ctx, s.ctx_pad, nbv, (uint4*)K_out, (uint4*)V_out,
+        codebook(BITS));
+    return cudaGetLastError();
 }
 
 }  // namespace

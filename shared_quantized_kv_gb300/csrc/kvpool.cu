@@ -6,8 +6,8 @@
 //   per layer l:  kq     int8  [Hk][ctx_pad][D]
 //                 vcodes uint8 [Hk][ctx_pad][D*bits_l/8]
 //                 vnorm  f32   [Hk][ctx_pad]
-//   kscale f32 [layers], kabsmax u32 [layers] (encode scratch), vnmax u32
-//   [layers] (largest V norm, float bits), status int32.
+//   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits (encode
+//   scratch), largest V norm float bits}, status int32.
 // Attention needs no scratch: the CTAs of a cluster merge their context
 // splits through distributed shared memory.
 // ctx_pad rounds the token axis up to a multiple of 128 so tiles never leave a
@@ -146,14 +146,13 @@ struct kvpool {
     size_t bytes = 0;
     float* kscale = nullptr;
     uint32_t* kabsmax = nullptr;
-    uint32_t* vnmax = nullptr;
     int* status = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
-                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + l, bits[l],
-                vnmax + l};
+                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
+                kabsmax + 2 * l + 1};
     }
 };
 
@@ -234,10 +233,8 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     }
     const size_t off_scale = off;
     off = align256(off + 4 * (size_t)layers);
-    const size_t off_absmax = off;
-    off = align256(off + 4 * (size_t)layers);
-    const size_t off_vnmax = off;
-    off = align256(off + 4 * (size_t)layers);
+    const size_t off_absmax = off;  // per layer {max|K| bits, largest V norm bits}
+    off = align256(off + 8 * (size_t)layers);
     const size_t off_status = off;
     off = align256(off + 4);
     p->bytes = off;
@@ -255,7 +252,6 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     }
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
-    p->vnmax = reinterpret_cast<uint32_t*>(p->base + off_vnmax);
     p->status = reinterpret_cast<int*>(p->base + off_status);
     kvp::codebook(2);  // derive the tables now, not inside a stream capture
     *out = p;

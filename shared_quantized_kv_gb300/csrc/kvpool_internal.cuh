@@ -38,7 +38,7 @@ struct LayerBufs {
     float* kscale;     // 1 float
     uint32_t* kabsmax; // 1 word: bf16 bits of max|K| (scratch of the encode)
     int bits;
-    uint32_t* vnmax;   // 1 word: float bits of the largest V norm of the layer
+    uint32_t* vnmax;   // 1 word right after kabsmax: float bits of the largest V norm
 };
 
 struct Shape {
