@@ -69,10 +69,19 @@ typedef struct {
 
 /* Device-side view of one compressed layer (for inspection and tests). The
  * token axis is padded to `ctx_padded`; padding is zero and never read as a
- * token. Pointers stay owned by the pool. */
+ * token. Pointers stay owned by the pool.
+ *
+ * V code layout: per KV head, the tokens form groups of 32; a group holds, for
+ * each rotated coordinate i in order, the codes of its 32 tokens in token order
+ * packed little-endian (8 codes in 3 bytes at 3 bits, 4 per byte at 2 bits, 2
+ * per byte low nibble first at 4 bits): 4*bits bytes per coordinate,
+ * head_dim*4*bits bytes per group. Token slots past ctx in the last group hold
+ * code 0. (PolyKV summary, section 2.B, fixes the packing; the grouping is this
+ * library's, so that one thread reading one coordinate of many tokens finds
+ * them in consecutive bytes.) */
 typedef struct {
     const int8_t* kq;      /* int8 [kv_heads][ctx_padded][head_dim]            */
-    const uint8_t* vcodes; /* uint8 [kv_heads][ctx_padded][head_dim*bits/8]    */
+    const uint8_t* vcodes; /* uint8 [kv_heads][ctx_padded/32][head_dim][4*bits] */
     const float* vnorm;    /* float [kv_heads][ctx_padded]                     */
     const float* kscale;   /* one float: the layer's K scale s = max|K| / 127  */
     int ctx;
@@ -154,8 +163,8 @@ int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view
  * Inputs and outputs are the caller's: one compressed layer in the pool's
  * layout (as kvpool_layer_view describes it, token axis padded to
  * ctx_padded = ctx rounded up to a multiple of 128): kq int8
- * [kv_heads][ctx_padded][head_dim], vcodes uint8 [kv_heads][ctx_padded]
- * [head_dim*bits/8], vnorm float [kv_heads][ctx_padded], kscale one float;
+ * [kv_heads][ctx_padded][head_dim], vcodes uint8 [kv_heads][ctx_padded/32]
+ * [head_dim][4*bits], vnorm float [kv_heads][ctx_padded], kscale one float;
  * Q, tail, out, softmax_scale and stream as in kvpool_attend. The result
  * equals kvpool_attend's on the same layer within float rounding.
  *
@@ -177,8 +186,9 @@ int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, const float* 
 
 /* Copy the stored bytes of one compressed layer, token padding removed, to
  * caller buffers in host or device memory (any of the four may be NULL):
- * kq int8 [kv_heads][ctx][head_dim], vcodes uint8 [kv_heads][ctx][head_dim*
- * bits/8], vnorm float [kv_heads][ctx], kscale one float. Asynchronous on
+ * kq int8 [kv_heads][ctx][head_dim], vcodes uint8 [kv_heads][ceil(ctx/32)]
+ * [head_dim][4*bits] (whole 32-token groups, see kvpool_layer_view_t), vnorm
+ * float [kv_heads][ctx], kscale one float. Asynchronous on
  * `stream` (host buffers should be pinned). This is the quantised-cache handoff
  * of the QKVShare blog (mhpn.cn, section 3.1: the sender packs the quantised
  * cache with its scales; the receiver loads it instead of recomputing). */

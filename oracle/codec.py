@@ -32,10 +32,15 @@ V (each head-vector v of head_dim = d values, bf16 -> float32):
      coordinate): code_i = #{ j : u_i > fl(m_j * n) }. A tie goes to the lower
      code. A zero vector (n = 0) yields codes that decode to exactly 0 because
      the decoded vector is scaled by n.
-  4. Packing, per vector in coordinate order, little-endian: 3 bits -> groups
-     of 8 codes in 3 bytes, w = sum_k code_{8g+k} << 3k, bytes (w, w>>8,
-     w>>16) & 255; 2 bits -> 4 codes per byte, code_{4g+k} << 2k; 4 bits -> 2
-     codes per byte, low nibble first.
+  4. Packing of a code sequence, little-endian: 3 bits -> groups of 8 codes
+     in 3 bytes, w = sum_k code_{8g+k} << 3k, bytes (w, w>>8, w>>16) & 255;
+     2 bits -> 4 codes per byte, code_{4g+k} << 2k; 4 bits -> 2 codes per
+     byte, low nibble first. The pages fix the packing (8 codes in 3 bytes)
+     but not which codes form a sequence; the pool takes, per KV head, groups
+     of 32 consecutive tokens and, inside a group, one sequence per rotated
+     coordinate i holding the 32 tokens' codes in token order (4*bits bytes);
+     the sequences of a group follow in coordinate order. Token slots past
+     the context in the last group hold code 0.
   5. The norm n is stored as float32.
 
 Decompress:
@@ -185,6 +190,29 @@ def unpack_codes(packed: np.ndarray, bits: int, d: int) -> np.ndarray:
     return out.reshape(lead + (d,)).astype(np.uint8)
 
 
+GROUP = 32  # tokens per packed V group in the pool
+
+
+def pack_pool_v(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pool layout of one layer's V codes: [kv_heads, ctx, d] -> uint8
+    [kv_heads, ceil(ctx/32), d, 4*bits] (step 4 above)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    H, T, d = c.shape
+    ng = -(-T // GROUP)
+    pad = np.zeros((H, ng * GROUP, d), dtype=np.uint8)
+    pad[:, :T] = c
+    seq = pad.reshape(H, ng, GROUP, d).transpose(0, 1, 3, 2)  # [H, group, coordinate, token]
+    return pack_codes(seq, bits)
+
+
+def unpack_pool_v(packed: np.ndarray, bits: int, ctx: int) -> np.ndarray:
+    """Inverse of pack_pool_v: codes [kv_heads, ctx, d]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    H, ng, d, _ = p.shape
+    seq = unpack_codes(p, bits, GROUP)  # [H, group, coordinate, token]
+    return seq.transpose(0, 1, 3, 2).reshape(H, ng * GROUP, d)[:, :ctx]
+
+
 def v_decompress_bf16(codes: np.ndarray, norms: np.ndarray, bits: int) -> np.ndarray:
     cen, _ = lloyd_max.tables_f32(bits)
     d = codes.shape[-1]
@@ -200,7 +228,7 @@ def encode_layer(K_bf16, V_bf16, bits: int) -> dict:
     q = k_quantize(K_bf16, scale)
     codes, norms = v_codes(V_bf16, bits)
     return dict(bits=bits, absmax=absmax, scale=scale, kq=q, codes=codes,
-                packed=pack_codes(codes, bits), norms=norms)
+                packed=pack_pool_v(codes, bits), norms=norms)
 
 
 def decompress_layer(enc: dict):

@@ -11,7 +11,8 @@
 //
 // CUDA-core path (split context):
 //   attend_split: grid (context split, kv head, row block). A CTA walks its
-//     token range in tiles of 32 tokens: K int8 and the V codes are expanded
+//     token range in tiles of 32 tokens (one V code group of the pool
+//     layout): K int8 and the V codes are expanded
 //     to float32 in shared memory (V already scaled by its norm), then each
 //     warp runs an online softmax for its rows (lane = token for the logits,
 //     lane = channel for the rotated accumulator). It writes (m, l, acc) per
@@ -99,16 +100,20 @@ attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ v
             for (int e = 0; e < 16; ++e)
                 Ks[tt][c * 16 + e] = (float)(int8_t)((ws[e / 4] >> (8 * (e % 4))) & 0xFF);
         }
-        // V tile: 8 codes at a time -> n_t * c[code]
-        for (int i = tid; i < kTileTok * D / 8; i += blockDim.x) {
-            const int tt = i / (D / 8), gi = i % (D / 8);
-            const uint8_t* p = vbase + (long long)(t0 + tt) * VB + gi * BITS;
+        // V tile (one 32-token code group, t0 % 32 == 0): a task is 8 tokens of
+        // one coordinate, BITS bytes of that coordinate's code sequence -> n_t * c[code]
+        const uint8_t* grp = vbase + (long long)t0 * VB;
+        for (int i = tid; i < 4 * D; i += blockDim.x) {
+            const int ch = i / D, c = i % D;
+            const uint8_t* p = grp + c * (4 * BITS) + ch * BITS;
             uint32_t word = 0;
 #pragma unroll
             for (int b = 0; b < BITS; ++b) word |= (uint32_t)p[b] << (8 * b);
-            const float n = nbase[t0 + tt];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) Vs[tt][gi * 8 + k] = cen[(word >> (BITS * k)) & MASK] * n;
+            for (int k = 0; k < 8; ++k) {
+                const int t = t0 + ch * 8 + k;  // slots past the range hold 0 (their p is 0)
+                Vs[ch * 8 + k][c] = t < t_end ? cen[(word >> (BITS * k)) & MASK] * nbase[t] : 0.f;
+            }
         }
         __syncthreads();
 

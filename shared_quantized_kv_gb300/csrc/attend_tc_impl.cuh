@@ -10,116 +10,105 @@
 // shares the KV head is served by one pass over the packed pool bytes, so the
 // pool is read once per step no matter how many agents there are.
 //
-// Per CTA (512 threads, 16 warps; warp w reads TMEM lane quarter w % 4 and
-// column group w / 4; lane 0 of warp 15 issues the bulk copies and MMAs and
-// warp 15 takes no share of the operand conversion):
-//   lane 0 of warp 15 keeps a ring of shared-memory stages filled with bulk copies
-//     (cp.async.bulk) of the raw tiles -- 128 tokens of int8 K, packed V codes
-//     and float norms -- refilling a stage right after the barrier that ends
-//     its conversion; one mbarrier per stage tracks the bytes.
-//   all warps, per tile of 128 tokens:
-//     * int8 K -> fp16 K^ (exact) into a 128-byte-swizzled K-major operand;
-//       V codes -> fp16 lam * c[code] into a swizzled MN-major operand (d on
-//       the M axis, padded to 128 when d = 64);
-//     * one thread issues S^T = K^ Q^T (tokens on M = 128, rows on N) into TMEM;
-//     * softmax with the thread = token layout of TMEM: logits in log2 units,
-//       a running per-row maximum that is only raised (with a rescale of the
-//       TMEM accumulator) when a logit exceeds it by more than 2^8;
-//       P' = p * n_t / 2^k is split into fp16 hi (the top 11 significant
-//       bits) and fp16 lo (the exact remainder), two swizzled MN-major
-//       operands, so P' carries ~22 bits into the MMA;
-//     * one thread issues O^T += V^T (P'_hi + P'_lo)^T as two MMAs. V^T is a
-//       pure table lookup, fp16(lam * c[code]), with lam chosen so that all
-//       lam * c[k] sit within 2^-13..2^-22 of an fp16 value. The accumulator
-//       lives in the rotated domain, sum_t p_t n_t c[code_t], and never needs
-//       the inverse FWHT per token.
-//   epilogue: row sums and O^T are staged in shared memory; the cluster's CTAs
-//     merge their splits through distributed shared memory (log-sum-exp), each
-//     CTA for the rows of the agents it owns; one inverse FWHT per row (warp
-//     shuffles), the agent's tail (computed in the prologue while the first
-//     tiles are in flight) joins, and the row is written.
+// Per CTA: 256 threads, 8 warps; warp w owns TMEM lane quarter w % 4 and
+// column half w / 4. Both MMAs take their A operand from tensor memory, so the
+// expanded K and V never touch shared memory:
+//   * thread 0 keeps a ring of shared-memory stages filled: a TMA tile of 128
+//     tokens of int8 K (128-byte swizzle, so that one thread per token reads
+//     its row without bank conflicts), the tile's packed V code groups and its
+//     norms (plain bulk copies), one mbarrier per stage. When no kernel before
+//     it in the stream can still be writing the layer, the first tiles are
+//     requested before the grid-dependency wait, overlapping the previous
+//     kernel's tail.
+//   * K^: thread = token, int8 -> fp16 (exact, byte permutes) straight into
+//     TMEM as the A operand of S^T = K^ Q^T (tokens on M = 128, query rows on
+//     N); Q is fp16 in shared memory, each row scaled by its own power of two.
+//   * V^T: thread = rotated coordinate, its 64 codes of the tile (one packed
+//     sequence per coordinate and 32-token group in the pool layout) -> fp16
+//     lam * c[code] by byte-permute table lookups, into TMEM as the A operand
+//     of O^T += V^T P'^T. The accumulator stays in the rotated domain,
+//     sum_t p_t n_t c[code_t]; the inverse FWHT runs once per output row.
+//   * softmax with thread = token: logits in log2 units against a running
+//     per-row maximum that is raised (with a rescale of O^T in TMEM) only when
+//     a logit exceeds it by more than 2^8; P' = p * n_t / 2^k split into fp16
+//     hi (top 11 significant bits) and fp16 lo (the exact remainder), written
+//     as two MN-major operands, so P' carries ~22 bits into the MMA.
+//   * software pipeline per tile: MMA1(i) runs while V(i) is expanded, MMA2(i)
+//     while K(i+1) is expanded.
+//   epilogue: each CTA pushes its partial rows (m, l, O^T) into the shared
+//     memory of the CTA that owns the row's agent (distributed shared memory
+//     stores, no remote loads), one cluster barrier, then every owner merges
+//     its rows (log-sum-exp), applies one inverse FWHT per row (warp
+//     shuffles), joins the agent's tail (computed in the prologue while the
+//     first tiles are in flight) and writes the row.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // KVPOOL_ERR_TIMEOUT in the status word and carries on to its exit without
 // waiting again, so a fault never hangs the device.
 #pragma once
 
-#include <cooperative_groups.h>
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <algorithm>
+
 #include "kvpool_internal.cuh"
 #include "tc_ptx.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace kvp {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kWork = 512;       // 16 warps: (TMEM lane quarter) x (column group)
-constexpr int kThreads = kWork;
-constexpr int kMmaWarp = 15;     // its lane 0 issues bulk copies and MMAs; it converts nothing
-constexpr int kConv = 480;       // threads of warps 0..14, which convert the operands
-constexpr float kTau = 8.0f;                  // P <= 2^kTau between rescales
+constexpr int kThreads = 256;   // 8 warps: (TMEM lane quarter) x (column half)
+constexpr float kTau = 8.0f;    // P <= 2^kTau between rescales
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
 
 struct TcParams {
-    const int8_t* kq;
     const uint8_t* vcodes;
     const float* vnorm;
     const float* kscale;
     const uint32_t* vnmax;
     int ctx, ctx_pad, Hk;
     const uint16_t* Q;
-    int Hq, G, R, agents;
+    int Hq, G, R;
     const uint16_t* tK;
     const uint16_t* tV;
     const int32_t* tlen;
     int tail_max;
     float* out;
     float scale_log2;
-    int tps;  // tokens per split, multiple of kTile
-    int bits, nstage;
-    uint32_t tmem_cols;
+    int tps;     // tokens per CTA, a multiple of kTile
+    int nstage;  // shared-memory stages of raw tiles
+    int early;   // 1: the layer's bytes may be read before the grid-dependency wait
+    int own;     // most query rows one CTA owns in the merge
     int* status;
-    uint32_t c16[8];  // fp16 pairs: lam * centroid[2k], lam * centroid[2k+1]
+    uint32_t tlo[4], thi[4];  // low / high bytes of fp16 lam * c[k], entry k in byte k % 4 of word k / 4
     float inv_lam;
 };
 
 struct Layout {
-    uint32_t q, khat, vhat, p, raw, lut, bars, misc, total;
-    uint32_t stage, rk, rv, rn;  // bytes per stage and offsets inside one
+    uint32_t stage, rv, rn;  // bytes per raw stage; V codes and norms inside one
+    uint32_t q, p, plo, misc, bars, total;
 };
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// W = rows per row block (MMA N), NB = row blocks per CTA.
-__host__ __device__ inline Layout make_layout(int D, int bits, int W, int NB, int nstage) {
+// W = query rows per CTA (MMA N).
+__host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage) {
     Layout L;
-    uint32_t o = 0;
-    L.q = o;
-    o += NB * W * D * 2;
-    o = align_up(o, 1024);
-    L.khat = o;
-    o += kTile * D * 2;
-    L.vhat = o;  // two buffers of 128 (M) x 128 (tokens) fp16
-    o += 2 * 32768;
-    L.p = o;  // per row block: P hi and P lo, each 16 token-groups x 1024 B
-    o += NB * 2 * 16384;
-    L.raw = o;
-    L.rk = 0;
     L.rv = kTile * D;
     L.rn = L.rv + kTile * D * bits / 8;
-    L.stage = align_up(L.rn + kTile * 4, 128);
-    o += nstage * L.stage;
-    o = align_up(o, 16);
-    L.lut = o;  // pair table: 2^(2*bits) fp16x2 entries
-    o += 1024;
-    L.bars = o;  // full[nstage], mma
-    o += 8 * 8;
-    L.misc = o;
-    // misc: tmem slot, flags, qexp, lsum[4][128], colmax[4][128], M[128], l[128], tail m/l[128][2]
-    o += 128 + 4 * 128 * 4 * 2 + 128 * 4 * 2 + 128 * 8;
+    L.stage = align_up(L.rn + kTile * 4, 1024);
+    uint32_t o = nstage * L.stage;  // raw stages start at 0
+    L.q = o;
+    o = align_up(o + W * D * 2, 1024);
+    L.p = o;
+    L.plo = W <= 64 ? 16384 : 32768;  // P' hi, then P' lo
+    o += 2 * L.plo;
+    L.misc = o;  // everything below misc is free after the main loop (merge slots)
+    o += (14 * W + 16) * 4;
+    L.bars = align_up(o, 8);
+    o = L.bars + 8 * (nstage + 2) + 8;
     L.total = align_up(o, 1024);
     return L;
 }
@@ -137,23 +126,85 @@ __device__ __forceinline__ int f2ord(float f) {
 }
 __device__ __forceinline__ float ord2f(int i) { return __int_as_float(i >= 0 ? i : i ^ 0x7FFFFFFF); }
 
-// four int8 (biased by 128) -> two fp16x2 holding the signed values exactly
+// four int8 -> two fp16x2 holding the signed values exactly
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-    const uint32_t x = w ^ 0x80808080u;
+    const uint32_t x = w ^ 0x80808080u;  // biased by 128
     const uint32_t magic = 0x64646464u;  // fp16 0x64xx = 1024 + xx
-    uint32_t a, b;
-    asm("prmt.b32 %0, %1, %2, 0x5140;" : "=r"(a) : "r"(x), "r"(magic));
-    asm("prmt.b32 %0, %1, %2, 0x7362;" : "=r"(b) : "r"(x), "r"(magic));
+    const uint32_t a = ptx::prmt(x, magic, 0x5140);
+    const uint32_t b = ptx::prmt(x, magic, 0x7362);
     const __half2 bias = __floats2half2_rn(1152.0f, 1152.0f);
-    __half2 ha = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
+    __half2 ha = __hsub2(*reinterpret_cast<const __half2*>(&a), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
     lo = *reinterpret_cast<uint32_t*>(&ha);
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+// 8 codes of BITS bits (the low 8*BITS bits of x) -> 8 nibbles
+template <int BITS>
+__device__ __forceinline__ uint32_t spread8(uint32_t x) {
+    if constexpr (BITS == 2) {
+        uint32_t y = (x & 0xFFu) | ((x & 0xFF00u) << 8);
+        y = (y & 0x000F000Fu) | ((y & 0x00F000F0u) << 4);
+        return (y & 0x03030303u) | ((y & 0x0C0C0C0Cu) << 2);
+    } else if constexpr (BITS == 3) {
+        uint32_t y = (x & 0xFFFu) | ((x & 0xFFF000u) << 4);
+        y = (y & 0x003F003Fu) | ((y & 0x0FC00FC0u) << 2);
+        return (y & 0x07070707u) | ((y & 0x38383838u) << 1);
+    } else {
+        return x;
+    }
+}
+
+// 4 codes (nibbles of the low 16 bits of sel) -> two fp16x2 of lam * c[code]
+template <int BITS>
+__device__ __forceinline__ void lookup4(uint32_t sel, const uint32_t (&tlo)[4], const uint32_t (&thi)[4],
+                                        uint32_t& h01, uint32_t& h23) {
+    uint32_t L, H;
+    if constexpr (BITS <= 3) {
+        L = ptx::prmt(tlo[0], tlo[1], sel);
+        H = ptx::prmt(thi[0], thi[1], sel);
+    } else {
+        const uint32_t s3 = sel & 0x7777u;
+        const uint32_t La = ptx::prmt(tlo[0], tlo[1], s3), Lb = ptx::prmt(tlo[2], tlo[3], s3);
+        const uint32_t Ha = ptx::prmt(thi[0], thi[1], s3), Hb = ptx::prmt(thi[2], thi[3], s3);
+        // byte mask of the codes >= 8: the sign-replicate mode of a selector
+        // nibble with bit 3 set turns 0x80 into 0xFF
+        uint32_t m = ptx::prmt(0x80808080u, 0x80808080u, sel) & 0x7F7F7F7Fu;
+        m |= m << 1;
+        L = (La & ~m) | (Lb & m);
+        H = (Ha & ~m) | (Hb & m);
+    }
+    h01 = ptx::prmt(L, H, 0x5140);
+    h23 = ptx::prmt(L, H, 0x7362);
+}
+
+// the 32 codes of one packed sequence (4*BITS bytes at `row`) -> 16 fp16x2
+template <int BITS>
+__device__ __forceinline__ void decode32(const unsigned char* row, const uint32_t (&tlo)[4],
+                                         const uint32_t (&thi)[4], uint32_t* h) {
+    uint32_t f[4];  // four fields of 8 codes
+    if constexpr (BITS == 2) {
+        const uint2 w = *reinterpret_cast<const uint2*>(row);
+        f[0] = w.x; f[1] = w.x >> 16; f[2] = w.y; f[3] = w.y >> 16;
+    } else if constexpr (BITS == 3) {
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(row);
+        const uint32_t w0 = wp[0], w1 = wp[1], w2 = wp[2];
+        f[0] = w0; f[1] = __funnelshift_r(w0, w1, 24); f[2] = __funnelshift_r(w1, w2, 16); f[3] = w2 >> 8;
+    } else {
+        const uint4 w = *reinterpret_cast<const uint4*>(row);
+        f[0] = w.x; f[1] = w.y; f[2] = w.z; f[3] = w.w;
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t y = spread8<BITS>(f[k]);
+        lookup4<BITS>(y, tlo, thi, h[4 * k], h[4 * k + 1]);
+        lookup4<BITS>(y >> 16, tlo, thi, h[4 * k + 2], h[4 * k + 3]);
+    }
+}
+
 // sum over the 32 lanes for each of N values; afterwards lane l holds the
 // sums of columns [l*N/32, l*N/32 + N/32) when N >= 32, or column l*N/32
-// (replicated over 32/N lanes) when N < 32. Returns the number of values kept.
+// (replicated over 32/N lanes) when N < 32.
 template <int N>
 __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
     int len = N;
@@ -177,71 +228,65 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
     }
 }
 
-// 32 V codes of token t (channels 32*qd .. 32*qd+31) -> fp16 lam * c[code]
-// via a table of code pairs, into four 16-byte chunks of the token's
-// MN-major swizzled row of the V^T operand.
-template <int BITS>
-__device__ __forceinline__ void convert_v_quarter(const unsigned char* src, const uint32_t* pairs,
-                                                  unsigned char* vrow, int t, int dc0) {
-    constexpr uint32_t PMASK = (1u << (2 * BITS)) - 1;
-    uint32_t w[BITS + 1];  // 32 codes = 4*BITS bytes = BITS words
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+    if constexpr (N % 16 == 0) {
 #pragma unroll
-    for (int k = 0; k < BITS; ++k) w[k] = *reinterpret_cast<const uint32_t*>(src + 4 * k);
-    w[BITS] = 0;
+        for (int c = 0; c < N; c += 16) {
+            uint32_t r[16];
+            ptx::tmem_ld16(taddr + c, r);
 #pragma unroll
-    for (int dc = 0; dc < 4; ++dc) {
-        uint32_t h[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int bit = (dc * 8 + 2 * e) * BITS, wi = bit >> 5, off = bit & 31;
-            h[e] = pairs[__funnelshift_r(w[wi], w[wi + 1], off) & PMASK];
+            for (int e = 0; e < 16; ++e) v[c + e] = __uint_as_float(r[e]);
         }
-        *reinterpret_cast<uint4*>(vrow + (((dc0 + dc) ^ (t % 8)) * 16)) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+        static_assert(N == 8, "column count");
+        uint32_t r[8];
+        ptx::tmem_ld8(taddr, r);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[e]);
     }
 }
 
 // Attention of the owned agents' rows over their private bf16 tails (plain
 // CUDA cores, online softmax in log2 units). Writes the unnormalised
-// accumulator to `out` and (m, l) per row to `tailml`; uses the K^ operand
-// area as staging (free before the main loop).
+// accumulator to `out` and (m, l) per row to `tailml`; `stage` is 12.5 KB of
+// shared memory that is free until the main loop.
 template <int D>
-__device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* sK, float* tailml, int S,
-                                            int crank, int g, int row0, int nrows) {
+__device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* stage, float* tailml,
+                                            int S, int crank, int g, int row0, int nrows) {
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    // staging in the K^ operand area, unused until the main loop
-    float* tq = reinterpret_cast<float*>(sK);                                // [8][D]
-    float* tl = reinterpret_cast<float*>(sK + 8 * D * 4);                   // [8][256]
-    float* tred = reinterpret_cast<float*>(sK + 8 * D * 4 + 8 * 256 * 4);   // [8 warps][8]
-    constexpr int TCH = 256;                                                 // tokens per chunk
-    constexpr int RPT = kWork / D;  // row sub-blocks in the P.V phase
+    float* tq = reinterpret_cast<float*>(stage);                               // [8][D]
+    float* tl = reinterpret_cast<float*>(stage + 8 * D * 4);                  // [8][256]
+    float* tred = reinterpret_cast<float*>(stage + 8 * D * 4 + 8 * 256 * 4);  // [8 warps][8]
+    constexpr int TCH = 256;            // tokens per chunk (one per thread)
+    constexpr int RPT = kThreads / D;   // row sub-blocks in the P.V phase
+    static_assert(TCH == kThreads, "one tail token per thread");
     const int c = tid % D, sub = tid / D;
     const int G = p.G;
-    const int a_first = row0 / G, a_last = (row0 + nrows - 1) / G;
-    for (int a = a_first + ((crank - a_first % S) % S + S) % S; a <= a_last; a += S)
-    for (int jb = max(0, row0 - a * G); jb < min(G, row0 + nrows - a * G); jb += 8) {
-        // rows k = 0..7 of the batch are (agent a, head jb + k)
-        const int cnt = min(8, min(G, row0 + nrows - a * G) - jb);
-        const int ownmask = (1 << cnt) - 1;
-        const int rr0 = a * G + jb - row0;
-        const int tmax = min(max(p.tlen[a], 0), p.tail_max);
-        for (int i = tid; i < 8 * D; i += kThreads) {
-            const int k = i / D, cc = i % D;
-            float v = 0.f;
-            if ((ownmask >> k) & 1)
-                v = bf2f(p.Q[((long long)a * p.Hq + g * G + jb + k) * D + cc]);
-            tq[k * D + cc] = v;
-        }
-        float m_run[8], l_run[8], acc[8];
+    for (int ar = crank; ar * G < nrows; ar += S) {
+        const int a = row0 / G + ar;
+        for (int jb = 0; jb < G; jb += 8) {
+            // rows k = 0..7 of the batch are (agent a, head jb + k)
+            const int cnt = min(8, G - jb);
+            const int ownmask = (1 << cnt) - 1;
+            const int rr0 = ar * G + jb;
+            const int tmax = min(max(p.tlen[a], 0), p.tail_max);
+            for (int i = tid; i < 8 * D; i += kThreads) {
+                const int k = i / D, cc = i % D;
+                float v = 0.f;
+                if ((ownmask >> k) & 1) v = bf2f(p.Q[((long long)a * p.Hq + g * G + jb + k) * D + cc]);
+                tq[k * D + cc] = v;
+            }
+            float m_run[8], l_run[8], acc[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; acc[k] = 0.f; }
-        __syncthreads();
-        for (int c0 = 0; c0 < tmax; c0 += TCH) {
-            const int t = c0 + tid;
+            for (int k = 0; k < 8; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; acc[k] = 0.f; }
+            __syncthreads();
+            for (int c0 = 0; c0 < tmax; c0 += TCH) {
+                const int t = c0 + tid;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float lg = -CUDART_INF_F;
-                if (tid < TCH && ((ownmask >> k) & 1)) {
-                    if (t < tmax) {
+                for (int k = 0; k < 8; ++k) {
+                    float lg = -CUDART_INF_F;
+                    if (((ownmask >> k) & 1) && t < tmax) {
                         const uint16_t* kr = p.tK + (((long long)a * p.Hk + g) * p.tail_max + t) * D;
                         const float* qq = tq + k * D;
                         float dot = 0.f;
@@ -258,144 +303,153 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* sK
                         }
                         lg = dot * p.scale_log2;
                     }
-                }
-                if (tid < TCH) {
                     tl[k * TCH + tid] = lg;
                     const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(lg)));
                     if (lane == 0) tred[warp * 8 + k] = mx;
                 }
-            }
-            __syncthreads();
-            float mnew[8], alpha[8];
+                __syncthreads();
+                float mnew[8], alpha[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float mx = -CUDART_INF_F;
+                for (int k = 0; k < 8; ++k) {
+                    float mx = -CUDART_INF_F;
 #pragma unroll
-                for (int w = 0; w < TCH / 32; ++w) mx = fmaxf(mx, tred[w * 8 + k]);
-                mnew[k] = fmaxf(m_run[k], mx);
-                alpha[k] = (mnew[k] == -CUDART_INF_F) ? 1.f : ptx::ex2(m_run[k] - mnew[k]);
-                if (tid < TCH) {
+                    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, tred[w * 8 + k]);
+                    mnew[k] = fmaxf(m_run[k], mx);
+                    alpha[k] = (mnew[k] == -CUDART_INF_F) ? 1.f : ptx::ex2(m_run[k] - mnew[k]);
                     const float lg = tl[k * TCH + tid];
                     tl[k * TCH + tid] = (lg == -CUDART_INF_F) ? 0.f : ptx::ex2(lg - mnew[k]);
                 }
+                __syncthreads();
+                const int cnt2 = min(TCH, tmax - c0);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    l_run[k] *= alpha[k];
+                    acc[k] *= alpha[k];
+                    m_run[k] = mnew[k];
+                    if ((k % RPT) != sub || !((ownmask >> k) & 1)) continue;
+                    const uint16_t* vr0 = p.tV + (((long long)a * p.Hk + g) * p.tail_max + c0) * D + c;
+                    float sacc = 0.f, ls = 0.f;
+                    for (int t2 = 0; t2 < cnt2; ++t2) {
+                        const float pv = tl[k * TCH + t2];
+                        sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
+                        ls += pv;
+                    }
+                    acc[k] += sacc;
+                    l_run[k] += ls;
+                }
+                __syncthreads();
             }
-            __syncthreads();
-            const int cend = min(TCH, tmax - c0);
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-                l_run[k] *= alpha[k];
-                acc[k] *= alpha[k];
-                m_run[k] = mnew[k];
                 if ((k % RPT) != sub || !((ownmask >> k) & 1)) continue;
-                const int n = tmax;
-                const uint16_t* vr0 = p.tV + (((long long)a * p.Hk + g) * p.tail_max + c0) * D + c;
-                const int cnt = min(cend, n - c0);
-                float sacc = 0.f, ls = 0.f;
-                for (int t2 = 0; t2 < cnt; ++t2) {
-                    const float pv = tl[k * TCH + t2];
-                    sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
-                    ls += pv;
+                const int rr = rr0 + k, j = jb + k;
+                p.out[((long long)a * p.Hq + g * G + j) * D + c] = acc[k];
+                if (c == 0) {
+                    tailml[2 * rr] = m_run[k];
+                    tailml[2 * rr + 1] = l_run[k];
                 }
-                acc[k] += sacc;
-                l_run[k] += ls;
             }
             __syncthreads();
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            if ((k % RPT) != sub || !((ownmask >> k) & 1)) continue;
-            const int rr = rr0 + k, j = jb + k;
-            p.out[((long long)a * p.Hq + g * G + j) * D + c] = acc[k];
-            if (c == 0) {
-                tailml[2 * rr] = m_run[k];
-                tailml[2 * rr + 1] = l_run[k];
-            }
-        }
-        __syncthreads();
     }
 }
 
-template <int D, int W, int NB, int BITS>
-__global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p) {
-    constexpr int RG = NB * W;                   // rows per CTA (W = MMA N per row block)
-    constexpr int NCG = (W / 8) < 4 ? (W / 8) : 4;  // column groups of warps
-    constexpr int HC = W / NCG;                  // columns per thread per row block (8 or 16)
-    constexpr int CPT = NB * HC;                 // columns per thread
-    constexpr int EPL = D / 32;                  // elements per lane in the epilogue
+template <int D, int W, int BITS>
+__global__ void __launch_bounds__(kThreads, (W <= 64 ? 2 : 1))
+attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
+    constexpr int HW = W / 2;            // query rows (TMEM columns) per thread
+    constexpr int EPL = D / 32;          // channels per lane in the merge
+    constexpr int VB = D * BITS / 8;     // code bytes per token
+    constexpr int GB = D * 4 * BITS;     // bytes per 32-token code group
+    constexpr uint32_t kCols = W <= 64 ? 256 : 512;
+    constexpr uint32_t kColO = W <= 64 ? 64 : 128;  // O^T; S^T at column 0
+    constexpr uint32_t kColK = 2 * kColO;           // K^ (D/2 columns)
+    constexpr uint32_t kColV = kColK + 64;          // V^T (64 columns: 128 tokens of fp16 pairs)
+    constexpr int KC = D / 32;           // 16-byte K chunks per thread (half a row)
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const Layout lay = make_layout(D, BITS, W, NB, p.nstage);
+    const Layout lay = make_layout(D, BITS, W, p.nstage);
     unsigned char* sQ = sm + lay.q;
-    unsigned char* sK = sm + lay.khat;
-    unsigned char* sV = sm + lay.vhat;
     unsigned char* sP = sm + lay.p;
-    unsigned char* sRaw = sm + lay.raw;
-    uint32_t* pairs = reinterpret_cast<uint32_t*>(sm + lay.lut);
+    float* sM = reinterpret_cast<float*>(sm + lay.misc);  // [W] running row maxima (log2 units)
+    float* sCf = sM + W;                                    // [W] logit factor per row
+    float* sL = sCf + W;                                    // [W] row sums
+    float* lsum = sL + W;                                   // [4][W]
+    float* colmax = lsum + 4 * W;                           // [4][W]
+    float* tailml = colmax + 4 * W;                         // [W][2]
+    uint32_t* sOwn = reinterpret_cast<uint32_t*>(tailml + 2 * W);  // [W] owner << 16 | slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
-    unsigned char* misc = sm + lay.misc;
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(misc);
-    float* sred = reinterpret_cast<float*>(misc + 16);      // [16] block reduction scratch
-    float* lsum = reinterpret_cast<float*>(misc + 128);     // [4][128]
-    float* colmax = lsum + 4 * 128;                          // [4][128]
-    float* sM = colmax + 4 * 128;                            // [128] running row maxima
-    float* sL = sM + 128;                                    // [128] row sums
-    float* tailml = sL + 128;                                // [128][2]
-    float* sO = reinterpret_cast<float*>(sK);                // epilogue: [RG][D], aliases K^, V^
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + p.nstage + 2);
+    const uint32_t bar_full = ptx::smem_u32(bars);
+    const uint32_t bar_s = bar_full + 8 * p.nstage;  // S^T of the tile is in TMEM
+    const uint32_t bar_o = bar_s + 8;                // the tile's P.V MMAs are done
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const int S = (int)cluster.num_blocks();
-    const int crank = (int)cluster.block_rank();
+    const int S = (int)ptx::cluster_size();
+    const int crank = (int)ptx::cluster_rank();
     const int g = blockIdx.y;
-    const int row0 = blockIdx.z * RG;
-    const int nrows = min(RG, p.R - row0);
+    const int row0 = blockIdx.z * W;
+    const int nrows = min(W, p.R - row0);
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const int q = warp & 3, cg = warp >> 2;
+    const int tok = q * 32 + lane;      // token of this thread in S^T / K^; channel in O^T / V^T
+    const bool has_ch = q * 32 < D;     // warp-uniform: lanes of this quarter hold channels
     const int t_begin = crank * p.tps;
     const int t_end = min(p.ctx, t_begin + p.tps);
-    const int ntile = t_end > t_begin ? (t_end - t_begin + kTile - 1) / kTile : 0;
-    constexpr int VB = D * BITS / 8;
+    const int ntile = (t_end - t_begin + kTile - 1) / kTile;  // >= 1
+    const long long head_tok = (long long)g * p.ctx_pad;
     const uint32_t stage_bytes = kTile * D + kTile * VB + kTile * 4;
-    const uint32_t bar_full = ptx::smem_u32(bars);
-    const uint32_t bar_mma = bar_full + 8 * p.nstage;
+
+    auto issue_tile = [&](int i) {
+        const int s = i % p.nstage;
+        const long long t0 = head_tok + t_begin + (long long)i * kTile;
+        const uint32_t dst = ptx::smem_u32(sm + s * lay.stage);
+        const uint32_t bar = bar_full + 8 * s;
+        ptx::mbar_expect_tx(bar, stage_bytes);
+        ptx::tma_load_2d(dst, &kmap, 0, (int)t0, bar);
+        ptx::bulk_g2s(dst + lay.rv, p.vcodes + t0 * VB, kTile * VB, bar);
+        ptx::bulk_g2s(dst + lay.rn, p.vnorm + t0, kTile * 4, bar);
+    };
+    auto issue_first = [&]() {
+        for (int i = 0; i < min(ntile, p.nstage); ++i) issue_tile(i);
+        for (int i = p.nstage; i < ntile; ++i) {  // later tiles: warm L2
+            const long long t0 = head_tok + t_begin + (long long)i * kTile;
+            ptx::tma_prefetch_2d(&kmap, 0, (int)t0);
+            ptx::prefetch_l2(p.vcodes + t0 * VB, kTile * VB);
+            ptx::prefetch_l2(p.vnorm + t0, kTile * 4);
+        }
+    };
 
     // ---------------------------------------------------------------- setup
-    if (warp == 0) ptx::tmem_alloc(ptx::smem_u32(tslot), p.tmem_cols);
-    if (tid == 32) {
-        for (int s = 0; s < p.nstage; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
-        ptx::mbar_init(bar_mma, 1);
+    if (tid == 0) {
+        for (int s = 0; s < p.nstage + 2; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
         ptx::mbar_init_fence();
+        if (p.early) issue_first();
     }
-    {
-        for (int i = tid; i < (1 << (2 * BITS)); i += kThreads) {
-            const int c0 = i & ((1 << BITS) - 1), c1 = i >> BITS;
-            const uint32_t h0 = (p.c16[c0 >> 1] >> (16 * (c0 & 1))) & 0xFFFFu;
-            const uint32_t h1 = (p.c16[c1 >> 1] >> (16 * (c1 & 1))) & 0xFFFFu;
-            pairs[i] = h0 | (h1 << 16);
-        }
-    }
-    if (tid < 128) sM[tid] = -CUDART_INF_F;
-    if (D == 64) {  // rows 64..127 of both V^T operand buffers stay zero
-        for (int i = tid; i < 2 * 1024; i += kThreads)
-            reinterpret_cast<uint4*>(sV + (i / 1024) * 32768 + 16384)[i % 1024] = make_uint4(0, 0, 0, 0);
+    if (warp == 0) ptx::tmem_alloc(ptx::smem_u32(tslot), kCols);
+    if (tid < W) {
+        sM[tid] = -CUDART_INF_F;
+        const int ar = tid / p.G;  // agent of row tid, relative to the CTA's first agent
+        sOwn[tid] = ((uint32_t)(ar % S) << 16) | (uint32_t)((ar / S) * p.G + tid % p.G);
     }
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t tS = tmem;            // S^T: NB*W columns
-    const uint32_t tO = tmem + NB * W;   // O^T: NB*W columns
-
-    const long long head_tok = (long long)g * p.ctx_pad;
-    if (tid == 0) {  // warm L2 while the previous kernel in the stream drains
-        for (int i = 0; i < ntile; ++i) {
-            const long long t0 = head_tok + t_begin + (long long)i * kTile;
-            ptx::prefetch_l2(p.kq + t0 * D, kTile * D);
-            ptx::prefetch_l2(p.vcodes + t0 * VB, kTile * VB);
-        }
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t tS = tmem, tO = tmem + kColO, tK = tmem + kColK, tV = tmem + kColV;
+    if (D == 64 && !has_ch) {  // V^T rows 64..127 stay zero (M = 128 with d = 64)
+        uint32_t z[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) z[e] = 0u;
+        ptx::tmem_st32(tV + lane_off + 32 * cg, z);
+        ptx::tmem_wait_st();
     }
+
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
+    if (tid == 0 && !p.early) issue_first();
     bool timed_out = false;
     // P' = p * n_t / nref with nref the power of two >= the largest norm of the layer
     float vr = 1.0f, nref = 1.0f;
@@ -408,353 +462,317 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
             vr = ldexpf(1.0f, -k);
         }
     }
-    auto issue_tile = [&](int i) {
-        const int s = i % p.nstage;
-        const long long t0 = head_tok + t_begin + (long long)i * kTile;
-        const uint32_t dst = ptx::smem_u32(sRaw + s * lay.stage);
-        ptx::mbar_expect_tx(bar_full + 8 * s, stage_bytes);
-        ptx::bulk_g2s(dst + lay.rk, p.kq + t0 * D, kTile * D, bar_full + 8 * s);
-        ptx::bulk_g2s(dst + lay.rv, p.vcodes + t0 * VB, kTile * VB, bar_full + 8 * s);
-        ptx::bulk_g2s(dst + lay.rn, p.vnorm + t0, kTile * 4, bar_full + 8 * s);
-    };
-    if (warp == kMmaWarp && lane == 0)
-        for (int i = 0; i < min(ntile, p.nstage); ++i) issue_tile(i);
+    const float kscale = *p.kscale;
 
-    // 1. Q rows of this CTA -> fp16, scaled by a power of two, swizzled K-major.
-    //    All loads of a thread are issued before any is used.
-    constexpr int QCH = RG * (D / 8);                     // 16-byte chunks
-    constexpr int QPT = (QCH + kWork - 1) / kWork;  // chunks per compute thread
-    uint4 qv[QPT];
-    uint32_t qmax = 0;
+    // 1. Q rows -> fp16 in a 128-byte-swizzled K-major operand; each row is
+    //    scaled by the power of two that puts its largest |q| in [2^14, 2^15)
+    //    (exact), and the logit factor of the row undoes it.
+    {
+        constexpr int CPR = D / 8;            // 16-byte chunks per row
+        constexpr int RPP = kThreads / CPR;   // rows per pass
+        constexpr int NP = (W + RPP - 1) / RPP;
+        uint4 qv[NP];
+        const int c = tid % CPR;
 #pragma unroll
-    for (int k = 0; k < QPT; ++k) {
-        const int idx = k * kWork + tid, rr = idx / (D / 8), c = idx % (D / 8);
-        qv[k] = make_uint4(0, 0, 0, 0);
-        if (idx < QCH && rr < nrows) {
-            const int r = row0 + rr, a = r / p.G, j = r % p.G;
-            qv[k] = *reinterpret_cast<const uint4*>(p.Q + ((long long)a * p.Hq + g * p.G + j) * D + c * 8);
+        for (int k = 0; k < NP; ++k) {
+            const int r = k * RPP + tid / CPR;
+            qv[k] = make_uint4(0, 0, 0, 0);
+            if (r < nrows) {
+                const int a = (row0 + r) / p.G, j = (row0 + r) % p.G;
+                qv[k] = *reinterpret_cast<const uint4*>(p.Q + ((long long)a * p.Hq + g * p.G + j) * D + c * 8);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < NP; ++k) {
+            const int r = k * RPP + tid / CPR;
+            const uint32_t m7 = 0x7FFF7FFFu;
+            const uint4 u = qv[k];
+            const uint32_t am = __vmaxu2(__vmaxu2(u.x & m7, u.y & m7), __vmaxu2(u.z & m7, u.w & m7));
+            uint32_t qmax = max(am & 0xFFFFu, am >> 16);
+#pragma unroll
+            for (int o = CPR / 2; o >= 1; o >>= 1) qmax = max(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+            int qe = 0;
+            if (qmax != 0 && qmax < 0x7F80u) qe = 14 - ((int)((qmax >> 7) & 0xFF) - 127);
+            qe = max(-100, min(100, qe));
+            const float qmul = ldexpf(1.0f, qe);
+            if (r < W) {
+                uint4 v;
+                v.x = pack_h2(bf2f(u.x & 0xFFFF) * qmul, bf2f(u.x >> 16) * qmul);
+                v.y = pack_h2(bf2f(u.y & 0xFFFF) * qmul, bf2f(u.y >> 16) * qmul);
+                v.z = pack_h2(bf2f(u.z & 0xFFFF) * qmul, bf2f(u.z >> 16) * qmul);
+                v.w = pack_h2(bf2f(u.w & 0xFFFF) * qmul, bf2f(u.w >> 16) * qmul);
+                *reinterpret_cast<uint4*>(sQ + (c / 8) * (W * 128) + (r / 8) * 1024 + (r % 8) * 128 +
+                                          (((c % 8) ^ (r % 8)) * 16)) = v;
+                if (c == 0) sCf[r] = r < nrows ? p.scale_log2 * kscale * ldexpf(1.0f, -qe) : 0.f;
+            }
         }
     }
-#pragma unroll
-    for (int k = 0; k < QPT; ++k) {
-        const uint32_t m = 0x7FFF7FFFu;
-        const uint32_t a = __vmaxu2(__vmaxu2(qv[k].x & m, qv[k].y & m), __vmaxu2(qv[k].z & m, qv[k].w & m));
-        qmax = max(qmax, max(a & 0xFFFFu, a >> 16));
-    }
-    qmax = __reduce_max_sync(0xffffffffu, qmax);
-    if (lane == 0) reinterpret_cast<uint32_t*>(sred)[warp] = qmax;
-    __syncthreads();
-#pragma unroll
-    for (int w = 0; w < kThreads / 32; ++w) qmax = max(qmax, reinterpret_cast<uint32_t*>(sred)[w]);
-    const float amax = __uint_as_float(qmax << 16);
-    int qe = 0;  // scale Q by 2^qe so that max |q| lands in [2^14, 2^15)
-    if (qmax != 0 && qmax < 0x7F80u) qe = 14 - ((int)((qmax >> 7) & 0xFF) - 127);
-    (void)amax;
-    qe = max(-100, min(100, qe));
-    const float qmul = ldexpf(1.0f, qe);
-#pragma unroll
-    for (int k = 0; k < QPT; ++k) {
-        const int idx = k * kWork + tid, rr = idx / (D / 8), c = idx % (D / 8);
-        if (idx >= QCH) continue;
-        const uint4 u = qv[k];
-        uint4 v;
-        v.x = pack_h2(bf2f(u.x & 0xFFFF) * qmul, bf2f(u.x >> 16) * qmul);
-        v.y = pack_h2(bf2f(u.y & 0xFFFF) * qmul, bf2f(u.y >> 16) * qmul);
-        v.z = pack_h2(bf2f(u.z & 0xFFFF) * qmul, bf2f(u.z >> 16) * qmul);
-        v.w = pack_h2(bf2f(u.w & 0xFFFF) * qmul, bf2f(u.w >> 16) * qmul);
-        const int rb = rr / W, rl = rr % W;
-        *reinterpret_cast<uint4*>(sQ + rb * W * D * 2 + (c / 8) * (W * 128) + (rl / 8) * 1024 +
-                                  (rl % 8) * 128 + (((c % 8) ^ (rl % 8)) * 16)) = v;
-    }
-    const float cf = p.scale_log2 * (*p.kscale) * ldexpf(1.0f, -qe);
 
     // 2. tails of the agents this CTA owns (CUDA cores), overlapping the first
-    //    bulk copies; acc (unnormalised) goes to `out`, m and l to shared memory
-    if (p.tK != nullptr) tail_attention<D>(p, sK, tailml, S, crank, g, row0, nrows);
+    //    copies; the P' area is free until the first softmax
+    if (p.tK != nullptr) tail_attention<D>(p, sP, tailml, S, crank, g, row0, nrows);
+    ptx::fence_proxy_async();
     __syncthreads();
 
-    // 3. main loop over this CTA's tiles
-    const int wq = warp & 3;           // TMEM lane quarter
-    const int cgr = warp >> 2;         // column group
-    const bool has_cols = cgr < NCG;   // warp-uniform
-    const int tok = wq * 32 + lane;    // token (S^T lanes) / channel (O^T lanes)
-    float lp[CPT];                     // per-thread row-sum partials
+    // 3. main loop
+    uint32_t tlo[4], thi[4];
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) lp[j] = 0.f;
+    for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
+    float lp[HW];  // per-thread row-sum partials
+#pragma unroll
+    for (int j = 0; j < HW; ++j) lp[j] = 0.f;
     const uint32_t idesc1 = ptx::idesc_f16(128, W, 0, 0);
-    const uint32_t idesc2 = ptx::idesc_f16(128, W, 1, 1);
-    const uint32_t aK = ptx::smem_u32(sK), aQ = ptx::smem_u32(sQ), aV = ptx::smem_u32(sV),
-                   aP = ptx::smem_u32(sP);
+    const uint32_t idesc2 = ptx::idesc_f16(128, W, 0, 1);
+    const uint32_t aQ = ptx::smem_u32(sQ), aP = ptx::smem_u32(sP);
 
-    for (int i = 0; i < ntile; ++i) {
-        const int s = i % p.nstage;
-        const int buf = i & 1;
-        if (!timed_out && !ptx::mbar_wait(bar_full + 8 * s, (i / p.nstage) & 1, kWaitNs))
+    auto wait_full = [&](int i) {
+        if (!timed_out && !ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs))
             timed_out = true;
-        const unsigned char* rk = sRaw + s * lay.stage + lay.rk;
-        const unsigned char* rv = sRaw + s * lay.stage + lay.rv;
-        const float* rn = reinterpret_cast<const float*>(sRaw + s * lay.stage + lay.rn);
-        // K: 16 int8 per step -> two 16-byte fp16 chunks of the swizzled operand
+    };
+    // K^ of tile i: token row -> fp16 pairs in TMEM columns [cg*D/4, cg*D/4 + D/4)
+    auto convert_k = [&](int i) {
+        const unsigned char* rk = sm + (i % p.nstage) * lay.stage;
+        uint32_t r[D / 4];
 #pragma unroll
-        for (int it = 0; it < (kTile * D / 16 + kConv - 1) / kConv; ++it) {
-            const int q = it * kConv + tid;
-            if (tid >= kConv || q >= kTile * D / 16) break;
-            const int t = q / (D / 16), c16 = q % (D / 16);
-            const uint4 u = *reinterpret_cast<const uint4*>(rk + t * D + c16 * 16);
-            uint4 o0, o1;
-            i8x4_to_h2x2(u.x, o0.x, o0.y);
-            i8x4_to_h2x2(u.y, o0.z, o0.w);
-            i8x4_to_h2x2(u.z, o1.x, o1.y);
-            i8x4_to_h2x2(u.w, o1.z, o1.w);
-            const int dc0 = 2 * c16, dc1 = dc0 + 1;
-            unsigned char* base = sK + (t / 8) * 1024 + (t % 8) * 128;
-            unsigned char* d0 = base + (dc0 / 8) * 16384 + (((dc0 % 8) ^ (t % 8)) * 16);
-            unsigned char* d1 = base + (dc1 / 8) * 16384 + (((dc1 % 8) ^ (t % 8)) * 16);
-            if (c16 < 4) {
-                *reinterpret_cast<uint4*>(d0) = o0;
-                *reinterpret_cast<uint4*>(d1) = o1;
-            } else {
-                *reinterpret_cast<uint4*>(d1) = o1;
-                *reinterpret_cast<uint4*>(d0) = o0;
-            }
+        for (int k = 0; k < KC; ++k) {
+            const int c = cg * KC + k;
+            const int sw = D == 128 ? (tok & 7) : ((tok >> 1) & 3);  // TMA 128 B / 64 B swizzle
+            const uint4 u = *reinterpret_cast<const uint4*>(rk + tok * D + ((c ^ sw) << 4));
+            i8x4_to_h2x2(u.x, r[8 * k + 0], r[8 * k + 1]);
+            i8x4_to_h2x2(u.y, r[8 * k + 2], r[8 * k + 3]);
+            i8x4_to_h2x2(u.z, r[8 * k + 4], r[8 * k + 5]);
+            i8x4_to_h2x2(u.w, r[8 * k + 6], r[8 * k + 7]);
         }
-        // V: task = (token, quarter of 32 channels)
-        for (int task = tid; tid < kConv && task < kTile * D / 32; task += kConv) {
-            const int t = task % kTile, qd = task / kTile;
-            const unsigned char* src = rv + t * VB + qd * 4 * BITS;
-            unsigned char* vrow = sV + buf * 32768 + (qd / 2) * 16384 + (t / 8) * 1024 + (t % 8) * 128;
-            convert_v_quarter<BITS>(src, pairs, vrow, t, (qd % 2) * 4);
-        }
-        const float ns = rn[tok] * vr;  // this thread's token norm, read before the stage is refilled
-        ptx::fence_proxy_async();
-        __syncthreads();  // (A) operands of tile i ready
-        if (warp == kMmaWarp && lane == 0) {
-            if (i + p.nstage < ntile) issue_tile(i + p.nstage);  // stage s is free again
+        if constexpr (D == 128) ptx::tmem_st32(tK + lane_off + cg * 32, r);
+        else ptx::tmem_st16(tK + lane_off + cg * 16, r);
+        ptx::tmem_wait_st();
+    };
+
+    wait_full(0);
+    convert_k(0);
+    ptx::tc_fence_before();
+    __syncthreads();  // K^(0) ready
+    for (int i = 0; i < ntile; ++i) {
+        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
+        if (tid == 0) {  // S^T = K^ Q^T
             ptx::tc_fence_after();
 #pragma unroll
-            for (int rb = 0; rb < NB; ++rb) {
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint64_t ad = ptx::sdesc(aK + (ks / 4) * 16384 + (ks % 4) * 32, 16, 1024);
-                    const uint64_t bd = ptx::sdesc(aQ + rb * W * D * 2 + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
-                    ptx::mma_f16(tS + rb * W, ad, bd, idesc1, ks > 0 ? 1u : 0u);
-                }
+            for (int ks = 0; ks < D / 16; ++ks) {
+                const uint64_t bd = ptx::sdesc(aQ + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
+                ptx::mma_f16_ta(tS, tK + ks * 8, bd, idesc1, ks > 0 ? 1u : 0u);
             }
-            ptx::mma_commit(bar_mma);
+            ptx::mma_commit(bar_s);
         }
-        if (!timed_out && !ptx::mbar_wait(bar_mma, i & 1, kWaitNs)) timed_out = true;
+        // V^T of tile i while MMA1 runs (V^ and P' are free once MMA2(i-1) is done)
+        if (i > 0 && !timed_out && !ptx::mbar_wait(bar_o, (i - 1) & 1, kWaitNs)) timed_out = true;
         ptx::tc_fence_after();
-
-        // softmax, one row block at a time (rows are independent)
         const bool valid = (t_begin + i * kTile + tok) < t_end;
-        float sv[CPT];
-        if (has_cols) {  // all of this thread's scores, one TMEM wait
-#pragma unroll
-            for (int rb = 0; rb < NB; ++rb) {
-                const uint32_t ta = tS + ((uint32_t)(wq * 32) << 16) + rb * W + cgr * HC;
-                if constexpr (HC == 16) {
-                    uint32_t r[16];
-                    ptx::tmem_ld16(ta, r);
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) sv[rb * HC + e] = __uint_as_float(r[e]);
-                } else {
-                    uint32_t r[8];
-                    ptx::tmem_ld8(ta, r);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) sv[rb * HC + e] = __uint_as_float(r[e]);
-                }
-            }
-            ptx::tmem_wait_ld();
+        const float ns = valid ? reinterpret_cast<const float*>(st + lay.rn)[tok] * vr : 0.f;
+        if (has_ch) {
+            uint32_t h[32];
+            const unsigned char* rv = st + lay.rv + tok * (4 * BITS);
+            decode32<BITS>(rv + (2 * cg) * GB, tlo, thi, h);
+            decode32<BITS>(rv + (2 * cg + 1) * GB, tlo, thi, h + 16);
+            ptx::tmem_st32(tV + lane_off + 32 * cg, h);
         }
+
+        // softmax of tile i
+        if (!timed_out && !ptx::mbar_wait(bar_s, i & 1, kWaitNs)) timed_out = true;
+        ptx::tc_fence_after();
+        // logits l = y * cf (log2 units) of this thread's token for its HW rows
+        float l[HW];
+        tmem_ld_cols<HW>(tS + lane_off + cg * HW, l);
+        ptx::tmem_wait_ld();
+        float over = -CUDART_INF_F;
 #pragma unroll
-        for (int rb = 0; rb < NB; ++rb) {
-            const int colb = rb * W + cgr * HC;  // this thread's first column
-            float x[HC], m[HC];
-            float over = -CUDART_INF_F;
+        for (int j = 0; j < HW; j += 4) {
+            const float4 c4 = *reinterpret_cast<const float4*>(sCf + cg * HW + j);
+            const float4 m4 = *reinterpret_cast<const float4*>(sM + cg * HW + j);
+            l[j] = valid ? l[j] * c4.x : -CUDART_INF_F;
+            l[j + 1] = valid ? l[j + 1] * c4.y : -CUDART_INF_F;
+            l[j + 2] = valid ? l[j + 2] * c4.z : -CUDART_INF_F;
+            l[j + 3] = valid ? l[j + 3] * c4.w : -CUDART_INF_F;
+            over = fmaxf(over, fmaxf(fmaxf(l[j] - m4.x, l[j + 1] - m4.y), fmaxf(l[j + 2] - m4.z, l[j + 3] - m4.w)));
+        }
+        // the running maxima sM change only after the tile's last read of them
+        // (below, after the barrier); until then the new maxima are
+        // max(sM, colmax over the four lane quarters)
+        const bool slow = ptx::bar_or(2, kThreads, over > kTau);
+        auto new_max = [&](int col) {
+            return fmaxf(sM[col], fmaxf(fmaxf(colmax[col], colmax[W + col]),
+                                        fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
+        };
+        if (slow) {
+            // exact maxima of this tile's rows, then rescale what was accumulated
 #pragma unroll
-            for (int e = 0; e < HC; ++e) {
-                x[e] = (valid && has_cols) ? sv[rb * HC + e] * cf : -CUDART_INF_F;
-                m[e] = has_cols ? sM[colb + e] : 0.f;
-                over = fmaxf(over, x[e] - m[e]);
+            for (int j = 0; j < HW; ++j) {
+                const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(l[j])));
+                if (lane == (j & 31)) colmax[q * W + cg * HW + j] = mx;
             }
-            if (ptx::bar_or(1, kWork, over > kTau)) {
-                // exact maxima of this tile's rows, then raise the running maxima
-                if (has_cols) {
+            ptx::bar_sync(1, kThreads);
 #pragma unroll
-                    for (int j = 0; j < HC; ++j) {
-                        const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(x[j])));
-                        if (lane == j) colmax[wq * 128 + colb + j] = mx;
-                    }
+            for (int c0 = 0; c0 < HW; c0 += 8) {
+                float alpha[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int col = cg * HW + c0 + e;
+                    const float mo = sM[col];
+                    alpha[e] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2(mo - new_max(col));
+                    lp[c0 + e] *= alpha[e];
                 }
-                ptx::bar_sync(1, kWork);
-                float alpha[HC];
+                if (i > 0 && has_ch) {  // O^T columns (MMA2(i-1) is done)
+                    uint32_t r8[8];
+                    ptx::tmem_ld8(tO + lane_off + cg * HW + c0, r8);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < HC; ++j) {
-                    const int col = colb + j;
-                    float mn = m[j];
-                    if (has_cols)
-                        mn = fmaxf(m[j], fmaxf(fmaxf(colmax[col], colmax[128 + col]),
-                                              fmaxf(colmax[256 + col], colmax[384 + col])));
-                    alpha[j] = (m[j] == -CUDART_INF_F) ? 0.f : ptx::ex2(m[j] - mn);
-                    lp[rb * HC + j] *= alpha[j];
-                    m[j] = mn;
-                }
-                if (i > 0 && has_cols) {  // the MMAs into O^T finished before this tile's S^T
-                    const uint32_t ta = tO + ((uint32_t)(wq * 32) << 16) + colb;
-#pragma unroll
-                    for (int c0 = 0; c0 < HC; c0 += 8) {
-                        uint32_t r8[8];
-                        ptx::tmem_ld8(ta + c0, r8);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            r8[e] = __float_as_uint(__uint_as_float(r8[e]) * alpha[c0 + e]);
-                        ptx::tmem_st8(ta + c0, r8);
-                    }
-                    ptx::tmem_wait_st();
-                }
-                ptx::bar_sync(1, kWork);  // every compute thread has read sM and colmax
-                if (has_cols && wq == 0 && lane == 0) {
-#pragma unroll
-                    for (int j = 0; j < HC; ++j) sM[colb + j] = m[j];
-                }
-            }
-            // P'^T = p * n_t / nref as fp16 hi + lo (MN-major: one 128-byte row per
-            // token) and the row-sum partials of p
-            if (has_cols) {
-#pragma unroll
-                for (int c0 = 0; c0 < HC; c0 += 8) {
-                    float hi[8], lo[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float pv = valid ? ptx::ex2(x[c0 + e] - m[c0 + e]) : 0.f;
-                        lp[rb * HC + c0 + e] += pv;
-                        const float pp = pv * ns;
-                        hi[e] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
-                        lo[e] = pp - hi[e];                                          // exact
-                    }
-                    const int chunk = (cgr * HC + c0) / 8;
-                    const int off = (tok / 8) * 1024 + (tok % 8) * 128 + ((chunk ^ (tok % 8)) * 16);
-                    *reinterpret_cast<uint4*>(sP + rb * 32768 + off) =
-                        make_uint4(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]), pack_h2(hi[4], hi[5]),
-                                   pack_h2(hi[6], hi[7]));
-                    *reinterpret_cast<uint4*>(sP + rb * 32768 + 16384 + off) =
-                        make_uint4(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]), pack_h2(lo[4], lo[5]),
-                                   pack_h2(lo[6], lo[7]));
+                    for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(r8[e]) * alpha[e]);
+                    ptx::tmem_st8(tO + lane_off + cg * HW + c0, r8);
                 }
             }
         }
+        // P'^T = p * n_t / nref as fp16 hi + lo, MN-major (one 128-byte swizzled
+        // row of 64 query rows per token), and the row-sum partials of p
+#pragma unroll
+        for (int c0 = 0; c0 < HW; c0 += 8) {
+            float hi[8], lo[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int col = cg * HW + c0 + e;
+                const float mc = slow ? new_max(col) : sM[col];
+                const float pv = ptx::ex2(l[c0 + e] - mc);  // 0 for invalid tokens
+                lp[c0 + e] += pv;
+                const float pp = pv * ns;
+                hi[e] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
+                lo[e] = pp - hi[e];                                          // exact
+            }
+            const int col0 = cg * HW + c0;
+            const int off = (col0 >> 6) * 16384 + (tok >> 3) * 1024 + (tok & 7) * 128 +
+                            ((((col0 & 63) >> 3) ^ (tok & 7)) << 4);
+            *reinterpret_cast<uint4*>(sP + off) =
+                make_uint4(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]), pack_h2(hi[4], hi[5]), pack_h2(hi[6], hi[7]));
+            *reinterpret_cast<uint4*>(sP + lay.plo + off) =
+                make_uint4(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]), pack_h2(lo[4], lo[5]), pack_h2(lo[6], lo[7]));
+        }
+        ptx::tmem_wait_st();  // V^T (and any O^T rescale) stores
         ptx::fence_proxy_async();
         ptx::tc_fence_before();
-        __syncthreads();  // (B) P of tile i ready
-        if (warp == kMmaWarp && lane == 0) {  // overlaps the other warps' next conversion
+        __syncthreads();  // P'(i) and V^T(i) ready; raw stage of tile i consumed
+        if (slow && q == 0 && lane == 0) {  // every read of sM for this tile is done
+#pragma unroll 4
+            for (int j = 0; j < HW; ++j) sM[cg * HW + j] = new_max(cg * HW + j);
+        }
+        if (tid == 0) {  // O^T += V^T (P'_hi + P'_lo)^T, then refill the stage
             ptx::tc_fence_after();
 #pragma unroll
-            for (int rb = 0; rb < NB; ++rb) {
-#pragma unroll
-                for (int ks = 0; ks < kTile / 16; ++ks) {
-                    const uint64_t ad = ptx::sdesc(aV + buf * 32768 + ks * 2048, 16384, 1024);
-                    const uint64_t bh = ptx::sdesc(aP + rb * 32768 + ks * 2048, 16384, 1024);
-                    const uint64_t bl = ptx::sdesc(aP + rb * 32768 + 16384 + ks * 2048, 16384, 1024);
-                    ptx::mma_f16(tO + rb * W, ad, bh, idesc2, (i > 0 || ks > 0) ? 1u : 0u);
-                    ptx::mma_f16(tO + rb * W, ad, bl, idesc2, 1u);
-                }
+            for (int ks = 0; ks < kTile / 16; ++ks) {
+                const uint64_t bh = ptx::sdesc(aP + ks * 2048, 16384, 1024);
+                const uint64_t bl = ptx::sdesc(aP + lay.plo + ks * 2048, 16384, 1024);
+                ptx::mma_f16_ta(tO, tV + ks * 8, bh, idesc2, (i > 0 || ks > 0) ? 1u : 0u);
+                ptx::mma_f16_ta(tO, tV + ks * 8, bl, idesc2, 1u);
             }
+            ptx::mma_commit(bar_o);
+            if (i + p.nstage < ntile) issue_tile(i + p.nstage);
+        }
+        if (i + 1 < ntile) {  // K^(i+1) while MMA2(i) runs (MMA1(i) has finished with K^)
+            wait_full(i + 1);
+            convert_k(i + 1);
+            ptx::tc_fence_before();
+            __syncthreads();
         }
     }
-    if (ntile > 0) {
-        if (warp == kMmaWarp && lane == 0) ptx::mma_commit(bar_mma);
-        if (!timed_out && !ptx::mbar_wait(bar_mma, ntile & 1, kWaitNs)) timed_out = true;
-        ptx::tc_fence_after();
-    }
-    if (warp == kMmaWarp && lane == 0 && timed_out) {
-        // give the copies still in flight a bounded chance to land before exit
+    if (!timed_out && !ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
+    ptx::tc_fence_after();
+    if (tid == 0 && timed_out) {
+        // give the copies still in flight a bounded chance to land before the
+        // stages are reused and the CTA exits
         for (int i = max(0, ntile - p.nstage); i < ntile; ++i)
             ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs);
     }
 
-    // 4. epilogue: row sums and O^T to shared memory (sM already holds the maxima)
-    warp_reduce_scatter<CPT>(lp, lane);
+    // 4. epilogue: row sums and O^T into registers, TMEM released
+    warp_reduce_scatter<HW>(lp, lane);
     {
-        constexpr int KEEP = CPT >= 32 ? CPT / 32 : 1;  // sums kept per lane
-        constexpr int REP = CPT >= 32 ? 1 : 32 / CPT;    // lanes holding the same sum
+        constexpr int KEEP = HW >= 32 ? HW / 32 : 1;  // sums kept per lane
+        constexpr int REP = HW >= 32 ? 1 : 32 / HW;    // lanes holding the same sum
 #pragma unroll
         for (int k = 0; k < KEEP; ++k) {
-            const int j = lane / REP * KEEP + k;
-            const int col = (j / HC) * W + cgr * HC + (j % HC);
-            if (has_cols && lane % REP == 0) lsum[wq * 128 + col] = lp[k];
+            const int col = cg * HW + lane / REP * KEEP + k;
+            if (lane % REP == 0) lsum[q * W + col] = lp[k];
         }
     }
-    __syncthreads();  // all MMAs have completed; sO may now alias the operands
-    if (tid < RG) sL[tid] = ntile > 0 ? lsum[tid] + lsum[128 + tid] + lsum[256 + tid] + lsum[384 + tid] : 0.f;
-    if (ntile > 0 && has_cols && wq * 32 < D) {  // warp-uniform
+    float o[HW];
+    if (has_ch) {
+        tmem_ld_cols<HW>(tO + lane_off + cg * HW, o);
+        ptx::tmem_wait_ld();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kCols);
+    }
+    if (tid < nrows) sL[tid] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
+    if (timed_out && lane == 0) atomicOr(p.status, kStTimeout);
+    ptx::cluster_arrive();  // every CTA of the cluster is past its main loop:
+    ptx::cluster_wait();    // the stage / Q / P' areas become merge slots
+
+    // 5. push the partial rows to their owners: slot (source rank, row of the
+    //    owner) holds O^T[:, row] and (m, l)
+    float* slots = reinterpret_cast<float*>(sm);         // [S][own][D]
+    float* slotml = slots + (size_t)S * p.own * D;        // [S][own][2]
+    if (has_ch) {
 #pragma unroll
-        for (int rb = 0; rb < NB; ++rb) {
-#pragma unroll
-            for (int c0 = 0; c0 < HC; c0 += 8) {
-                uint32_t r8[8];
-                ptx::tmem_ld8(tO + ((uint32_t)(wq * 32) << 16) + rb * W + cgr * HC + c0, r8);
-                ptx::tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    sO[(rb * W + cgr * HC + c0 + e) * D + tok] = __uint_as_float(r8[e]);
+        for (int j = 0; j < HW; ++j) {
+            const int r = cg * HW + j;
+            if (r < nrows) {
+                const uint32_t ow = sOwn[r];
+                const float* dst = slots + ((size_t)(crank * p.own + (int)(ow & 0xFFFF)) * D + tok);
+                ptx::st_dsmem(ptx::dsmem_addr(dst, ow >> 16), o[j]);
             }
         }
     }
-    if (timed_out) atomicOr(p.status, kStTimeout);
-    ptx::tc_fence_before();
-    cluster.sync();  // every CTA's partial is in its shared memory
+    if (tid < nrows) {
+        const uint32_t ow = sOwn[tid];
+        const float* dst = slotml + (size_t)(crank * p.own + (int)(ow & 0xFFFF)) * 2;
+        ptx::st_dsmem2(ptx::dsmem_addr(dst, ow >> 16), sM[tid], sL[tid]);
+    }
+    ptx::cluster_arrive();
+    ptx::cluster_wait();
 
-    // 5. merge the splits for the rows of owned agents (agent % S == rank),
-    //    one warp per row; the walk steps over owned agents only, so the
-    //    integer divisions happen once per CTA
+    // 6. merge the owned rows, one warp per row
     {
         const int G = p.G;
-        const int a_first = row0 / G, a_last = (row0 + nrows - 1) / G;
-        int item = 0;
-        for (int a = a_first + ((crank - a_first % S) % S + S) % S; a <= a_last; a += S)
-        for (int j = max(0, row0 - a * G); j < min(G, row0 + nrows - a * G); ++j) {
-            if ((item++ % (kWork / 32)) != warp) continue;
-            const int rr = a * G + j - row0;
-            // lane s fetches CTA s's running maximum and row sum
+        for (int loc = warp; loc < p.own; loc += kThreads / 32) {
+            const int ar = (loc / G) * S + crank, j = loc % G;
+            const int rr = ar * G + j;
+            if (rr >= nrows) break;  // rr grows with loc
+            const int a = row0 / G + ar;
             float Ms = -CUDART_INF_F, Ls = 0.f;
             if (lane < S) {
-                Ms = ptx::ld_dsmem(ptx::dsmem_addr(sM + rr, lane));
-                Ls = ptx::ld_dsmem(ptx::dsmem_addr(sL + rr, lane));
+                const float2 ml = *reinterpret_cast<const float2*>(slotml + (size_t)(lane * p.own + loc) * 2);
+                Ms = ml.x;
+                Ls = ml.y;
             }
             float M = (Ls > 0.f) ? Ms : -CUDART_INF_F;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+            for (int o2 = 16; o2; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
             const float wl = (Ls > 0.f) ? ptx::ex2(Ms - M) : 0.f;
             float L = wl * Ls;
 #pragma unroll
-            for (int o = 16; o; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-            // partial rows are fetched 8 CTAs at a time, all loads before any use
+            for (int o2 = 16; o2; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
             float acc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-#pragma unroll
-            for (int s0 = 0; s0 < 16; s0 += 8) {
-                if (s0 >= S) break;
-                // unconditional loads (ranks past S re-read the last CTA and get
-                // weight 0) so that all eight are in flight before any is used
-                float part[8][EPL];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t ra = ptx::dsmem_addr(sO + rr * D + lane * EPL, min(s0 + k, S - 1));
-                    if constexpr (EPL == 4) {
-                        const float4 v = ptx::ld_dsmem4(ra);
-                        part[k][0] = v.x; part[k][1] = v.y; part[k][2] = v.z; part[k][3] = v.w;
-                    } else {
-                        const float2 v = ptx::ld_dsmem2(ra);
-                        part[k][0] = v.x; part[k][1] = v.y;
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float w = __shfl_sync(0xffffffffu, wl, s0 + k);
-#pragma unroll
-                    for (int e = 0; e < EPL; ++e) acc[e] = fmaf(w, part[k][e], acc[e]);
+            for (int s = 0; s < S; ++s) {
+                const float w = __shfl_sync(0xffffffffu, wl, s);
+                const float* src = slots + (size_t)(s * p.own + loc) * D + lane * EPL;
+                if constexpr (EPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+                    acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
                 }
             }
             // inverse rotation H acc; lane holds EPL consecutive channels
@@ -770,17 +788,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
                 }
             }
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const bool upper = (lane & o) != 0;
+            for (int o2 = 1; o2 < 32; o2 <<= 1) {
+                const bool upper = (lane & o2) != 0;
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) {
-                    const float other = __shfl_xor_sync(0xffffffffu, acc[e], o);
+                    const float other = __shfl_xor_sync(0xffffffffu, acc[e], o2);
                     acc[e] = upper ? other - acc[e] : acc[e] + other;
                 }
             }
             const float oscale = nref / (float)D * p.inv_lam;
             float mt = -CUDART_INF_F, lt = 0.f;
-            float* orow = p.out + ((long long)a * p.Hq + g * p.G + j) * D + lane * EPL;
+            float* orow = p.out + ((long long)a * p.Hq + g * G + j) * D + lane * EPL;
             float tacc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) tacc[e] = 0.f;
@@ -800,28 +818,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const TcParams p
             for (int e = 0; e < EPL; ++e) orow[e] = (acc[e] * oscale * wp + tacc[e] * wt) * inv;
         }
     }
-    cluster.sync();  // remote shared memory stays valid until every CTA has read it
-    ptx::tc_fence_after();
-    if (warp == 0) ptx::tmem_dealloc(tmem, p.tmem_cols);
 }
 
-template <int D, int W, int NB, int BITS>
+template <int D, int W, int BITS>
 void configure() {
     static bool done = false;
     if (done) return;
-    auto kern = attend_tc_kernel<D, W, NB, BITS>;
+    auto kern = attend_tc_kernel<D, W, BITS>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     done = true;
 }
 
 // How many clusters of S CTAs with `smem` bytes each can be resident at once.
-template <int D, int W, int NB, int BITS>
+template <int D, int W, int BITS>
 int max_clusters(int S, size_t smem) {
     static int cache[17][2] = {};  // [S] -> (smem key / 1024 + 1, count)
     const int key = (int)(smem / 1024) + 1;
     if (cache[S][0] == key) return cache[S][1];
-    configure<D, W, NB, BITS>();
+    configure<D, W, BITS>();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -834,7 +849,7 @@ int max_clusters(int S, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel<D, W, NB, BITS>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel<D, W, BITS>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -843,17 +858,32 @@ int max_clusters(int S, size_t smem) {
     return n;
 }
 
-template <int D, int W, int NB, int BITS>
-cudaError_t launch_cfg(TcParams prm, int ntiles, int Hk, int RGN, size_t smem, cudaStream_t st) {
-    configure<D, W, NB, BITS>();
-    // cluster size: fewest (waves x tiles per CTA), then the larger cluster
+template <int D, int W, int BITS>
+cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
+    configure<D, W, BITS>();
+    // shared memory: as many raw stages as fit (no more than a CTA has tiles),
+    // and a floor that keeps the CTAs per SM within what TMEM holds (2 x 256
+    // columns, or 1 x 512): a CTA waiting in tcgen05.alloc for a cluster peer
+    // on its own SM would never run
+    const uint32_t cap = (W <= 64 ? 112u : 227u) * 1024;
+    const size_t floor_bytes = W <= 64 ? 80 * 1024 : 116 * 1024;
+    int max_stage = W <= 64 ? 2 : 4;
+    while (max_stage > 1 && make_layout(D, BITS, W, max_stage).total + 1024 > cap) --max_stage;
+    // cluster size: fewest (waves x tiles per CTA), then the larger cluster;
+    // the merge slots must fit below the misc area of the layout the CTA uses
+    const int rows_cta = std::min(W, prm.R);
+    const int agents_cta = (rows_cta + prm.G - 1) / prm.G;
     const int clusters = Hk * RGN;
-    int bestS = 1;
+    int bestS = 0;
     long long best = -1;
     for (int S = 1; S <= 16 && S <= ntiles; ++S) {
-        const int n = max_clusters<D, W, NB, BITS>(S, smem);
-        if (n < 1) continue;
         const int per = (ntiles + S - 1) / S;
+        const Layout lay = make_layout(D, BITS, W, std::min(max_stage, per));
+        const size_t smem = std::max<size_t>(lay.total + 1024, floor_bytes);
+        const int own = (agents_cta + S - 1) / S * prm.G;
+        if ((size_t)S * own * (D + 2) * 4 > lay.misc) continue;
+        const int n = max_clusters<D, W, BITS>(S, smem);
+        if (n < 1) continue;
         const long long waves = (clusters + n - 1) / n;
         const long long cost = waves * per;
         if (best < 0 || cost <= best) {
@@ -861,9 +891,15 @@ cudaError_t launch_cfg(TcParams prm, int ntiles, int Hk, int RGN, size_t smem, c
             bestS = S;
         }
     }
+    if (bestS == 0) return cudaErrorInvalidConfiguration;
     const int per = (ntiles + bestS - 1) / bestS;
     const int S = (ntiles + per - 1) / per;
     prm.tps = per * kTile;
+    prm.nstage = std::min(max_stage, per);
+    prm.own = (agents_cta + S - 1) / S * prm.G;
+    const Layout lay = make_layout(D, BITS, W, prm.nstage);
+    const size_t smem = std::max<size_t>(lay.total + 1024, floor_bytes);
+    if ((size_t)S * prm.own * (D + 2) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, Hk, RGN);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -878,7 +914,7 @@ cudaError_t launch_cfg(TcParams prm, int ntiles, int Hk, int RGN, size_t smem, c
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attend_tc_kernel<D, W, NB, BITS>, prm);
+    return cudaLaunchKernelEx(&cfg, attend_tc_kernel<D, W, BITS>, kmap, prm);
 }
 
 }  // namespace
@@ -888,16 +924,16 @@ template <int BITS>
 cudaError_t launch_attend_tc_bits(const Shape& s, const LayerBufs& L, const AttendArgs& a,
                                   int* status, cudaStream_t st) {
     const int D = s.head_dim;
-    int CPT;
-    if (a.rows <= 16) CPT = 8;
-    else if (a.rows <= 32) CPT = 16;
-    else if (a.rows <= 64) CPT = 32;
-    else CPT = 64;
-    const int W = CPT >= 32 ? 64 : 2 * CPT, NB = 2 * CPT / W, RG = NB * W;
-    const int RGN = (a.rows + RG - 1) / RG;
+    int W;
+    if (a.rows <= 16) W = 16;
+    else if (a.rows <= 32) W = 32;
+    else if (a.rows <= 64) W = 64;
+    else W = 128;
+    // row groups of W rows must hold whole agents
+    if (a.rows > W && W % a.group != 0) return cudaErrorInvalidValue;
+    const int RGN = (a.rows + W - 1) / W;
     const int ntiles = (s.ctx + kTile - 1) / kTile;
     TcParams prm = {};
-    prm.kq = L.kq;
     prm.vcodes = L.vcodes;
     prm.vnorm = L.vnorm;
     prm.kscale = L.kscale;
@@ -909,37 +945,31 @@ cudaError_t launch_attend_tc_bits(const Shape& s, const LayerBufs& L, const Atte
     prm.Hq = a.q_heads;
     prm.G = a.group;
     prm.R = a.rows;
-    prm.agents = a.agents;
     prm.tK = (const uint16_t*)a.tailK;
     prm.tV = (const uint16_t*)a.tailV;
     prm.tlen = a.tail_len;
     prm.tail_max = a.tail_max;
     prm.out = a.out;
     prm.scale_log2 = a.scale_log2;
-    prm.bits = BITS;
+    prm.early = a.early;
     prm.status = status;
     const Codebook& cb = codebook(BITS);
-    for (int k = 0; k < 8; ++k) prm.c16[k] = (uint32_t)cb.c16[2 * k] | ((uint32_t)cb.c16[2 * k + 1] << 16);
-    prm.inv_lam = 1.0f / cb.lam;
-    uint32_t cols = 2 * NB * W;
-    uint32_t tc = 32;
-    while (tc < cols) tc <<= 1;
-    prm.tmem_cols = tc;
-    int nstage = 3;
-    Layout lay = make_layout(D, BITS, W, NB, nstage);
-    while (lay.total + 1024 > 227 * 1024 && nstage > 1) lay = make_layout(D, BITS, W, NB, --nstage);
-    prm.nstage = nstage;
-    const size_t smem = lay.total + 1024;
-    if (D == 64) {
-        if (CPT == 8) return launch_cfg<64, 16, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-        if (CPT == 16) return launch_cfg<64, 32, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-        if (CPT == 32) return launch_cfg<64, 64, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-        return launch_cfg<64, 64, 2, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
+    for (int k = 0; k < 16; ++k) {
+        prm.tlo[k / 4] |= (uint32_t)(cb.c16[k] & 0xFF) << (8 * (k % 4));
+        prm.thi[k / 4] |= (uint32_t)(cb.c16[k] >> 8) << (8 * (k % 4));
     }
-    if (CPT == 8) return launch_cfg<128, 16, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-    if (CPT == 16) return launch_cfg<128, 32, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-    if (CPT == 32) return launch_cfg<128, 64, 1, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
-    return launch_cfg<128, 64, 2, BITS>(prm, ntiles, s.kv_heads, RGN, smem, st);
+    prm.inv_lam = 1.0f / cb.lam;
+    const CUtensorMap& km = *L.kmap;
+    if (D == 64) {
+        if (W == 16) return launch_cfg<64, 16, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+        if (W == 32) return launch_cfg<64, 32, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+        if (W == 64) return launch_cfg<64, 64, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+        return launch_cfg<64, 128, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+    }
+    if (W == 16) return launch_cfg<128, 16, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+    if (W == 32) return launch_cfg<128, 32, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+    if (W == 64) return launch_cfg<128, 64, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+    return launch_cfg<128, 128, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
 }
 
 }  // namespace kvp

@@ -7,8 +7,9 @@
 // pool avoids.
 //
 // One kernel, grid (blocks, kv heads):
-//   V blocks: D/32 threads per head-vector, 32 coordinates each: unpack the
-//     slice's codes, look the centroids up in a shared-memory table, FWHT in
+//   V blocks: the block's code groups are unpacked into bytes [token]
+//     [coordinate] in shared memory; then D/32 threads per head-vector, 32
+//     coordinates each, look the centroids up in a shared-memory table, FWHT in
 //     the encoder's stage order (h < 32 in registers, h = 32, 64 by
 //     shfl.xor), V_i = bf16(fl(fl(z_i * n) * (1/d))), coalesced 16-byte stores.
 //   K blocks: K = bf16(fl(q * s)), 16 elements per thread.
@@ -35,8 +36,6 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
                   int ctx_pad, int nbv, uint4* __restrict__ Kout, uint4* __restrict__ Vout,
                   Codebook cb) {
     constexpr int TPV = D / 32;
-    constexpr int VB = D * BITS / 8;
-    constexpr int TB = 4 * BITS;
     constexpr uint32_t MASK = (1u << BITS) - 1;
     const int tid = threadIdx.x;
     const long long head = blockIdx.y;
@@ -61,27 +60,39 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
         return;
     }
     // ---- V = bf16(fl(fl(z * n) * (1/d))), z = FWHT(c[codes])
+    // the block's code groups (pool layout: per 32 tokens, one sequence per
+    // coordinate) are unpacked into bytes [token][coordinate] first
+    constexpr int VPB = kDecThreads / TPV;  // head-vectors per block (a multiple of 32)
     __shared__ float cen[16];
+    __shared__ __align__(16) uint8_t codes8[VPB * D];
     if (tid < 16) cen[tid] = cb.c[tid];
+    {
+        const int gq = tid / D, c = tid % D;
+        const long long grp = (head * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
+        const uint32_t* in = reinterpret_cast<const uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+        uint32_t w[BITS + 1];
+#pragma unroll
+        for (int k = 0; k < BITS; ++k) w[k] = __ldg(in + k);
+        w[BITS] = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int bit = j * BITS;
+            codes8[(gq * 32 + j) * D + c] = (uint8_t)(__funnelshift_r(w[bit / 32], w[bit / 32 + 1], bit % 32) & MASK);
+        }
+    }
     __syncthreads();
     const int lt = tid % TPV;
-    const int t = blockIdx.x * (kDecThreads / TPV) + tid / TPV;
+    const int t = blockIdx.x * VPB + tid / TPV;
     const bool live = t < ctx;
     const unsigned gmask = 0xffffffffu;
     const long long src = head * ctx_pad + (live ? t : 0);
-    uint32_t words[BITS + 1];
-    const uint32_t* in = reinterpret_cast<const uint32_t*>(vcodes + src * VB + lt * TB);
-#pragma unroll
-    for (int w = 0; w < BITS; ++w) words[w] = live ? __ldg(in + w) : 0u;
-    words[BITS] = 0;
+    const uint4* c8 = reinterpret_cast<const uint4*>(codes8 + (tid / TPV) * D + lt * 32);
+    const uint4 ca = c8[0], cb8 = c8[1];
+    const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb8.x, cb8.y, cb8.z, cb8.w};
     const float n = live ? __ldg(vnorm + src) : 0.f;
     float x[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const int bit = i * BITS, w = bit / 32, off = bit % 32;
-        const uint32_t code = __funnelshift_r(words[w], words[w + 1], off) & MASK;
-        x[i] = cen[code];
-    }
+    for (int i = 0; i < 32; ++i) x[i] = cen[(cw[i / 4] >> (8 * (i % 4))) & 0xFF];
 #pragma unroll
     for (int h = 1; h < 32; h <<= 1) {
 #pragma unroll

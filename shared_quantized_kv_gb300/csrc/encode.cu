@@ -16,8 +16,11 @@
 //     Per vector: the norm by the pairwise tree (the first levels cross
 //     threads by shuffles), the FWHT (stages h < 32 in registers, h = 32, 64
 //     by shfl.xor), one float32 threshold per midpoint (m_j * n), the codes by
-//     a branchless binary search over the sorted thresholds, and the packed
-//     bits of the thread's 32 codes (4*BITS bytes, byte aligned).
+//     a branchless binary search over the sorted thresholds. The codes are
+//     then regrouped through shared memory into the pool layout: per group of
+//     32 tokens, one packed sequence per coordinate (the 32 tokens' codes in
+//     token order, 4*BITS bytes), so that a reader holding one coordinate of
+//     many tokens finds them in consecutive bytes.
 //   encode_k_pack: s = max|K| / 127, q = clamp(rint(k / s), -127, 127), 16
 //     elements per thread. k / s is formed as k * (1/s) and the correctly
 //     rounded quotient is recomputed with an IEEE division only when the
@@ -88,9 +91,9 @@ encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, i
                      uint32_t* __restrict__ scratch, int* __restrict__ status, Codebook cb) {
     constexpr int TPV = D / 32;          // threads per head-vector
     constexpr int L = 1 << BITS;
-    constexpr int VB = D * BITS / 8;     // packed bytes per head-vector
-    constexpr int TB = 4 * BITS;         // packed bytes per thread (32 codes)
     __shared__ uint32_t red[2][kEncThreads / 32];
+    constexpr int VPB = kEncThreads / TPV;  // head-vectors per block (a multiple of 32)
+    __shared__ __align__(16) uint8_t codes8[VPB * D];
     const int tid = threadIdx.x, lane = tid % 32;
     const int lt = tid % TPV;            // this thread's 32-coordinate slice
     const int t = blockIdx.x * (kEncThreads / TPV) + tid / TPV;  // token
@@ -173,30 +176,46 @@ encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, i
         }
     }
 
-    // 4. thresholds m_j * n, 5. codes = number of thresholds exceeded
+    // 4. thresholds m_j * n, 5. codes = number of thresholds exceeded (0 past the context)
     float tau[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) tau[j] = (j < L - 1) ? __fmul_rn(cb.m[j], n) : 0.f;
-    uint32_t words[BITS];
+    uint32_t cw[8];
 #pragma unroll
-    for (int w = 0; w < BITS; ++w) words[w] = 0;
+    for (int w = 0; w < 8; ++w) cw[w] = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-        const uint32_t code = bucket<L>(x[i], tau);
-        const int bit = i * BITS, w = bit / 32, off = bit % 32;
-        words[w] |= code << off;
-        if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
+        const uint32_t code = live ? bucket<L>(x[i], tau) : 0u;
+        cw[i / 4] |= code << (8 * (i % 4));
     }
-
-    // 6. store codes (this slice's 4*BITS bytes) and the norm at the padded position
-    if (!live) return;
-    const long long dst = (long long)blockIdx.y * ctx_pad + t;
-    uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + dst * VB + lt * TB);
-#pragma unroll
-    for (int w = 0; w < BITS; ++w) out[w] = words[w];
-    if (lt == 0) {
-        vnorm[dst] = n;
+    // this slice's codes as bytes [token][coordinate] in shared memory
+    uint4* c8 = reinterpret_cast<uint4*>(codes8 + (tid / TPV) * D + lt * 32);
+    c8[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+    c8[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+    if (live && lt == 0) {
+        vnorm[(long long)blockIdx.y * ctx_pad + t] = n;
         if (!isfinite(n)) atomicOr(status, kStNonfinite);
+    }
+    __syncthreads();
+
+    // 6. pool layout: one thread per (32-token group of this block, coordinate)
+    //    packs the group's 32 codes of that coordinate, in token order
+    {
+        const int gq = tid / D, c = tid % D;
+        uint32_t words[BITS + 1];
+#pragma unroll
+        for (int w = 0; w <= BITS; ++w) words[w] = 0;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const uint32_t code = codes8[(gq * 32 + j) * D + c];
+            const int bit = j * BITS, w = bit / 32, off = bit % 32;
+            words[w] |= code << off;
+            if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
+        }
+        const long long grp = ((long long)blockIdx.y * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
+        uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+#pragma unroll
+        for (int w = 0; w < BITS; ++w) out[w] = words[w];
     }
 }
 

@@ -4,12 +4,13 @@
 //
 // Memory layout of a pool (one cudaMalloc, every region 256-byte aligned):
 //   per layer l:  kq     int8  [Hk][ctx_pad][D]
-//                 vcodes uint8 [Hk][ctx_pad][D*bits_l/8]
+//                 vcodes uint8 [Hk][ctx_pad/32][D][4*bits_l] (32-token groups)
 //                 vnorm  f32   [Hk][ctx_pad]
 //   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits (encode
 //   scratch), largest V norm float bits}, status int32.
 // Attention needs no scratch: the CTAs of a cluster merge their context
-// splits through distributed shared memory.
+// splits through distributed shared memory. Each layer also has a TMA tensor
+// map of its kq (rows of head_dim bytes) for the attention kernel.
 // ctx_pad rounds the token axis up to a multiple of 128 so tiles never leave a
 // layer; the padding is zeroed once and never counted as tokens.
 #include <math.h>
@@ -142,6 +143,11 @@ struct kvpool {
     std::vector<int> bits;
     std::vector<size_t> off_kq, off_vc, off_vn;
     std::vector<unsigned char> compressed;
+    // 1 while the layer was written (compress, import, reset) after the last
+    // attend launched on it: that attend must not read the layer before its
+    // grid-dependency wait
+    std::vector<unsigned char> fresh;
+    std::vector<CUtensorMap> kmaps;
     unsigned char* base = nullptr;
     size_t bytes = 0;
     float* kscale = nullptr;
@@ -152,7 +158,7 @@ struct kvpool {
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
                 reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
-                kabsmax + 2 * l + 1};
+                kabsmax + 2 * l + 1, &kmaps[l]};
     }
 };
 
@@ -167,6 +173,43 @@ int map_cuda(cudaError_t e) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// cuTensorMapEncodeTiled, fetched from the driver at run time (the library
+// does not link libcuda).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                 CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                 CUtensorMapFloatOOBfill);
+EncodeTiled tensor_map_encoder() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(f);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// kq of one layer as a 2-D tensor of Hk*ctx_pad rows of D bytes; boxes of 128
+// rows land in shared memory with the 128-byte (D = 128) or 64-byte (D = 64)
+// swizzle that the attention kernel reads.
+bool make_kmap(CUtensorMap* map, void* kq, int D, long long rows) {
+    EncodeTiled enc = tensor_map_encoder();
+    if (!enc) return false;
+    const cuuint64_t gdim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)D};
+    const cuuint32_t box[2] = {(cuuint32_t)D, 128};
+    const cuuint32_t estride[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, kq, gdim, gstride, box, estride,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int check_layer(const kvpool* p, int layer) {
     if (!p || layer < 0 || layer >= p->layers) return KVPOOL_ERR_INVALID_ARG;
@@ -253,6 +296,15 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
     p->status = reinterpret_cast<int*>(p->base + off_status);
+    p->fresh.assign(layers, 1);
+    p->kmaps.resize(layers);
+    for (int l = 0; l < layers; ++l) {
+        if (!make_kmap(&p->kmaps[l], p->base + p->off_kq[l], head_dim, (long long)nvec)) {
+            cudaFree(p->base);
+            delete p;
+            return KVPOOL_ERR_UNSUPPORTED;
+        }
+    }
     kvp::codebook(2);  // derive the tables now, not inside a stream capture
     *out = p;
     return KVPOOL_OK;
@@ -274,6 +326,7 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     p->compressed[layer] = 1;
+    p->fresh[layer] = 1;
     return KVPOOL_OK;
 }
 
@@ -307,8 +360,10 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     a.out = out;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
+    a.early = p->fresh[layer] ? 0 : 1;
     cudaError_t e = kvp::launch_attend_tc(p->shape(), p->layer(layer), a, p->status, p->sm_count,
                                           static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) p->fresh[layer] = 0;
     return map_cuda(e);
 }
 
@@ -352,6 +407,7 @@ int kvpool_reset_layer(kvpool_t* p, int layer) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
     p->compressed[layer] = 0;
+    p->fresh[layer] = 1;
     return KVPOOL_OK;
 }
 
@@ -380,7 +436,8 @@ int copy_layer(const kvpool* p, int layer, bool to_pool, void* kq, void* vc, voi
     const size_t rows = (size_t)p->kv_heads;
     const size_t kw = (size_t)p->ctx * p->head_dim, kp = (size_t)p->ctx_pad * p->head_dim;
     const size_t vb = (size_t)p->head_dim * L.bits / 8;
-    const size_t vw = (size_t)p->ctx * vb, vp = (size_t)p->ctx_pad * vb;
+    // V codes travel in whole 32-token groups (the pool layout)
+    const size_t vw = (size_t)((p->ctx + 31) / 32 * 32) * vb, vp = (size_t)p->ctx_pad * vb;
     const size_t nw = (size_t)p->ctx * 4, np_ = (size_t)p->ctx_pad * 4;
     cudaError_t e = cudaSuccess;
     if (kq && e == cudaSuccess)
@@ -419,6 +476,7 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
                     static_cast<cudaStream_t>(stream));
     if (rc != KVPOOL_OK) return rc;
     rc = map_cuda(kvp::launch_norm_max(p->shape(), p->layer(layer), static_cast<cudaStream_t>(stream)));
+    p->fresh[layer] = 1;
     if (rc == KVPOOL_OK) p->compressed[layer] = 1;
     return rc;
 }

@@ -1,6 +1,7 @@
 // Internal declarations shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>  // CUtensorMap (the encode entry point is fetched at run time)
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -33,12 +34,13 @@ const Codebook& codebook(int bits);
 // Device buffers of one layer.
 struct LayerBufs {
     int8_t* kq;        // [Hk][ctx_pad][D]
-    uint8_t* vcodes;   // [Hk][ctx_pad][D*bits/8]
+    uint8_t* vcodes;   // [Hk][ctx_pad/32][D][4*bits]: per 32-token group, one code sequence per coordinate
     float* vnorm;      // [Hk][ctx_pad]
     float* kscale;     // 1 float
     uint32_t* kabsmax; // 1 word: bf16 bits of max|K| (scratch of the encode)
     int bits;
     uint32_t* vnmax;   // 1 word right after kabsmax: float bits of the largest V norm
+    const CUtensorMap* kmap;  // TMA map of kq as rows of D bytes (128 / 64-byte swizzle), or null
 };
 
 struct Shape {
@@ -63,6 +65,7 @@ struct AttendArgs {
     int tail_max;
     float* out;          // f32 [A][Hq][D]
     float scale_log2;    // softmax scale * log2(e)
+    int early;           // 1: no kernel before this one in the stream writes the layer
 };
 
 struct AttendScratch {

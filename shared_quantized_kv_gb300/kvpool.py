@@ -208,7 +208,8 @@ class KVPool:
 
     def export_layer(self, layer, stream=None):
         """The layer's stored bytes as device tensors (token padding removed):
-        kq int8 [Hk, ctx, d], vcodes uint8 [Hk, ctx, d*bits/8], vnorm float32
+        kq int8 [Hk, ctx, d], vcodes uint8 [Hk, ceil(ctx/32), d, 4*bits] (per
+        32-token group, one packed code sequence per coordinate), vnorm float32
         [Hk, ctx], kscale float32 [1]."""
         import torch
 
@@ -216,7 +217,7 @@ class KVPool:
         dev = torch.device("cuda", torch.cuda.current_device())
         Hk, T, d = self.kv_heads, self.ctx, self.head_dim
         kq = torch.empty((Hk, T, d), dtype=torch.int8, device=dev)
-        vc = torch.empty((Hk, T, d * bits // 8), dtype=torch.uint8, device=dev)
+        vc = torch.empty((Hk, (T + 31) // 32, d, 4 * bits), dtype=torch.uint8, device=dev)
         vn = torch.empty((Hk, T), dtype=torch.float32, device=dev)
         ks = torch.empty(1, dtype=torch.float32, device=dev)
         _check(_lib().kvpool_export_layer(self._h, layer, kq.data_ptr(), vc.data_ptr(),

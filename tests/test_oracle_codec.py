@@ -234,6 +234,54 @@ def test_packing_round_trip_random(bits):
     assert np.array_equal(codec.unpack_codes(p, bits, 64), c)
 
 
+def _golden_pool_layout(golden_dir):
+    cases, cur = [], None
+    with open(os.path.join(golden_dir, "pool_v_layout.txt")) as f:
+        for line in f:
+            t = line.split()
+            if not t or t[0].startswith("#"):
+                continue
+            if t[0] == "case":
+                cur = dict(bits=int(t[1]), H=int(t[2]), ctx=int(t[3]), d=int(t[4]), codes=[], bytes=[])
+            elif t[0] == "code":
+                cur["codes"].append(tuple(int(x) for x in t[1:]))
+            elif t[0] == "byte":
+                cur["bytes"].append(tuple(int(x, 0) for x in t[1:]))
+            elif t[0] == "end":
+                cases.append(cur)
+    return cases
+
+
+def test_pool_v_layout_golden(golden_dir):
+    cases = _golden_pool_layout(golden_dir)
+    assert len(cases) == 4
+    for c in cases:
+        bits, H, T, d = c["bits"], c["H"], c["ctx"], c["d"]
+        codes = np.zeros((H, T, d), np.uint8)
+        for h, t, i, v in c["codes"]:
+            codes[h, t, i] = v
+        want = np.zeros((H, -(-T // 32), d, 4 * bits), np.uint8)
+        for h, g, i, b, v in c["bytes"]:
+            want[h, g, i, b] = v
+        got = codec.pack_pool_v(codes, bits)
+        assert got.shape == want.shape
+        assert np.array_equal(got, want), np.argwhere(got != want)
+        assert np.array_equal(codec.unpack_pool_v(got, bits, T), codes)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_pool_v_layout_round_trip_ragged(bits):
+    rng = np.random.default_rng(40 + bits)
+    for T in (1, 31, 32, 33, 100, 128):
+        c = rng.integers(0, 1 << bits, size=(2, T, 64), dtype=np.uint8)
+        p = codec.pack_pool_v(c, bits)
+        assert p.shape == (2, -(-T // 32), 64, 4 * bits)
+        assert np.array_equal(codec.unpack_pool_v(p, bits, T), c)
+        # the padded token slots of the last group decode to code 0
+        full = codec.unpack_pool_v(p, bits, p.shape[1] * 32)
+        assert not full[:, T:].any()
+
+
 def test_v_codes_match_exact_float32_model():
     rng = np.random.default_rng(9)
     for bits in (2, 3, 4):
