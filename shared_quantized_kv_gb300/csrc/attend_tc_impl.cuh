@@ -10,37 +10,39 @@
 // shares the KV head is served by one pass over the packed pool bytes, so the
 // pool is read once per step no matter how many agents there are.
 //
-// Per CTA: 256 threads, 8 warps; warp w owns TMEM lane quarter w % 4 and
-// column half w / 4. Both MMAs take their A operand from tensor memory, so the
-// expanded K and V never touch shared memory:
+// Per CTA: 1024 threads, one CTA per SM. Warp w owns TMEM lane quarter w % 4
+// and column group w / 4 (eight groups), so that every per-tile phase is
+// spread over 32 warps and short. Both MMAs take their A operand from tensor
+// memory; the expanded K and V never touch shared memory:
 //   * thread 0 keeps a ring of shared-memory stages filled: a TMA tile of 128
 //     tokens of int8 K (128-byte swizzle, so that one thread per token reads
 //     its row without bank conflicts), the tile's packed V code groups and its
 //     norms (plain bulk copies), one mbarrier per stage. When no kernel before
 //     it in the stream can still be writing the layer, the first tiles are
 //     requested before the grid-dependency wait, overlapping the previous
-//     kernel's tail.
-//   * K^: thread = token, int8 -> fp16 (exact, byte permutes) straight into
-//     TMEM as the A operand of S^T = K^ Q^T (tokens on M = 128, query rows on
-//     N); Q is fp16 in shared memory, each row scaled by its own power of two.
-//   * V^T: thread = rotated coordinate, its 64 codes of the tile (one packed
-//     sequence per coordinate and 32-token group in the pool layout) -> fp16
+//     kernel's tail; the TMEM allocation overlaps the Q load.
+//   * K^: thread = (token, 16 channels), int8 -> fp16 (exact, byte permutes)
+//     straight into TMEM as the A operand of S^T = K^ Q^T (tokens on M = 128,
+//     query rows on N); Q is fp16 in shared memory, each row scaled by its own
+//     power of two.
+//   * V^T: thread = (rotated coordinate, 16 tokens): codes of the pool layout
+//     (one packed sequence per coordinate and 32-token group) -> fp16
 //     lam * c[code] by byte-permute table lookups, into TMEM as the A operand
 //     of O^T += V^T P'^T. The accumulator stays in the rotated domain,
 //     sum_t p_t n_t c[code_t]; the inverse FWHT runs once per output row.
-//   * softmax with thread = token: logits in log2 units against a running
-//     per-row maximum that is raised (with a rescale of O^T in TMEM) only when
-//     a logit exceeds it by more than 2^8; P' = p * n_t / 2^k split into fp16
-//     hi (top 11 significant bits) and fp16 lo (the exact remainder), written
-//     as two MN-major operands, so P' carries ~22 bits into the MMA.
-//   * software pipeline per tile: MMA1(i) runs while V(i) is expanded, MMA2(i)
-//     while K(i+1) is expanded.
-//   epilogue: each CTA pushes its partial rows (m, l, O^T) into the shared
-//     memory of the CTA that owns the row's agent (distributed shared memory
-//     stores, no remote loads), one cluster barrier, then every owner merges
-//     its rows (log-sum-exp), applies one inverse FWHT per row (warp
-//     shuffles), joins the agent's tail (computed in the prologue while the
-//     first tiles are in flight) and writes the row.
+//     K^ and V^T are double-buffered: tile i+1 is expanded while the MMAs of
+//     tile i run.
+//   * softmax with thread = (token, W/8 query rows): logits in log2 units
+//     against a running per-row maximum that is raised (with a rescale of O^T
+//     in TMEM) only when a logit exceeds it by more than 2^8; P' = p * n_t /
+//     2^k split into fp16 hi (top 11 significant bits) and fp16 lo (the exact
+//     remainder), two MN-major operands, so P' carries ~22 bits into the MMA.
+//   epilogue: each CTA stages its partial rows (O^T column, m, l) in shared
+//     memory and sends each row with one bulk copy into the shared memory of
+//     the CTA that owns the row's agent, completing on the owner's mbarrier;
+//     each owner merges its rows (log-sum-exp), applies one inverse FWHT per
+//     row (warp shuffles), joins the agent's tail (computed in the prologue
+//     while the first tiles are in flight) and writes the row.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // KVPOOL_ERR_TIMEOUT in the status word and carries on to its exit without
 // waiting again, so a fault never hangs the device.
@@ -59,9 +61,11 @@ namespace kvp {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 256;   // 8 warps: (TMEM lane quarter) x (column half)
+constexpr int kThreads = 1024;  // 32 warps: (TMEM lane quarter) x (column group)
+constexpr int kGroups = 8;      // column groups
 constexpr float kTau = 8.0f;    // P <= 2^kTau between rescales
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
+constexpr uint32_t kCols = 512;  // TMEM: S^T, O^T, then K^ and V^T twice
 
 struct TcParams {
     const uint8_t* vcodes;
@@ -80,7 +84,7 @@ struct TcParams {
     int tps;     // tokens per CTA, a multiple of kTile
     int nstage;  // shared-memory stages of raw tiles
     int early;   // 1: the layer's bytes may be read before the grid-dependency wait
-    int own;     // most query rows one CTA owns in the merge
+    int own;     // merge slots per source CTA (the most rows one CTA owns)
     int* status;
     uint32_t tlo[4], thi[4];  // low / high bytes of fp16 lam * c[k], entry k in byte k % 4 of word k / 4
     float inv_lam;
@@ -93,7 +97,9 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
-// W = query rows per CTA (MMA N).
+// W = query rows per CTA (MMA N). After the main loop everything below misc
+// (raw stages, Q, P') is reused: this CTA's staging rows at 0, the merge
+// slots that other CTAs fill right after them (epilogue_bytes).
 __host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage) {
     Layout L;
     L.rv = kTile * D;
@@ -105,13 +111,16 @@ __host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage
     L.p = o;
     L.plo = W <= 64 ? 16384 : 32768;  // P' hi, then P' lo
     o += 2 * L.plo;
-    L.misc = o;  // everything below misc is free after the main loop (merge slots)
-    o += (14 * W + 16) * 4;
+    L.misc = o;
+    o += 15 * W * 4;
     L.bars = align_up(o, 8);
-    o = L.bars + 8 * (nstage + 2) + 8;
+    o = L.bars + 8 * (nstage + 3) + 8;
     L.total = align_up(o, 1024);
     return L;
 }
+
+// bytes of the staging rows (W rows of D + 4 floats); the merge slots start there
+__host__ __device__ inline uint32_t staging_bytes(int D, int W) { return align_up(W * (D + 4) * 4, 1024); }
 
 __device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
 
@@ -228,66 +237,77 @@ __device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
     }
 }
 
+
 template <int N>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
-    if constexpr (N % 16 == 0) {
+__device__ __forceinline__ void tmem_ld_f(uint32_t taddr, float (&v)[N]) {
+    uint32_t r[N];
+    ptx::tmem_ldn<N>(taddr, r);
 #pragma unroll
-        for (int c = 0; c < N; c += 16) {
-            uint32_t r[16];
-            ptx::tmem_ld16(taddr + c, r);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) v[c + e] = __uint_as_float(r[e]);
-        }
+    for (int e = 0; e < N; ++e) v[e] = __uint_as_float(r[e]);
+}
+
+// 16 codes (half h of one packed 32-token sequence at `row`) -> 8 fp16x2
+template <int BITS>
+__device__ __forceinline__ void decode16(const unsigned char* row, int h, const uint32_t (&tlo)[4],
+                                         const uint32_t (&thi)[4], uint32_t (&r)[8]) {
+    uint32_t f0, f1;  // two fields of 8 codes
+    if constexpr (BITS == 2) {
+        const uint32_t w = reinterpret_cast<const uint32_t*>(row)[h];
+        f0 = w; f1 = w >> 16;
+    } else if constexpr (BITS == 3) {
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(row) + h;
+        const uint32_t a = wp[0], b = wp[1];
+        if (h == 0) { f0 = a; f1 = __funnelshift_r(a, b, 24); }
+        else { f0 = __funnelshift_r(a, b, 16); f1 = b >> 8; }
     } else {
-        static_assert(N == 8, "column count");
-        uint32_t r[8];
-        ptx::tmem_ld8(taddr, r);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(r[e]);
+        const uint2 w = reinterpret_cast<const uint2*>(row)[h];
+        f0 = w.x; f1 = w.y;
     }
+    const uint32_t y0 = spread8<BITS>(f0), y1 = spread8<BITS>(f1);
+    lookup4<BITS>(y0, tlo, thi, r[0], r[1]);
+    lookup4<BITS>(y0 >> 16, tlo, thi, r[2], r[3]);
+    lookup4<BITS>(y1, tlo, thi, r[4], r[5]);
+    lookup4<BITS>(y1 >> 16, tlo, thi, r[6], r[7]);
 }
 
 // Attention of the owned agents' rows over their private bf16 tails (plain
-// CUDA cores, online softmax in log2 units). Writes the unnormalised
-// accumulator to `out` and (m, l) per row to `tailml`; `stage` is 12.5 KB of
-// shared memory that is free until the main loop.
+// CUDA cores, online softmax in log2 units, 256 tokens per chunk). Writes the
+// unnormalised accumulator to `out` and (m, l) per row to `tailml`; `stage` is
+// 13 KB of shared memory that is free until the main loop.
 template <int D>
 __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* stage, float* tailml,
                                             int S, int crank, int g, int row0, int nrows) {
+    constexpr int TCH = 256;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    float* tq = reinterpret_cast<float*>(stage);                               // [8][D]
-    float* tl = reinterpret_cast<float*>(stage + 8 * D * 4);                  // [8][256]
-    float* tred = reinterpret_cast<float*>(stage + 8 * D * 4 + 8 * 256 * 4);  // [8 warps][8]
-    constexpr int TCH = 256;            // tokens per chunk (one per thread)
-    constexpr int RPT = kThreads / D;   // row sub-blocks in the P.V phase
-    static_assert(TCH == kThreads, "one tail token per thread");
-    const int c = tid % D, sub = tid / D;
+    float* tq = reinterpret_cast<float*>(stage);                                // [8][D]
+    float* tl = reinterpret_cast<float*>(stage + 8 * D * 4);                   // [8][TCH]
+    float* tmx = reinterpret_cast<float*>(stage + 8 * D * 4 + 8 * TCH * 4);    // [8]
+    const int c = tid % D, sub = tid / D;  // P.V phase: row sub, channel c
+    const int t = tid % TCH, k0 = tid / TCH;  // logit phase: token t, rows k0 and k0 + 4
     const int G = p.G;
     for (int ar = crank; ar * G < nrows; ar += S) {
         const int a = row0 / G + ar;
+        const int tmax = min(max(p.tlen[a], 0), p.tail_max);
+        const long long tbase = ((long long)a * p.Hk + g) * p.tail_max;
         for (int jb = 0; jb < G; jb += 8) {
-            // rows k = 0..7 of the batch are (agent a, head jb + k)
             const int cnt = min(8, G - jb);
-            const int ownmask = (1 << cnt) - 1;
-            const int rr0 = ar * G + jb;
-            const int tmax = min(max(p.tlen[a], 0), p.tail_max);
             for (int i = tid; i < 8 * D; i += kThreads) {
                 const int k = i / D, cc = i % D;
-                float v = 0.f;
-                if ((ownmask >> k) & 1) v = bf2f(p.Q[((long long)a * p.Hq + g * G + jb + k) * D + cc]);
-                tq[k * D + cc] = v;
+                tq[k * D + cc] = k < cnt ? bf2f(p.Q[((long long)a * p.Hq + g * G + jb + k) * D + cc]) : 0.f;
             }
-            float m_run[8], l_run[8], acc[8];
+            float m_run[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; acc[k] = 0.f; }
+            for (int k = 0; k < 8; ++k) m_run[k] = -CUDART_INF_F;
+            float acc = 0.f, l_run = 0.f;
             __syncthreads();
             for (int c0 = 0; c0 < tmax; c0 += TCH) {
-                const int t = c0 + tid;
+                float lg[2];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    float lg = -CUDART_INF_F;
-                    if (((ownmask >> k) & 1) && t < tmax) {
-                        const uint16_t* kr = p.tK + (((long long)a * p.Hk + g) * p.tail_max + t) * D;
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int k = k0 + 4 * kk;
+                    lg[kk] = -CUDART_INF_F;
+                    if (k < cnt && c0 + t < tmax) {
+                        const uint16_t* kr = p.tK + (tbase + c0 + t) * D;
                         const float* qq = tq + k * D;
                         float dot = 0.f;
                         for (int cc = 0; cc < D; cc += 8) {
@@ -301,52 +321,59 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
                             dot = fmaf(qq[cc + 6], bf2f(u.w & 0xFFFF), dot);
                             dot = fmaf(qq[cc + 7], bf2f(u.w >> 16), dot);
                         }
-                        lg = dot * p.scale_log2;
+                        lg[kk] = dot * p.scale_log2;
                     }
-                    tl[k * TCH + tid] = lg;
-                    const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(lg)));
-                    if (lane == 0) tred[warp * 8 + k] = mx;
+                    tl[k * TCH + t] = lg[kk];
                 }
                 __syncthreads();
-                float mnew[8], alpha[8];
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
+                if (warp < 8) {  // row maximum of the chunk
                     float mx = -CUDART_INF_F;
 #pragma unroll
-                    for (int w = 0; w < kThreads / 32; ++w) mx = fmaxf(mx, tred[w * 8 + k]);
-                    mnew[k] = fmaxf(m_run[k], mx);
-                    alpha[k] = (mnew[k] == -CUDART_INF_F) ? 1.f : ptx::ex2(m_run[k] - mnew[k]);
-                    const float lg = tl[k * TCH + tid];
-                    tl[k * TCH + tid] = (lg == -CUDART_INF_F) ? 0.f : ptx::ex2(lg - mnew[k]);
+                    for (int i = 0; i < TCH / 32; ++i) mx = fmaxf(mx, tl[warp * TCH + lane + 32 * i]);
+#pragma unroll
+                    for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    if (lane == 0) tmx[warp] = mx;
                 }
                 __syncthreads();
-                const int cnt2 = min(TCH, tmax - c0);
+                float alpha[8];
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
-                    l_run[k] *= alpha[k];
-                    acc[k] *= alpha[k];
-                    m_run[k] = mnew[k];
-                    if ((k % RPT) != sub || !((ownmask >> k) & 1)) continue;
-                    const uint16_t* vr0 = p.tV + (((long long)a * p.Hk + g) * p.tail_max + c0) * D + c;
+                    const float mn = fmaxf(m_run[k], tmx[k]);
+                    alpha[k] = (mn == -CUDART_INF_F) ? 1.f : ptx::ex2(m_run[k] - mn);
+                    m_run[k] = mn;
+                }
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int k = k0 + 4 * kk;
+                    tl[k * TCH + t] = (lg[kk] == -CUDART_INF_F) ? 0.f : ptx::ex2(lg[kk] - m_run[k]);
+                }
+                __syncthreads();
+                if (sub < cnt) {
+                    float al = 1.f;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) if (k == sub) al = alpha[k];
+                    const uint16_t* vr0 = p.tV + (tbase + c0) * D + c;
+                    const int n2 = min(TCH, tmax - c0);
                     float sacc = 0.f, ls = 0.f;
-                    for (int t2 = 0; t2 < cnt2; ++t2) {
-                        const float pv = tl[k * TCH + t2];
+                    for (int t2 = 0; t2 < n2; ++t2) {
+                        const float pv = tl[sub * TCH + t2];
                         sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
                         ls += pv;
                     }
-                    acc[k] += sacc;
-                    l_run[k] += ls;
+                    acc = acc * al + sacc;
+                    l_run = l_run * al + ls;
                 }
                 __syncthreads();
             }
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if ((k % RPT) != sub || !((ownmask >> k) & 1)) continue;
-                const int rr = rr0 + k, j = jb + k;
-                p.out[((long long)a * p.Hq + g * G + j) * D + c] = acc[k];
+            if (sub < cnt) {
+                const int rr = ar * G + jb + sub;
+                p.out[((long long)a * p.Hq + g * G + jb + sub) * D + c] = acc;
                 if (c == 0) {
-                    tailml[2 * rr] = m_run[k];
-                    tailml[2 * rr + 1] = l_run[k];
+                    float mr = -CUDART_INF_F;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) if (k == sub) mr = m_run[k];
+                    tailml[2 * rr] = mr;
+                    tailml[2 * rr + 1] = l_run;
                 }
             }
             __syncthreads();
@@ -355,44 +382,45 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
 }
 
 template <int D, int W, int BITS>
-__global__ void __launch_bounds__(kThreads, (W <= 64 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
-    constexpr int HW = W / 2;            // query rows (TMEM columns) per thread
-    constexpr int EPL = D / 32;          // channels per lane in the merge
-    constexpr int VB = D * BITS / 8;     // code bytes per token
-    constexpr int GB = D * 4 * BITS;     // bytes per 32-token code group
-    constexpr uint32_t kCols = W <= 64 ? 256 : 512;
-    constexpr uint32_t kColO = W <= 64 ? 64 : 128;  // O^T; S^T at column 0
-    constexpr uint32_t kColK = 2 * kColO;           // K^ (D/2 columns)
-    constexpr uint32_t kColV = kColK + 64;          // V^T (64 columns: 128 tokens of fp16 pairs)
-    constexpr int KC = D / 32;           // 16-byte K chunks per thread (half a row)
+    constexpr int CPT = W / kGroups;       // query rows (TMEM columns) per thread: 2, 4, 8 or 16
+    constexpr int CH = CPT < 8 ? CPT : 8;  // columns per softmax chunk
+    constexpr int EPL = D / 32;            // channels per lane in the merge
+    constexpr int VB = D * BITS / 8;       // code bytes per token
+    constexpr int GB = D * 4 * BITS;       // bytes per 32-token code group
+    constexpr int KCH = D / 16;            // 16-byte K chunks per token row
+    constexpr int ROWF = D + 4;            // floats per merge row: O^T column, m, l, padding
+    constexpr uint32_t kColO = 128, kColK = 256, kColV = 320;  // + 128 for the second buffer
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int S = (int)ptx::cluster_size();
+    const int crank = (int)ptx::cluster_rank();
     const Layout lay = make_layout(D, BITS, W, p.nstage);
     unsigned char* sQ = sm + lay.q;
     unsigned char* sP = sm + lay.p;
-    float* sM = reinterpret_cast<float*>(sm + lay.misc);  // [W] running row maxima (log2 units)
-    float* sCf = sM + W;                                    // [W] logit factor per row
-    float* sL = sCf + W;                                    // [W] row sums
-    float* lsum = sL + W;                                   // [4][W]
-    float* colmax = lsum + 4 * W;                           // [4][W]
-    float* tailml = colmax + 4 * W;                         // [W][2]
+    float* sO = reinterpret_cast<float*>(sm);                                // epilogue: [W][ROWF]
+    float* slots = reinterpret_cast<float*>(sm + staging_bytes(D, W));       // epilogue: [S][own][ROWF]
+    float* sMx = reinterpret_cast<float*>(sm + lay.misc);     // [2][W] running row maxima (log2 units)
+    float* sCf = sMx + 2 * W;                                 // [W] logit factor per row
+    float* lsum = sCf + W;                                    // [4][W] row-sum partials
+    float* colmax = lsum + 4 * W;                             // [4][W]
+    float* tailml = colmax + 4 * W;                           // [W][2]
     uint32_t* sOwn = reinterpret_cast<uint32_t*>(tailml + 2 * W);  // [W] owner << 16 | slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + p.nstage + 2);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + p.nstage + 3);
     const uint32_t bar_full = ptx::smem_u32(bars);
     const uint32_t bar_s = bar_full + 8 * p.nstage;  // S^T of the tile is in TMEM
     const uint32_t bar_o = bar_s + 8;                // the tile's P.V MMAs are done
+    const uint32_t bar_m = bar_o + 8;                // every merge row sent to this CTA has landed
 
-    const int S = (int)ptx::cluster_size();
-    const int crank = (int)ptx::cluster_rank();
     const int g = blockIdx.y;
     const int row0 = blockIdx.z * W;
-    const int nrows = min(W, p.R - row0);
+    const int nrows = min(W, p.R - row0);  // a multiple of G
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int q = warp & 3, cg = warp >> 2;
+    const int q = warp & 3, cgp = warp >> 2;
     const int tok = q * 32 + lane;      // token of this thread in S^T / K^; channel in O^T / V^T
     const bool has_ch = q * 32 < D;     // warp-uniform: lanes of this quarter hold channels
     const int t_begin = crank * p.tps;
@@ -400,6 +428,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     const int ntile = (t_end - t_begin + kTile - 1) / kTile;  // >= 1
     const long long head_tok = (long long)g * p.ctx_pad;
     const uint32_t stage_bytes = kTile * D + kTile * VB + kTile * 4;
+    // rows owned here: the G rows of every agent ar (relative) with ar % S == crank
+    const int nag = nrows / p.G;
+    const int own_cnt = crank < nag ? ((nag - crank + S - 1) / S) * p.G : 0;
 
     auto issue_tile = [&](int i) {
         const int s = i % p.nstage;
@@ -423,28 +454,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 
     // ---------------------------------------------------------------- setup
     if (tid == 0) {
-        for (int s = 0; s < p.nstage + 2; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
+        for (int s = 0; s < p.nstage + 3; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
         ptx::mbar_init_fence();
+        if (own_cnt > 0) ptx::mbar_expect_tx(bar_m, (uint32_t)(S * own_cnt * ROWF * 4));
         if (p.early) issue_first();
     }
     if (warp == 0) ptx::tmem_alloc(ptx::smem_u32(tslot), kCols);
     if (tid < W) {
-        sM[tid] = -CUDART_INF_F;
+        sMx[tid] = -CUDART_INF_F;
         const int ar = tid / p.G;  // agent of row tid, relative to the CTA's first agent
         sOwn[tid] = ((uint32_t)(ar % S) << 16) | (uint32_t)((ar / S) * p.G + tid % p.G);
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    const uint32_t tmem = *tslot;
-    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const uint32_t tS = tmem, tO = tmem + kColO, tK = tmem + kColK, tV = tmem + kColV;
-    if (D == 64 && !has_ch) {  // V^T rows 64..127 stay zero (M = 128 with d = 64)
-        uint32_t z[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) z[e] = 0u;
-        ptx::tmem_st32(tV + lane_off + 32 * cg, z);
-        ptx::tmem_wait_st();
     }
 
     ptx::grid_dep_wait();
@@ -452,16 +471,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     if (tid == 0 && !p.early) issue_first();
     bool timed_out = false;
     // P' = p * n_t / nref with nref the power of two >= the largest norm of the layer
-    float vr = 1.0f, nref = 1.0f;
-    {
-        const uint32_t nb = *p.vnmax;
-        const int ex = (int)((nb >> 23) & 0xFF);
-        if (nb != 0 && ex < 255 && ex > 0) {
-            const int k = ex - 127 + ((nb & 0x7FFFFF) != 0 ? 1 : 0);
-            nref = ldexpf(1.0f, k);
-            vr = ldexpf(1.0f, -k);
-        }
-    }
+    const uint32_t nb = *p.vnmax;
     const float kscale = *p.kscale;
 
     // 1. Q rows -> fp16 in a 128-byte-swizzled K-major operand; each row is
@@ -507,180 +517,221 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             }
         }
     }
+    float vr = 1.0f, nref = 1.0f;
+    {
+        const int ex = (int)((nb >> 23) & 0xFF);
+        if (nb != 0 && ex < 255 && ex > 0) {
+            const int k = ex - 127 + ((nb & 0x7FFFFF) != 0 ? 1 : 0);
+            nref = ldexpf(1.0f, k);
+            vr = ldexpf(1.0f, -k);
+        }
+    }
 
     // 2. tails of the agents this CTA owns (CUDA cores), overlapping the first
     //    copies; the P' area is free until the first softmax
     if (p.tK != nullptr) tail_attention<D>(p, sP, tailml, S, crank, g, row0, nrows);
     ptx::fence_proxy_async();
+    ptx::tc_fence_before();
     __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    const uint32_t tS = tmem, tO = tmem + kColO, tK = tmem + kColK, tV = tmem + kColV;
 
     // 3. main loop
     uint32_t tlo[4], thi[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
-    float lp[HW];  // per-thread row-sum partials
+    float lp[CPT];  // per-thread row-sum partials
 #pragma unroll
-    for (int j = 0; j < HW; ++j) lp[j] = 0.f;
+    for (int j = 0; j < CPT; ++j) lp[j] = 0.f;
     const uint32_t idesc1 = ptx::idesc_f16(128, W, 0, 0);
     const uint32_t idesc2 = ptx::idesc_f16(128, W, 0, 1);
     const uint32_t aQ = ptx::smem_u32(sQ), aP = ptx::smem_u32(sP);
+    const bool designated = q == 0 && lane == 0;  // writes the next running maxima of its columns
 
     auto wait_full = [&](int i) {
         if (!timed_out && !ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs))
             timed_out = true;
     };
-    // K^ of tile i: token row -> fp16 pairs in TMEM columns [cg*D/4, cg*D/4 + D/4)
-    auto convert_k = [&](int i) {
-        const unsigned char* rk = sm + (i % p.nstage) * lay.stage;
-        uint32_t r[D / 4];
-#pragma unroll
-        for (int k = 0; k < KC; ++k) {
-            const int c = cg * KC + k;
+    // K^ and V^T of tile i into TMEM buffer b
+    auto convert = [&](int i, int b) {
+        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
+        if (cgp < KCH) {  // token tok, channels 16*cgp .. 16*cgp+15
             const int sw = D == 128 ? (tok & 7) : ((tok >> 1) & 3);  // TMA 128 B / 64 B swizzle
-            const uint4 u = *reinterpret_cast<const uint4*>(rk + tok * D + ((c ^ sw) << 4));
-            i8x4_to_h2x2(u.x, r[8 * k + 0], r[8 * k + 1]);
-            i8x4_to_h2x2(u.y, r[8 * k + 2], r[8 * k + 3]);
-            i8x4_to_h2x2(u.z, r[8 * k + 4], r[8 * k + 5]);
-            i8x4_to_h2x2(u.w, r[8 * k + 6], r[8 * k + 7]);
+            const uint4 u = *reinterpret_cast<const uint4*>(st + tok * D + ((cgp ^ sw) << 4));
+            uint32_t r[8];
+            i8x4_to_h2x2(u.x, r[0], r[1]);
+            i8x4_to_h2x2(u.y, r[2], r[3]);
+            i8x4_to_h2x2(u.z, r[4], r[5]);
+            i8x4_to_h2x2(u.w, r[6], r[7]);
+            ptx::tmem_stn<8>(tK + 128 * b + lane_off + cgp * 8, r);
         }
-        if constexpr (D == 128) ptx::tmem_st32(tK + lane_off + cg * 32, r);
-        else ptx::tmem_st16(tK + lane_off + cg * 16, r);
+        if (has_ch) {  // channel tok, tokens 16*cgp .. 16*cgp+15
+            uint32_t r[8];
+            decode16<BITS>(st + lay.rv + (cgp >> 1) * GB + tok * (4 * BITS), cgp & 1, tlo, thi, r);
+            ptx::tmem_stn<8>(tV + 128 * b + lane_off + cgp * 8, r);
+        }
         ptx::tmem_wait_st();
     };
-
-    wait_full(0);
-    convert_k(0);
-    ptx::tc_fence_before();
-    __syncthreads();  // K^(0) ready
-    for (int i = 0; i < ntile; ++i) {
-        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
-        if (tid == 0) {  // S^T = K^ Q^T
-            ptx::tc_fence_after();
+    auto mma1 = [&](int b) {  // S^T = K^ Q^T
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                const uint64_t bd = ptx::sdesc(aQ + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
-                ptx::mma_f16_ta(tS, tK + ks * 8, bd, idesc1, ks > 0 ? 1u : 0u);
-            }
-            ptx::mma_commit(bar_s);
+        for (int ks = 0; ks < D / 16; ++ks) {
+            const uint64_t bd = ptx::sdesc(aQ + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
+            ptx::mma_f16_ta(tS, tK + 128 * b + ks * 8, bd, idesc1, ks > 0 ? 1u : 0u);
         }
-        // V^T of tile i while MMA1 runs (V^ and P' are free once MMA2(i-1) is done)
+        ptx::mma_commit(bar_s);
+    };
+
+    if (D == 64 && !has_ch) {  // V^T rows 64..127 stay zero in both buffers (M = 128 with d = 64)
+        const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        ptx::tmem_stn<8>(tV + lane_off + cgp * 8, z);
+        ptx::tmem_stn<8>(tV + 128 + lane_off + cgp * 8, z);
+    }
+    wait_full(0);
+    convert(0, 0);
+    ptx::tc_fence_before();
+    __syncthreads();  // K^(0), V^T(0) ready
+    if (tid == 0) {
+        ptx::tc_fence_after();
+        mma1(0);
+    }
+    for (int i = 0; i < ntile; ++i) {
+        const int b = i & 1;
+        // MMA2(i-1) done: buffer b^1 (K^, V^T of tile i-1) and P' are free
         if (i > 0 && !timed_out && !ptx::mbar_wait(bar_o, (i - 1) & 1, kWaitNs)) timed_out = true;
         ptx::tc_fence_after();
-        const bool valid = (t_begin + i * kTile + tok) < t_end;
-        const float ns = valid ? reinterpret_cast<const float*>(st + lay.rn)[tok] * vr : 0.f;
-        if (has_ch) {
-            uint32_t h[32];
-            const unsigned char* rv = st + lay.rv + tok * (4 * BITS);
-            decode32<BITS>(rv + (2 * cg) * GB, tlo, thi, h);
-            decode32<BITS>(rv + (2 * cg + 1) * GB, tlo, thi, h + 16);
-            ptx::tmem_st32(tV + lane_off + 32 * cg, h);
+        if (i + 1 < ntile) {
+            wait_full(i + 1);
+            convert(i + 1, b ^ 1);
         }
 
         // softmax of tile i
         if (!timed_out && !ptx::mbar_wait(bar_s, i & 1, kWaitNs)) timed_out = true;
         ptx::tc_fence_after();
-        // logits l = y * cf (log2 units) of this thread's token for its HW rows
-        float l[HW];
-        tmem_ld_cols<HW>(tS + lane_off + cg * HW, l);
-        ptx::tmem_wait_ld();
+        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
+        const bool valid = (t_begin + i * kTile + tok) < t_end;
+        const float ns = valid ? reinterpret_cast<const float*>(st + lay.rn)[tok] * vr : 0.f;
+        const float* mcur = sMx + (i & 1) * W;         // running maxima before this tile
+        float* mnext = sMx + ((i + 1) & 1) * W;        // after it
+        const int colb = cgp * CPT;
         float over = -CUDART_INF_F;
 #pragma unroll
-        for (int j = 0; j < HW; j += 4) {
-            const float4 c4 = *reinterpret_cast<const float4*>(sCf + cg * HW + j);
-            const float4 m4 = *reinterpret_cast<const float4*>(sM + cg * HW + j);
-            l[j] = valid ? l[j] * c4.x : -CUDART_INF_F;
-            l[j + 1] = valid ? l[j + 1] * c4.y : -CUDART_INF_F;
-            l[j + 2] = valid ? l[j + 2] * c4.z : -CUDART_INF_F;
-            l[j + 3] = valid ? l[j + 3] * c4.w : -CUDART_INF_F;
-            over = fmaxf(over, fmaxf(fmaxf(l[j] - m4.x, l[j + 1] - m4.y), fmaxf(l[j + 2] - m4.z, l[j + 3] - m4.w)));
+        for (int c0 = 0; c0 < CPT; c0 += CH) {
+            float y[CH];
+            tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < CH; ++e) {
+                const float lg = valid ? y[e] * sCf[colb + c0 + e] : -CUDART_INF_F;
+                over = fmaxf(over, lg - mcur[colb + c0 + e]);
+            }
         }
-        // the running maxima sM change only after the tile's last read of them
-        // (below, after the barrier); until then the new maxima are
-        // max(sM, colmax over the four lane quarters)
         const bool slow = ptx::bar_or(2, kThreads, over > kTau);
         auto new_max = [&](int col) {
-            return fmaxf(sM[col], fmaxf(fmaxf(colmax[col], colmax[W + col]),
-                                        fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
+            return fmaxf(mcur[col], fmaxf(fmaxf(colmax[col], colmax[W + col]),
+                                          fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
         };
         if (slow) {
             // exact maxima of this tile's rows, then rescale what was accumulated
 #pragma unroll
-            for (int j = 0; j < HW; ++j) {
-                const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(l[j])));
-                if (lane == (j & 31)) colmax[q * W + cg * HW + j] = mx;
+            for (int c0 = 0; c0 < CPT; c0 += CH) {
+                float y[CH];
+                tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < CH; ++e) {
+                    const float lg = valid ? y[e] * sCf[colb + c0 + e] : -CUDART_INF_F;
+                    const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(lg)));
+                    if (lane == ((c0 + e) & 31)) colmax[q * W + colb + c0 + e] = mx;
+                }
             }
             ptx::bar_sync(1, kThreads);
 #pragma unroll
-            for (int c0 = 0; c0 < HW; c0 += 8) {
-                float alpha[8];
+            for (int c0 = 0; c0 < CPT; c0 += CH) {
+                float alpha[CH];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int col = cg * HW + c0 + e;
-                    const float mo = sM[col];
-                    alpha[e] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2(mo - new_max(col));
+                for (int e = 0; e < CH; ++e) {
+                    const int col = colb + c0 + e;
+                    const float mo = mcur[col], mn = new_max(col);
+                    alpha[e] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2(mo - mn);
                     lp[c0 + e] *= alpha[e];
+                    if (designated) mnext[col] = mn;
                 }
                 if (i > 0 && has_ch) {  // O^T columns (MMA2(i-1) is done)
-                    uint32_t r8[8];
-                    ptx::tmem_ld8(tO + lane_off + cg * HW + c0, r8);
+                    uint32_t r[CH];
+                    ptx::tmem_ldn<CH>(tO + lane_off + colb + c0, r);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) r8[e] = __float_as_uint(__uint_as_float(r8[e]) * alpha[e]);
-                    ptx::tmem_st8(tO + lane_off + cg * HW + c0, r8);
+                    for (int e = 0; e < CH; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha[e]);
+                    ptx::tmem_stn<CH>(tO + lane_off + colb + c0, r);
                 }
             }
+        } else if (designated) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) mnext[colb + j] = mcur[colb + j];
         }
         // P'^T = p * n_t / nref as fp16 hi + lo, MN-major (one 128-byte swizzled
         // row of 64 query rows per token), and the row-sum partials of p
 #pragma unroll
-        for (int c0 = 0; c0 < HW; c0 += 8) {
-            float hi[8], lo[8];
+        for (int c0 = 0; c0 < CPT; c0 += CH) {
+            float y[CH];
+            tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
+            ptx::tmem_wait_ld();
+            uint32_t hw[CH / 2], lw[CH / 2];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int col = cg * HW + c0 + e;
-                const float mc = slow ? new_max(col) : sM[col];
-                const float pv = ptx::ex2(l[c0 + e] - mc);  // 0 for invalid tokens
-                lp[c0 + e] += pv;
-                const float pp = pv * ns;
-                hi[e] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
-                lo[e] = pp - hi[e];                                          // exact
+            for (int e = 0; e < CH; e += 2) {
+                float hi[2], lo[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int col = colb + c0 + e + u;
+                    const float mc = slow ? new_max(col) : mcur[col];
+                    const float lg = valid ? y[e + u] * sCf[col] : -CUDART_INF_F;
+                    const float pv = ptx::ex2(lg - mc);  // 0 for invalid tokens
+                    lp[c0 + e + u] += pv;
+                    const float pp = pv * ns;
+                    hi[u] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
+                    lo[u] = pp - hi[u];                                          // exact
+                }
+                hw[e / 2] = pack_h2(hi[0], hi[1]);
+                lw[e / 2] = pack_h2(lo[0], lo[1]);
             }
-            const int col0 = cg * HW + c0;
+            const int col0 = colb + c0;
             const int off = (col0 >> 6) * 16384 + (tok >> 3) * 1024 + (tok & 7) * 128 +
-                            ((((col0 & 63) >> 3) ^ (tok & 7)) << 4);
-            *reinterpret_cast<uint4*>(sP + off) =
-                make_uint4(pack_h2(hi[0], hi[1]), pack_h2(hi[2], hi[3]), pack_h2(hi[4], hi[5]), pack_h2(hi[6], hi[7]));
-            *reinterpret_cast<uint4*>(sP + lay.plo + off) =
-                make_uint4(pack_h2(lo[0], lo[1]), pack_h2(lo[2], lo[3]), pack_h2(lo[4], lo[5]), pack_h2(lo[6], lo[7]));
+                            ((((col0 & 63) >> 3) ^ (tok & 7)) << 4) + (col0 & 7) * 2;
+            if constexpr (CH == 8) {
+                *reinterpret_cast<uint4*>(sP + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4*>(sP + lay.plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            } else if constexpr (CH == 4) {
+                *reinterpret_cast<uint2*>(sP + off) = make_uint2(hw[0], hw[1]);
+                *reinterpret_cast<uint2*>(sP + lay.plo + off) = make_uint2(lw[0], lw[1]);
+            } else {
+                *reinterpret_cast<uint32_t*>(sP + off) = hw[0];
+                *reinterpret_cast<uint32_t*>(sP + lay.plo + off) = lw[0];
+            }
         }
-        ptx::tmem_wait_st();  // V^T (and any O^T rescale) stores
+        ptx::tmem_wait_st();  // K^/V^T(i+1) and any O^T rescale
         ptx::fence_proxy_async();
         ptx::tc_fence_before();
-        __syncthreads();  // P'(i) and V^T(i) ready; raw stage of tile i consumed
-        if (slow && q == 0 && lane == 0) {  // every read of sM for this tile is done
-#pragma unroll 4
-            for (int j = 0; j < HW; ++j) sM[cg * HW + j] = new_max(cg * HW + j);
-        }
-        if (tid == 0) {  // O^T += V^T (P'_hi + P'_lo)^T, then refill the stage
+        __syncthreads();  // P'(i), K^/V^T(i+1) ready; the raw stage of tile i is consumed
+        if (tid == 0) {
             ptx::tc_fence_after();
+            // O^T += V^T (P'_hi + P'_lo)^T
 #pragma unroll
             for (int ks = 0; ks < kTile / 16; ++ks) {
                 const uint64_t bh = ptx::sdesc(aP + ks * 2048, 16384, 1024);
                 const uint64_t bl = ptx::sdesc(aP + lay.plo + ks * 2048, 16384, 1024);
-                ptx::mma_f16_ta(tO, tV + ks * 8, bh, idesc2, (i > 0 || ks > 0) ? 1u : 0u);
-                ptx::mma_f16_ta(tO, tV + ks * 8, bl, idesc2, 1u);
+                ptx::mma_f16_ta(tO, tV + 128 * b + ks * 8, bh, idesc2, (i > 0 || ks > 0) ? 1u : 0u);
+                ptx::mma_f16_ta(tO, tV + 128 * b + ks * 8, bl, idesc2, 1u);
             }
             ptx::mma_commit(bar_o);
+            if (i + 1 < ntile) mma1(b ^ 1);
             if (i + p.nstage < ntile) issue_tile(i + p.nstage);
         }
-        if (i + 1 < ntile) {  // K^(i+1) while MMA2(i) runs (MMA1(i) has finished with K^)
-            wait_full(i + 1);
-            convert_k(i + 1);
-            ptx::tc_fence_before();
-            __syncthreads();
-        }
     }
-    if (!timed_out && !ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
+    // the last P.V commit covers every MMA issued; waited for even after a
+    // timeout, so that no MMA is still running when TMEM is released
+    if (!ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
     ptx::tc_fence_after();
     if (tid == 0 && timed_out) {
         // give the copies still in flight a bounded chance to land before the
@@ -689,67 +740,68 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs);
     }
 
-    // 4. epilogue: row sums and O^T into registers, TMEM released
-    warp_reduce_scatter<HW>(lp, lane);
-    {
-        constexpr int KEEP = HW >= 32 ? HW / 32 : 1;  // sums kept per lane
-        constexpr int REP = HW >= 32 ? 1 : 32 / HW;    // lanes holding the same sum
+    // this CTA is done with its stages, Q and P': other CTAs may write merge
+    // slots there once every CTA of the cluster has arrived (the wait comes
+    // right before the sends; the barrier inits are older still)
+    ptx::cluster_arrive();
+
+    // 4. epilogue: row sums and O^T columns into the staging rows, TMEM released
+    warp_reduce_scatter<CPT>(lp, lane);
+    if (lane % (32 / CPT) == 0) lsum[q * W + cgp * CPT + lane / (32 / CPT)] = lp[0];
+    float o[CPT];
+    if (has_ch) {
 #pragma unroll
-        for (int k = 0; k < KEEP; ++k) {
-            const int col = cg * HW + lane / REP * KEEP + k;
-            if (lane % REP == 0) lsum[q * W + col] = lp[k];
+        for (int c0 = 0; c0 < CPT; c0 += CH) {
+            float y[CH];
+            tmem_ld_f<CH>(tO + lane_off + cgp * CPT + c0, y);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < CH; ++e) o[c0 + e] = y[e];
         }
     }
-    float o[HW];
-    if (has_ch) {
-        tmem_ld_cols<HW>(tO + lane_off + cg * HW, o);
-        ptx::tmem_wait_ld();
-    }
     ptx::tc_fence_before();
-    __syncthreads();
+    __syncthreads();  // every MMA is done: the stage area becomes staging rows
     if (warp == 0) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kCols);
     }
-    if (tid < nrows) sL[tid] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
-    if (timed_out && lane == 0) atomicOr(p.status, kStTimeout);
-    ptx::cluster_arrive();  // every CTA of the cluster is past its main loop:
-    ptx::cluster_wait();    // the stage / Q / P' areas become merge slots
-
-    // 5. push the partial rows to their owners: slot (source rank, row of the
-    //    owner) holds O^T[:, row] and (m, l)
-    float* slots = reinterpret_cast<float*>(sm);         // [S][own][D]
-    float* slotml = slots + (size_t)S * p.own * D;        // [S][own][2]
     if (has_ch) {
 #pragma unroll
-        for (int j = 0; j < HW; ++j) {
-            const int r = cg * HW + j;
-            if (r < nrows) {
-                const uint32_t ow = sOwn[r];
-                const float* dst = slots + ((size_t)(crank * p.own + (int)(ow & 0xFFFF)) * D + tok);
-                ptx::st_dsmem(ptx::dsmem_addr(dst, ow >> 16), o[j]);
-            }
+        for (int j = 0; j < CPT; ++j) {
+            const int r = cgp * CPT + j;
+            if (r < nrows) sO[r * ROWF + tok] = o[j];
         }
     }
     if (tid < nrows) {
-        const uint32_t ow = sOwn[tid];
-        const float* dst = slotml + (size_t)(crank * p.own + (int)(ow & 0xFFFF)) * 2;
-        ptx::st_dsmem2(ptx::dsmem_addr(dst, ow >> 16), sM[tid], sL[tid]);
+        sO[tid * ROWF + D] = sMx[(ntile & 1) * W + tid];
+        sO[tid * ROWF + D + 1] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
     }
-    ptx::cluster_arrive();
-    ptx::cluster_wait();
+    if (timed_out && lane == 0) atomicOr(p.status, kStTimeout);
+    ptx::fence_proxy_async();
+    __syncthreads();
 
-    // 6. merge the owned rows, one warp per row
-    {
+    // 5. send row r to the owner of its agent: slot (this rank, owner's row index)
+    ptx::cluster_wait();
+    if (tid < nrows) {
+        const uint32_t ow = sOwn[tid], owner = ow >> 16;
+        const float* dst = slots + (size_t)(crank * p.own + (int)(ow & 0xFFFF)) * ROWF;
+        ptx::bulk_s2cluster(ptx::dsmem_addr(dst, owner), ptx::smem_u32(sO + tid * ROWF), ROWF * 4,
+                            ptx::dsmem_addr(bars + p.nstage + 2, owner));
+        ptx::bulk_commit();
+    }
+
+    // 6. merge the owned rows once all S copies of each have landed, one warp per row
+    if (own_cnt > 0) {
+        bool ok = !timed_out && ptx::mbar_wait(bar_m, 0, kWaitNs);
+        if (!ok && tid == 0) atomicOr(p.status, kStTimeout);
         const int G = p.G;
-        for (int loc = warp; loc < p.own; loc += kThreads / 32) {
+        for (int loc = warp; ok && loc < own_cnt; loc += kThreads / 32) {
             const int ar = (loc / G) * S + crank, j = loc % G;
             const int rr = ar * G + j;
-            if (rr >= nrows) break;  // rr grows with loc
             const int a = row0 / G + ar;
             float Ms = -CUDART_INF_F, Ls = 0.f;
             if (lane < S) {
-                const float2 ml = *reinterpret_cast<const float2*>(slotml + (size_t)(lane * p.own + loc) * 2);
+                const float2 ml = *reinterpret_cast<const float2*>(slots + (size_t)(lane * p.own + loc) * ROWF + D);
                 Ms = ml.x;
                 Ls = ml.y;
             }
@@ -765,7 +817,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
             for (int s = 0; s < S; ++s) {
                 const float w = __shfl_sync(0xffffffffu, wl, s);
-                const float* src = slots + (size_t)(s * p.own + loc) * D + lane * EPL;
+                const float* src = slots + (size_t)(s * p.own + loc) * ROWF + lane * EPL;
                 if constexpr (EPL == 4) {
                     const float4 v = *reinterpret_cast<const float4*>(src);
                     acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
@@ -818,6 +870,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             for (int e = 0; e < EPL; ++e) orow[e] = (acc[e] * oscale * wp + tacc[e] * wt) * inv;
         }
     }
+    if (tid < nrows) ptx::bulk_wait_read();  // the staging row may be released
 }
 
 template <int D, int W, int BITS>
@@ -861,27 +914,29 @@ int max_clusters(int S, size_t smem) {
 template <int D, int W, int BITS>
 cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
     configure<D, W, BITS>();
-    // shared memory: as many raw stages as fit (no more than a CTA has tiles),
-    // and a floor that keeps the CTAs per SM within what TMEM holds (2 x 256
-    // columns, or 1 x 512): a CTA waiting in tcgen05.alloc for a cluster peer
-    // on its own SM would never run
-    const uint32_t cap = (W <= 64 ? 112u : 227u) * 1024;
-    const size_t floor_bytes = W <= 64 ? 80 * 1024 : 116 * 1024;
-    int max_stage = W <= 64 ? 2 : 4;
-    while (max_stage > 1 && make_layout(D, BITS, W, max_stage).total + 1024 > cap) --max_stage;
-    // cluster size: fewest (waves x tiles per CTA), then the larger cluster;
-    // the merge slots must fit below the misc area of the layout the CTA uses
+    constexpr uint32_t kMaxSmem = 227 * 1024;
+    // one CTA per SM (it uses all 512 TMEM columns): the floor on shared
+    // memory keeps a second CTA off the SM, where it would wait in
+    // tcgen05.alloc
+    constexpr size_t kFloor = 116 * 1024;
     const int rows_cta = std::min(W, prm.R);
     const int agents_cta = (rows_cta + prm.G - 1) / prm.G;
     const int clusters = Hk * RGN;
+    // raw stages: as many as fit (up to 4), never fewer than two when a CTA
+    // has more than one tile (tile i+1 is expanded while tile i is in use)
+    int max_ns = 4;
+    while (max_ns > 2 && make_layout(D, BITS, W, max_ns).total + 1024 > kMaxSmem) --max_ns;
+    if (make_layout(D, BITS, W, max_ns).total + 1024 > kMaxSmem) return cudaErrorInvalidConfiguration;
+    // cluster size: fewest (waves x tiles per CTA), then the larger cluster;
+    // the staging rows and the merge slots must fit in the stage area
     int bestS = 0;
     long long best = -1;
     for (int S = 1; S <= 16 && S <= ntiles; ++S) {
         const int per = (ntiles + S - 1) / S;
-        const Layout lay = make_layout(D, BITS, W, std::min(max_stage, per));
-        const size_t smem = std::max<size_t>(lay.total + 1024, floor_bytes);
         const int own = (agents_cta + S - 1) / S * prm.G;
-        if ((size_t)S * own * (D + 2) * 4 > lay.misc) continue;
+        const Layout lay = make_layout(D, BITS, W, std::min(max_ns, per));
+        if (staging_bytes(D, W) + (size_t)S * own * (D + 4) * 4 > lay.misc) continue;
+        const size_t smem = std::max<size_t>(lay.total + 1024, kFloor);
         const int n = max_clusters<D, W, BITS>(S, smem);
         if (n < 1) continue;
         const long long waves = (clusters + n - 1) / n;
@@ -893,13 +948,13 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk
     }
     if (bestS == 0) return cudaErrorInvalidConfiguration;
     const int per = (ntiles + bestS - 1) / bestS;
-    const int S = (ntiles + per - 1) / per;
+    const int S = (ntiles + per - 1) / per;  // never more CTAs than needed for `per` tiles each
     prm.tps = per * kTile;
-    prm.nstage = std::min(max_stage, per);
     prm.own = (agents_cta + S - 1) / S * prm.G;
+    prm.nstage = std::min(max_ns, per);
     const Layout lay = make_layout(D, BITS, W, prm.nstage);
-    const size_t smem = std::max<size_t>(lay.total + 1024, floor_bytes);
-    if ((size_t)S * prm.own * (D + 2) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
+    if (staging_bytes(D, W) + (size_t)S * prm.own * (D + 4) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
+    const size_t smem = std::max<size_t>(lay.total + 1024, kFloor);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, Hk, RGN);
     cfg.blockDim = dim3(kThreads, 1, 1);
