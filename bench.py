@@ -264,7 +264,7 @@ def run_gpu(args):
                        "hbm_frac": round(gbs / peak, 4)}
     ph_info["attend"]["agent_steps_per_s"] = round(A * ws / (ph_ms["attend"] / 1e3), 1)
     dom = max(phases, key=lambda p: ph_ms[p])
-    dom_file = {"compress": "encode.cu", "attend": "attend.cu", "decompress": "decompress.cu"}[dom]
+    dom_file = {"compress": "encode.cu", "attend": "attend_tc_impl.cuh", "decompress": "decompress.cu"}[dom]
 
     # end to end through the same calls with pinned host buffers
     e2e = run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases) if not args.no_e2e else None
@@ -287,7 +287,8 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": ph_info[dom]["hbm_frac"],
                      "traffic": _traffic(dom_file), "peak_source": peak_kind,
                      "algo_bytes_per_launch": int(algo[dom])},
-        "gpu_launches": args.steps * L * 6,
+        # per layer: encode_v_kmax + encode_k_pack, attend_tc, decompress
+        "gpu_launches": args.steps * L * 4,
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
         "e2e": e2e,

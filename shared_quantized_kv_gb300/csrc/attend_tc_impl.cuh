@@ -550,10 +550,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     const uint32_t aQ = ptx::smem_u32(sQ), aP = ptx::smem_u32(sP);
     const bool designated = q == 0 && lane == 0;  // writes the next running maxima of its columns
 
-    auto wait_full = [&](int i) {
-        if (!timed_out && !ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs))
-            timed_out = true;
+    // Waits: thread 0 alone polls the mbarrier; every other thread sleeps in
+    // the CTA barrier that follows, so no issue slots go to spinning. Only
+    // thread 0 tracks timeouts.
+    auto t0_wait = [&](uint32_t bar, uint32_t parity) {
+        if (tid == 0 && !timed_out && !ptx::mbar_wait(bar, parity, kWaitNs)) timed_out = true;
     };
+    auto full_bar = [&](int i) { return bar_full + 8 * (i % p.nstage); };
+    auto full_par = [&](int i) { return (uint32_t)((i / p.nstage) & 1); };
     // K^ and V^T of tile i into TMEM buffer b
     auto convert = [&](int i, int b) {
         const unsigned char* st = sm + (i % p.nstage) * lay.stage;
@@ -588,7 +592,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
         ptx::tmem_stn<8>(tV + lane_off + cgp * 8, z);
         ptx::tmem_stn<8>(tV + 128 + lane_off + cgp * 8, z);
     }
-    wait_full(0);
+    t0_wait(full_bar(0), full_par(0));
+    __syncthreads();  // tile 0 has landed
     convert(0, 0);
     ptx::tc_fence_before();
     __syncthreads();  // K^(0), V^T(0) ready
@@ -598,16 +603,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     }
     for (int i = 0; i < ntile; ++i) {
         const int b = i & 1;
-        // MMA2(i-1) done: buffer b^1 (K^, V^T of tile i-1) and P' are free
-        if (i > 0 && !timed_out && !ptx::mbar_wait(bar_o, (i - 1) & 1, kWaitNs)) timed_out = true;
-        ptx::tc_fence_after();
-        if (i + 1 < ntile) {
-            wait_full(i + 1);
-            convert(i + 1, b ^ 1);
+        // MMA2(i-1) done: buffer b^1 (K^, V^T of tile i-1) and P' are free;
+        // tile i+1 has landed
+        if (i > 0 || i + 1 < ntile) {
+            if (i > 0) t0_wait(bar_o, (i - 1) & 1);
+            if (i + 1 < ntile) t0_wait(full_bar(i + 1), full_par(i + 1));
+            __syncthreads();
+            ptx::tc_fence_after();
         }
+        if (i + 1 < ntile) convert(i + 1, b ^ 1);
 
         // softmax of tile i
-        if (!timed_out && !ptx::mbar_wait(bar_s, i & 1, kWaitNs)) timed_out = true;
+        t0_wait(bar_s, i & 1);
+        __syncthreads();
         ptx::tc_fence_after();
         const unsigned char* st = sm + (i % p.nstage) * lay.stage;
         const bool valid = (t_begin + i * kTile + tok) < t_end;
@@ -731,8 +739,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     }
     // the last P.V commit covers every MMA issued; waited for even after a
     // timeout, so that no MMA is still running when TMEM is released
-    if (!ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
-    ptx::tc_fence_after();
+    if (tid == 0 && !ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
     if (tid == 0 && timed_out) {
         // give the copies still in flight a bounded chance to land before the
         // stages are reused and the CTA exits
@@ -743,6 +750,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     // this CTA is done with its stages, Q and P': other CTAs may write merge
     // slots there once every CTA of the cluster has arrived (the wait comes
     // right before the sends; the barrier inits are older still)
+    __syncthreads();
+    ptx::tc_fence_after();
     ptx::cluster_arrive();
 
     // 4. epilogue: row sums and O^T columns into the staging rows, TMEM released
@@ -776,7 +785,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
         sO[tid * ROWF + D] = sMx[(ntile & 1) * W + tid];
         sO[tid * ROWF + D + 1] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
     }
-    if (timed_out && lane == 0) atomicOr(p.status, kStTimeout);
+    if (timed_out) atomicOr(p.status, kStTimeout);
     ptx::fence_proxy_async();
     __syncthreads();
 
@@ -792,8 +801,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 
     // 6. merge the owned rows once all S copies of each have landed, one warp per row
     if (own_cnt > 0) {
-        bool ok = !timed_out && ptx::mbar_wait(bar_m, 0, kWaitNs);
-        if (!ok && tid == 0) atomicOr(p.status, kStTimeout);
+        const bool bad = tid == 0 && (timed_out || !ptx::mbar_wait(bar_m, 0, kWaitNs));
+        const bool ok = !__syncthreads_or(bad);
+        if (bad) atomicOr(p.status, kStTimeout);
         const int G = p.G;
         for (int loc = warp; ok && loc < own_cnt; loc += kThreads / 32) {
             const int ar = (loc / G) * S + crank, j = loc % G;
