@@ -10,33 +10,38 @@
 // shares the KV head is served by one pass over the packed pool bytes, so the
 // pool is read once per step no matter how many agents there are.
 //
-// Per CTA: 1024 threads, one CTA per SM. Warp w owns TMEM lane quarter w % 4
-// and column group w / 4 (eight groups), so that every per-tile phase is
-// spread over 32 warps and short. Both MMAs take their A operand from tensor
-// memory; the expanded K and V never touch shared memory:
-//   * thread 0 keeps a ring of shared-memory stages filled: a TMA tile of 128
-//     tokens of int8 K (128-byte swizzle, so that one thread per token reads
-//     its row without bank conflicts), the tile's packed V code groups and its
-//     norms (plain bulk copies), one mbarrier per stage. When no kernel before
-//     it in the stream can still be writing the layer, the first tiles are
-//     requested before the grid-dependency wait, overlapping the previous
-//     kernel's tail; the TMEM allocation overlaps the Q load.
-//   * K^: thread = (token, 16 channels), int8 -> fp16 (exact, byte permutes)
-//     straight into TMEM as the A operand of S^T = K^ Q^T (tokens on M = 128,
-//     query rows on N); Q is fp16 in shared memory, each row scaled by its own
-//     power of two.
-//   * V^T: thread = (rotated coordinate, 16 tokens): codes of the pool layout
-//     (one packed sequence per coordinate and 32-token group) -> fp16
-//     lam * c[code] by byte-permute table lookups, into TMEM as the A operand
-//     of O^T += V^T P'^T. The accumulator stays in the rotated domain,
-//     sum_t p_t n_t c[code_t]; the inverse FWHT runs once per output row.
-//     K^ and V^T are double-buffered: tile i+1 is expanded while the MMAs of
-//     tile i run.
-//   * softmax with thread = (token, W/8 query rows): logits in log2 units
-//     against a running per-row maximum that is raised (with a rescale of O^T
-//     in TMEM) only when a logit exceeds it by more than 2^8; P' = p * n_t /
-//     2^k split into fp16 hi (top 11 significant bits) and fp16 lo (the exact
-//     remainder), two MN-major operands, so P' carries ~22 bits into the MMA.
+// Per CTA (one per SM): 16 worker warps and one issuer warp. Worker warp w
+// owns TMEM lane quarter w % 4 and column group w / 4. The issuer warp
+// allocates tensor memory and its lane 0 issues every bulk copy and MMA, so
+// that the time the tensor pipe takes to accept a batch of MMAs never stalls
+// a worker; workers tell it that operands are ready through counted
+// mbarriers, and wait for its copies and MMAs on mbarriers (one worker thread
+// polls, the others sleep in a named barrier).
+//   * copies: per tile of 128 tokens a TMA load of int8 K (128-byte swizzle,
+//     so that one thread per token reads its row without bank conflicts) and
+//     bulk copies of the tile's packed V code groups and norms into a ring of
+//     stages, one mbarrier per stage. When no kernel before it in the stream
+//     can still be writing the layer, the first tiles are requested before
+//     the grid-dependency wait, overlapping the previous kernel's tail.
+//   * the context split of a CTA is processed in chunks of up to three tiles
+//     (two for 128 query rows), sized by tensor memory:
+//     - K^ of every tile of the chunk: int8 -> fp16 (exact, byte permutes)
+//       straight into TMEM as the A operand of S^T = K^ Q^T (tokens on
+//       M = 128, query rows on N); Q is fp16 in shared memory, each row scaled
+//       by its own power of two. One batch of MMAs for the chunk.
+//     - V^T: thread = (rotated coordinate, 32 tokens): codes of the pool
+//       layout (one packed sequence per coordinate and 32-token group) ->
+//       fp16 lam * c[code] by byte-permute table lookups, into the K^
+//       columns once the S^T MMAs are done, as the A operand of
+//       O^T += V^T P'^T. The accumulator stays in the rotated domain,
+//       sum_t p_t n_t c[code_t]; the inverse FWHT runs once per output row.
+//     - one exact maximum per row over the chunk (thread = token, then
+//       redux across lanes and shared memory across lane quarters); O^T and
+//       the row sums are rescaled at most once per chunk.
+//     - per tile, P' = p * n_t / 2^k split into fp16 hi (top 11 significant
+//       bits) and fp16 lo (the exact remainder), two MN-major operands, so P'
+//       carries ~22 bits into the MMA; the tile's P'.V MMAs run while the
+//       next tile's P' is formed.
 //   epilogue: each CTA stages its partial rows (O^T column, m, l) in shared
 //     memory and sends each row with one bulk copy into the shared memory of
 //     the CTA that owns the row's agent, completing on the owner's mbarrier;
@@ -61,11 +66,15 @@ namespace kvp {
 namespace {
 
 constexpr int kTile = 128;
-constexpr int kThreads = 1024;  // 32 warps: (TMEM lane quarter) x (column group)
-constexpr int kGroups = 8;      // column groups
-constexpr float kTau = 8.0f;    // P <= 2^kTau between rescales
+constexpr int kWorkers = 512;               // 16 worker warps: (TMEM lane quarter) x (column group)
+constexpr int kWorkerWarps = kWorkers / 32;
+constexpr int kThreads = kWorkers + 32;     // + the issuer warp
+constexpr int kIssuer = kWorkerWarps;       // warp index of the issuer
+constexpr int kGroups = 4;                  // column groups of worker warps
+constexpr uint32_t kBarWork = 1;            // named barrier of the worker warps
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
-constexpr uint32_t kCols = 512;  // TMEM: S^T, O^T, then K^ and V^T twice
+constexpr uint32_t kCols = 512;             // TMEM: O^T, S^T per chunk tile, K^/V^T per chunk tile
+constexpr int kMaxChunk = 3;
 
 struct TcParams {
     const uint8_t* vcodes;
@@ -83,6 +92,7 @@ struct TcParams {
     float scale_log2;
     int tps;     // tokens per CTA, a multiple of kTile
     int nstage;  // shared-memory stages of raw tiles
+    int nc;      // tiles per chunk, at most the stages
     int early;   // 1: the layer's bytes may be read before the grid-dependency wait
     int own;     // merge slots per source CTA (the most rows one CTA owns)
     int* status;
@@ -97,9 +107,12 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// most tiles per chunk for W query rows (TMEM: O^T, then S^T and K^/V^T per tile)
+__host__ __device__ constexpr int chunk_tiles(int W) { return W <= 64 ? 3 : 2; }
+
 // W = query rows per CTA (MMA N). After the main loop everything below misc
 // (raw stages, Q, P') is reused: this CTA's staging rows at 0, the merge
-// slots that other CTAs fill right after them (epilogue_bytes).
+// slots that other CTAs fill right after them.
 __host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage) {
     Layout L;
     L.rv = kTile * D;
@@ -109,12 +122,12 @@ __host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage
     L.q = o;
     o = align_up(o + W * D * 2, 1024);
     L.p = o;
-    L.plo = W <= 64 ? 16384 : 32768;  // P' hi, then P' lo
-    o += 2 * L.plo;
+    L.plo = W <= 64 ? 16384 : 32768;  // per chunk tile: P' hi, then P' lo
+    o += chunk_tiles(W) * 2 * L.plo;
     L.misc = o;
-    o += 15 * W * 4;
+    o += 14 * W * 4;
     L.bars = align_up(o, 8);
-    o = L.bars + 8 * (nstage + 3) + 8;
+    o = L.bars + 8 * (nstage + 4 + kMaxChunk) + 8;
     L.total = align_up(o, 1024);
     return L;
 }
@@ -271,19 +284,22 @@ __device__ __forceinline__ void decode16(const unsigned char* row, int h, const 
 }
 
 // Attention of the owned agents' rows over their private bf16 tails (plain
-// CUDA cores, online softmax in log2 units, 256 tokens per chunk). Writes the
-// unnormalised accumulator to `out` and (m, l) per row to `tailml`; `stage` is
-// 13 KB of shared memory that is free until the main loop.
+// CUDA cores on the worker threads, online softmax in log2 units, 256 tokens
+// per chunk). Writes the unnormalised accumulator to `out` and (m, l) per row
+// to `tailml`; `stage` is 13 KB of shared memory that is free until the main
+// loop. Every thread of the CTA calls it (it holds CTA barriers).
 template <int D>
 __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* stage, float* tailml,
                                             int S, int crank, int g, int row0, int nrows) {
     constexpr int TCH = 256;
+    constexpr int RPT = kWorkers / D;  // P.V phase: row sub-blocks
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+    const bool worker = tid < kWorkers;
     float* tq = reinterpret_cast<float*>(stage);                                // [8][D]
     float* tl = reinterpret_cast<float*>(stage + 8 * D * 4);                   // [8][TCH]
     float* tmx = reinterpret_cast<float*>(stage + 8 * D * 4 + 8 * TCH * 4);    // [8]
-    const int c = tid % D, sub = tid / D;  // P.V phase: row sub, channel c
-    const int t = tid % TCH, k0 = tid / TCH;  // logit phase: token t, rows k0 and k0 + 4
+    const int c = tid % D, sub = tid / D;      // P.V phase: rows k with k % RPT == sub, channel c
+    const int t = tid % TCH, k0 = tid / TCH;   // logit phase: token t, rows k0 + 2 * kk
     const int G = p.G;
     for (int ar = crank; ar * G < nrows; ar += S) {
         const int a = row0 / G + ar;
@@ -291,22 +307,21 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
         const long long tbase = ((long long)a * p.Hk + g) * p.tail_max;
         for (int jb = 0; jb < G; jb += 8) {
             const int cnt = min(8, G - jb);
-            for (int i = tid; i < 8 * D; i += kThreads) {
+            for (int i = tid; worker && i < 8 * D; i += kWorkers) {
                 const int k = i / D, cc = i % D;
                 tq[k * D + cc] = k < cnt ? bf2f(p.Q[((long long)a * p.Hq + g * G + jb + k) * D + cc]) : 0.f;
             }
-            float m_run[8];
+            float m_run[8], l_run[8], acc[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) m_run[k] = -CUDART_INF_F;
-            float acc = 0.f, l_run = 0.f;
+            for (int k = 0; k < 8; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; acc[k] = 0.f; }
             __syncthreads();
             for (int c0 = 0; c0 < tmax; c0 += TCH) {
-                float lg[2];
+                float lg[4];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int k = k0 + 4 * kk;
+                for (int kk = 0; kk < 4; ++kk) {
+                    const int k = k0 + 2 * kk;
                     lg[kk] = -CUDART_INF_F;
-                    if (k < cnt && c0 + t < tmax) {
+                    if (worker && k < cnt && c0 + t < tmax) {
                         const uint16_t* kr = p.tK + (tbase + c0 + t) * D;
                         const float* qq = tq + k * D;
                         float dot = 0.f;
@@ -323,7 +338,7 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
                         }
                         lg[kk] = dot * p.scale_log2;
                     }
-                    tl[k * TCH + t] = lg[kk];
+                    if (worker) tl[k * TCH + t] = lg[kk];
                 }
                 __syncthreads();
                 if (warp < 8) {  // row maximum of the chunk
@@ -342,38 +357,45 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
                     alpha[k] = (mn == -CUDART_INF_F) ? 1.f : ptx::ex2(m_run[k] - mn);
                     m_run[k] = mn;
                 }
+                if (worker) {
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int k = k0 + 4 * kk;
-                    tl[k * TCH + t] = (lg[kk] == -CUDART_INF_F) ? 0.f : ptx::ex2(lg[kk] - m_run[k]);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k = k0 + 2 * kk;
+                        float mk = m_run[0];
+#pragma unroll
+                        for (int q2 = 1; q2 < 8; ++q2) if (q2 == k) mk = m_run[q2];
+                        tl[k * TCH + t] = (lg[kk] == -CUDART_INF_F) ? 0.f : ptx::ex2(lg[kk] - mk);
+                    }
                 }
                 __syncthreads();
-                if (sub < cnt) {
-                    float al = 1.f;
-#pragma unroll
-                    for (int k = 0; k < 8; ++k) if (k == sub) al = alpha[k];
+                if (worker) {
                     const uint16_t* vr0 = p.tV + (tbase + c0) * D + c;
                     const int n2 = min(TCH, tmax - c0);
-                    float sacc = 0.f, ls = 0.f;
-                    for (int t2 = 0; t2 < n2; ++t2) {
-                        const float pv = tl[sub * TCH + t2];
-                        sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
-                        ls += pv;
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        if (k % RPT != sub || k >= cnt) continue;
+                        float sacc = 0.f, ls = 0.f;
+                        for (int t2 = 0; t2 < n2; ++t2) {
+                            const float pv = tl[k * TCH + t2];
+                            sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
+                            ls += pv;
+                        }
+                        acc[k] = acc[k] * alpha[k] + sacc;
+                        l_run[k] = l_run[k] * alpha[k] + ls;
                     }
-                    acc = acc * al + sacc;
-                    l_run = l_run * al + ls;
                 }
                 __syncthreads();
             }
-            if (sub < cnt) {
-                const int rr = ar * G + jb + sub;
-                p.out[((long long)a * p.Hq + g * G + jb + sub) * D + c] = acc;
-                if (c == 0) {
-                    float mr = -CUDART_INF_F;
+            if (worker) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) if (k == sub) mr = m_run[k];
-                    tailml[2 * rr] = mr;
-                    tailml[2 * rr + 1] = l_run;
+                for (int k = 0; k < 8; ++k) {
+                    if (k % RPT != sub || k >= cnt) continue;
+                    const int rr = ar * G + jb + k;
+                    p.out[((long long)a * p.Hq + g * G + jb + k) * D + c] = acc[k];
+                    if (c == 0) {
+                        tailml[2 * rr] = m_run[k];
+                        tailml[2 * rr + 1] = l_run[k];
+                    }
                 }
             }
             __syncthreads();
@@ -384,14 +406,15 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
 template <int D, int W, int BITS>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
-    constexpr int CPT = W / kGroups;       // query rows (TMEM columns) per thread: 2, 4, 8 or 16
-    constexpr int CH = CPT < 8 ? CPT : 8;  // columns per softmax chunk
-    constexpr int EPL = D / 32;            // channels per lane in the merge
-    constexpr int VB = D * BITS / 8;       // code bytes per token
-    constexpr int GB = D * 4 * BITS;       // bytes per 32-token code group
-    constexpr int KCH = D / 16;            // 16-byte K chunks per token row
-    constexpr int ROWF = D + 4;            // floats per merge row: O^T column, m, l, padding
-    constexpr uint32_t kColO = 128, kColK = 256, kColV = 320;  // + 128 for the second buffer
+    constexpr int CPT = W / kGroups;         // query rows (TMEM columns) per worker thread: 4..32
+    constexpr int CH = CPT < 16 ? CPT : 16;  // columns per TMEM load
+    constexpr int EPL = D / 32;              // channels per lane in the merge
+    constexpr int VB = D * BITS / 8;         // code bytes per token
+    constexpr int GB = D * 4 * BITS;         // bytes per 32-token code group
+    constexpr int KC = D / 64;               // 16-byte K chunks per worker thread (of D / 16 per row)
+    constexpr int ROWF = D + 4;              // floats per merge row: O^T column, m, l, padding
+    constexpr int NC = chunk_tiles(W);
+    constexpr uint32_t kColS = 128, kColKV = 128 + NC * W;  // O^T at column 0
 
     extern __shared__ unsigned char smem_raw[];
     unsigned char* sm = reinterpret_cast<unsigned char*>(
@@ -401,36 +424,41 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     const Layout lay = make_layout(D, BITS, W, p.nstage);
     unsigned char* sQ = sm + lay.q;
     unsigned char* sP = sm + lay.p;
-    float* sO = reinterpret_cast<float*>(sm);                                // epilogue: [W][ROWF]
-    float* slots = reinterpret_cast<float*>(sm + staging_bytes(D, W));       // epilogue: [S][own][ROWF]
-    float* sMx = reinterpret_cast<float*>(sm + lay.misc);     // [2][W] running row maxima (log2 units)
-    float* sCf = sMx + 2 * W;                                 // [W] logit factor per row
-    float* lsum = sCf + W;                                    // [4][W] row-sum partials
-    float* colmax = lsum + 4 * W;                             // [4][W]
-    float* tailml = colmax + 4 * W;                           // [W][2]
+    float* sO = reinterpret_cast<float*>(sm);                             // epilogue: [W][ROWF]
+    float* slots = reinterpret_cast<float*>(sm + staging_bytes(D, W));    // epilogue: [S][own][ROWF]
+    float* sMx = reinterpret_cast<float*>(sm + lay.misc);  // [W] final row maxima (log2 units)
+    float* sCf = sMx + W;                                  // [W] logit factor per row
+    float* lsum = sCf + W;                                 // [4][W] row-sum partials
+    float* colmax = lsum + 4 * W;                          // [4][W]
+    float* tailml = colmax + 4 * W;                        // [W][2]
     uint32_t* sOwn = reinterpret_cast<uint32_t*>(tailml + 2 * W);  // [W] owner << 16 | slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + p.nstage + 3);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + p.nstage + 4 + kMaxChunk);
     const uint32_t bar_full = ptx::smem_u32(bars);
-    const uint32_t bar_s = bar_full + 8 * p.nstage;  // S^T of the tile is in TMEM
-    const uint32_t bar_o = bar_s + 8;                // the tile's P.V MMAs are done
+    const uint32_t bar_s = bar_full + 8 * p.nstage;  // S^T of the chunk is in TMEM
+    const uint32_t bar_o = bar_s + 8;                // the chunk's P'.V MMAs are done
     const uint32_t bar_m = bar_o + 8;                // every merge row sent to this CTA has landed
+    const uint32_t bar_k = bar_m + 8;                // workers: K^ of the chunk is in TMEM
+    const uint32_t bar_p = bar_k + 8;                // workers: P'_j (and V^T) ready, one per chunk tile
 
     const int g = blockIdx.y;
     const int row0 = blockIdx.z * W;
     const int nrows = min(W, p.R - row0);  // a multiple of G
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int q = warp & 3, cgp = warp >> 2;
-    const int tok = q * 32 + lane;      // token of this thread in S^T / K^; channel in O^T / V^T
-    const bool has_ch = q * 32 < D;     // warp-uniform: lanes of this quarter hold channels
+    const bool worker = warp < kWorkerWarps;
+    const int q = warp & 3, cgp = (warp >> 2) & 3;
+    const int tok = q * 32 + lane;      // token of a worker in S^T / K^; channel in O^T / V^T
+    const bool has_ch = worker && q * 32 < D;  // warp-uniform
     const int t_begin = crank * p.tps;
     const int t_end = min(p.ctx, t_begin + p.tps);
     const int ntile = (t_end - t_begin + kTile - 1) / kTile;  // >= 1
+    const int nchunk = (ntile + p.nc - 1) / p.nc;
     const long long head_tok = (long long)g * p.ctx_pad;
     const uint32_t stage_bytes = kTile * D + kTile * VB + kTile * 4;
     // rows owned here: the G rows of every agent ar (relative) with ar % S == crank
     const int nag = nrows / p.G;
     const int own_cnt = crank < nag ? ((nag - crank + S - 1) / S) * p.G : 0;
+    const bool leader = warp == kIssuer && lane == 0;  // issues copies and MMAs
 
     auto issue_tile = [&](int i) {
         const int s = i % p.nstage;
@@ -453,13 +481,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     };
 
     // ---------------------------------------------------------------- setup
-    if (tid == 0) {
-        for (int s = 0; s < p.nstage + 3; ++s) ptx::mbar_init(bar_full + 8 * s, 1);
+    if (leader) {
+        for (int s = 0; s < p.nstage + 3; ++s) ptx::mbar_init(bar_full + 8 * s, 1);  // stages, S^T, P'.V, merge
+        ptx::mbar_init(bar_k, kWorkerWarps);
+        for (int j = 0; j < kMaxChunk; ++j) ptx::mbar_init(bar_p + 8 * j, kWorkerWarps);
         ptx::mbar_init_fence();
         if (own_cnt > 0) ptx::mbar_expect_tx(bar_m, (uint32_t)(S * own_cnt * ROWF * 4));
         if (p.early) issue_first();
     }
-    if (warp == 0) ptx::tmem_alloc(ptx::smem_u32(tslot), kCols);
+    if (warp == kIssuer) ptx::tmem_alloc(ptx::smem_u32(tslot), kCols);  // overlaps the Q load
     if (tid < W) {
         sMx[tid] = -CUDART_INF_F;
         const int ar = tid / p.G;  // agent of row tid, relative to the CTA's first agent
@@ -468,7 +498,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 
     ptx::grid_dep_wait();
     ptx::grid_dep_launch();
-    if (tid == 0 && !p.early) issue_first();
+    if (leader && !p.early) issue_first();
     bool timed_out = false;
     // P' = p * n_t / nref with nref the power of two >= the largest norm of the layer
     const uint32_t nb = *p.vnmax;
@@ -477,9 +507,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     // 1. Q rows -> fp16 in a 128-byte-swizzled K-major operand; each row is
     //    scaled by the power of two that puts its largest |q| in [2^14, 2^15)
     //    (exact), and the logit factor of the row undoes it.
-    {
+    if (worker) {
         constexpr int CPR = D / 8;            // 16-byte chunks per row
-        constexpr int RPP = kThreads / CPR;   // rows per pass
+        constexpr int RPP = kWorkers / CPR;   // rows per pass
         constexpr int NP = (W + RPP - 1) / RPP;
         uint4 qv[NP];
         const int c = tid % CPR;
@@ -536,215 +566,248 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     ptx::tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const uint32_t tS = tmem, tO = tmem + kColO, tK = tmem + kColK, tV = tmem + kColV;
+    const uint32_t tO = tmem;                  // O^T: W columns
+    const uint32_t tS = tmem + kColS;          // S^T of chunk tile j: W columns at tS + j*W
+    const uint32_t tKV = tmem + kColKV;        // K^, then V^T, of chunk tile j: 64 columns at tKV + 64*j
+    float lp[CPT];     // worker: row-sum partials of its token
+    float mrun[CPT];   // worker: running row maxima of its columns (the same in every worker)
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) { lp[j] = 0.f; mrun[j] = -CUDART_INF_F; }
+    const int colb = cgp * CPT;
 
-    // 3. main loop
-    uint32_t tlo[4], thi[4];
+    if (warp == kIssuer) {
+        // 3a. issuer: S^T MMAs once the chunk's K^ is in TMEM, P'.V MMAs per
+        //     tile once its P' is in shared memory; refills the chunk's stages
+        //     once the first P' shows that the workers are done with them
+        if (lane == 0) {
+            const uint32_t idesc1 = ptx::idesc_f16(128, W, 0, 0);
+            const uint32_t idesc2 = ptx::idesc_f16(128, W, 0, 1);
+            const uint32_t aQ = ptx::smem_u32(sQ), aP = ptx::smem_u32(sP);
+            for (int c0 = 0, k = 0; c0 < ntile; c0 += p.nc, ++k) {
+                const int n = min(p.nc, ntile - c0);
+                if (!timed_out && !ptx::mbar_wait(bar_k, k & 1, kWaitNs)) timed_out = true;
+                ptx::tc_fence_after();
+                for (int j = 0; j < n; ++j) {  // S^T_j = K^_j Q^T
 #pragma unroll
-    for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
-    float lp[CPT];  // per-thread row-sum partials
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t bd = ptx::sdesc(aQ + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
+                        ptx::mma_f16_ta(tS + j * W, tKV + 64 * j + ks * 8, bd, idesc1, ks > 0 ? 1u : 0u);
+                    }
+                }
+                ptx::mma_commit(bar_s);
+                for (int j = 0; j < n; ++j) {  // O^T += V^T_j (P'_hi + P'_lo)_j^T
+                    if (!timed_out && !ptx::mbar_wait(bar_p + 8 * j, k & 1, kWaitNs)) timed_out = true;
+                    ptx::tc_fence_after();
+                    const uint32_t aPj = aP + j * 2 * lay.plo;
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) lp[j] = 0.f;
-    const uint32_t idesc1 = ptx::idesc_f16(128, W, 0, 0);
-    const uint32_t idesc2 = ptx::idesc_f16(128, W, 0, 1);
-    const uint32_t aQ = ptx::smem_u32(sQ), aP = ptx::smem_u32(sP);
-    const bool designated = q == 0 && lane == 0;  // writes the next running maxima of its columns
-
-    // Waits: thread 0 alone polls the mbarrier; every other thread sleeps in
-    // the CTA barrier that follows, so no issue slots go to spinning. Only
-    // thread 0 tracks timeouts.
-    auto t0_wait = [&](uint32_t bar, uint32_t parity) {
-        if (tid == 0 && !timed_out && !ptx::mbar_wait(bar, parity, kWaitNs)) timed_out = true;
-    };
-    auto full_bar = [&](int i) { return bar_full + 8 * (i % p.nstage); };
-    auto full_par = [&](int i) { return (uint32_t)((i / p.nstage) & 1); };
-    // K^ and V^T of tile i into TMEM buffer b
-    auto convert = [&](int i, int b) {
-        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
-        if (cgp < KCH) {  // token tok, channels 16*cgp .. 16*cgp+15
-            const int sw = D == 128 ? (tok & 7) : ((tok >> 1) & 3);  // TMA 128 B / 64 B swizzle
-            const uint4 u = *reinterpret_cast<const uint4*>(st + tok * D + ((cgp ^ sw) << 4));
-            uint32_t r[8];
-            i8x4_to_h2x2(u.x, r[0], r[1]);
-            i8x4_to_h2x2(u.y, r[2], r[3]);
-            i8x4_to_h2x2(u.z, r[4], r[5]);
-            i8x4_to_h2x2(u.w, r[6], r[7]);
-            ptx::tmem_stn<8>(tK + 128 * b + lane_off + cgp * 8, r);
-        }
-        if (has_ch) {  // channel tok, tokens 16*cgp .. 16*cgp+15
-            uint32_t r[8];
-            decode16<BITS>(st + lay.rv + (cgp >> 1) * GB + tok * (4 * BITS), cgp & 1, tlo, thi, r);
-            ptx::tmem_stn<8>(tV + 128 * b + lane_off + cgp * 8, r);
-        }
-        ptx::tmem_wait_st();
-    };
-    auto mma1 = [&](int b) {  // S^T = K^ Q^T
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-            const uint64_t bd = ptx::sdesc(aQ + (ks / 4) * (W * 128) + (ks % 4) * 32, 16, 1024);
-            ptx::mma_f16_ta(tS, tK + 128 * b + ks * 8, bd, idesc1, ks > 0 ? 1u : 0u);
-        }
-        ptx::mma_commit(bar_s);
-    };
-
-    if (D == 64 && !has_ch) {  // V^T rows 64..127 stay zero in both buffers (M = 128 with d = 64)
-        const uint32_t z[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        ptx::tmem_stn<8>(tV + lane_off + cgp * 8, z);
-        ptx::tmem_stn<8>(tV + 128 + lane_off + cgp * 8, z);
-    }
-    t0_wait(full_bar(0), full_par(0));
-    __syncthreads();  // tile 0 has landed
-    convert(0, 0);
-    ptx::tc_fence_before();
-    __syncthreads();  // K^(0), V^T(0) ready
-    if (tid == 0) {
-        ptx::tc_fence_after();
-        mma1(0);
-    }
-    for (int i = 0; i < ntile; ++i) {
-        const int b = i & 1;
-        // MMA2(i-1) done: buffer b^1 (K^, V^T of tile i-1) and P' are free;
-        // tile i+1 has landed
-        if (i > 0 || i + 1 < ntile) {
-            if (i > 0) t0_wait(bar_o, (i - 1) & 1);
-            if (i + 1 < ntile) t0_wait(full_bar(i + 1), full_par(i + 1));
-            __syncthreads();
-            ptx::tc_fence_after();
-        }
-        if (i + 1 < ntile) convert(i + 1, b ^ 1);
-
-        // softmax of tile i
-        t0_wait(bar_s, i & 1);
-        __syncthreads();
-        ptx::tc_fence_after();
-        const unsigned char* st = sm + (i % p.nstage) * lay.stage;
-        const bool valid = (t_begin + i * kTile + tok) < t_end;
-        const float ns = valid ? reinterpret_cast<const float*>(st + lay.rn)[tok] * vr : 0.f;
-        const float* mcur = sMx + (i & 1) * W;         // running maxima before this tile
-        float* mnext = sMx + ((i + 1) & 1) * W;        // after it
-        const int colb = cgp * CPT;
-        float over = -CUDART_INF_F;
-#pragma unroll
-        for (int c0 = 0; c0 < CPT; c0 += CH) {
-            float y[CH];
-            tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < CH; ++e) {
-                const float lg = valid ? y[e] * sCf[colb + c0 + e] : -CUDART_INF_F;
-                over = fmaxf(over, lg - mcur[colb + c0 + e]);
+                    for (int ks = 0; ks < kTile / 16; ++ks) {
+                        const uint64_t bh = ptx::sdesc(aPj + ks * 2048, 16384, 1024);
+                        const uint64_t bl = ptx::sdesc(aPj + lay.plo + ks * 2048, 16384, 1024);
+                        ptx::mma_f16_ta(tO, tKV + 64 * j + ks * 8, bh, idesc2, (c0 + j > 0 || ks > 0) ? 1u : 0u);
+                        ptx::mma_f16_ta(tO, tKV + 64 * j + ks * 8, bl, idesc2, 1u);
+                    }
+                    if (j == 0)
+                        for (int jj = 0; jj < n; ++jj)
+                            if (c0 + jj + p.nstage < ntile) issue_tile(c0 + jj + p.nstage);
+                }
+                ptx::mma_commit(bar_o);
+            }
+            // the last commit covers every MMA issued; waited for even after
+            // a timeout, so that no MMA is still running when TMEM is released
+            if (!ptx::mbar_wait(bar_o, (nchunk - 1) & 1, kWaitNs)) timed_out = true;
+            if (timed_out) {
+                // give the copies still in flight a bounded chance to land
+                for (int i = max(0, ntile - p.nstage); i < ntile; ++i)
+                    ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs);
             }
         }
-        const bool slow = ptx::bar_or(2, kThreads, over > kTau);
-        auto new_max = [&](int col) {
-            return fmaxf(mcur[col], fmaxf(fmaxf(colmax[col], colmax[W + col]),
-                                          fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
+        __syncwarp();
+    } else {
+        // 3b. workers
+        uint32_t tlo[4], thi[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
+        // one worker polls, the others sleep in the workers' named barrier
+        auto wwait = [&](uint32_t bar, uint32_t parity) {
+            if (tid == 0 && !timed_out && !ptx::mbar_wait(bar, parity, kWaitNs)) timed_out = true;
         };
-        if (slow) {
-            // exact maxima of this tile's rows, then rescale what was accumulated
+        // after a warp's own TMEM stores / shared-memory writes, one arrive for the warp
+        auto warp_arrive = [&](uint32_t bar) {
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar);
+            __syncwarp();
+        };
+        for (int c0 = 0, k = 0; c0 < ntile; c0 += p.nc, ++k) {
+            const int n = min(p.nc, ntile - c0);
+            int sj[NC];  // raw stage of chunk tile j
 #pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += CH) {
-                float y[CH];
-                tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
-                ptx::tmem_wait_ld();
+            for (int j = 0; j < NC; ++j) sj[j] = (c0 + j) % p.nstage;
+            // (a) the previous chunk's P'.V MMAs are done (K^/V^T columns, P'
+            //     free, O^T final for this chunk's rescale); the tiles landed
+            if (k > 0) wwait(bar_o, (k - 1) & 1);
+            for (int j = 0; j < n; ++j) wwait(bar_full + 8 * sj[j], ((c0 + j) / p.nstage) & 1);
+            ptx::bar_sync(kBarWork, kWorkers);
+            ptx::tc_fence_after();
+
+            // (b) K^ of the chunk: token tok, channels 16*KC*cgp .. +16*KC
+            if (cgp * KC < D / 16) {
 #pragma unroll
-                for (int e = 0; e < CH; ++e) {
-                    const float lg = valid ? y[e] * sCf[colb + c0 + e] : -CUDART_INF_F;
-                    const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(lg)));
-                    if (lane == ((c0 + e) & 31)) colmax[q * W + colb + c0 + e] = mx;
+                for (int j = 0; j < NC; ++j) {
+                    if (j >= n) break;
+                    const unsigned char* st = sm + sj[j] * lay.stage;
+                    const int sw = D == 128 ? (tok & 7) : ((tok >> 1) & 3);  // TMA 128 B / 64 B swizzle
+                    uint32_t r[8 * KC];
+#pragma unroll
+                    for (int kc = 0; kc < KC; ++kc) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(st + tok * D + (((cgp * KC + kc) ^ sw) << 4));
+                        i8x4_to_h2x2(u.x, r[8 * kc + 0], r[8 * kc + 1]);
+                        i8x4_to_h2x2(u.y, r[8 * kc + 2], r[8 * kc + 3]);
+                        i8x4_to_h2x2(u.z, r[8 * kc + 4], r[8 * kc + 5]);
+                        i8x4_to_h2x2(u.w, r[8 * kc + 6], r[8 * kc + 7]);
+                    }
+                    if constexpr (KC == 2) ptx::tmem_st16(tKV + 64 * j + lane_off + cgp * 16, r);
+                    else ptx::tmem_stn<8>(tKV + 64 * j + lane_off + cgp * 8, r);
+                }
+                ptx::tmem_wait_st();
+            }
+            warp_arrive(bar_k);
+
+            // (c) token norms of the chunk while the S^T MMAs run
+            float nsj[NC];
+#pragma unroll
+            for (int j = 0; j < NC; ++j) {
+                nsj[j] = 0.f;
+                if (j < n) {
+                    const bool valid = (t_begin + (c0 + j) * kTile + tok) < t_end;
+                    nsj[j] = valid ? reinterpret_cast<const float*>(sm + sj[j] * lay.stage + lay.rn)[tok] * vr : 0.f;
                 }
             }
-            ptx::bar_sync(1, kThreads);
+
+            // (d) S^T is in TMEM and K^ is consumed: V^T (channel tok, tokens
+            //     32*cgp .. 32*cgp+31) into the same columns
+            wwait(bar_s, k & 1);
+            ptx::bar_sync(kBarWork, kWorkers);
+            ptx::tc_fence_after();
+            if (has_ch) {
 #pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += CH) {
-                float alpha[CH];
-#pragma unroll
-                for (int e = 0; e < CH; ++e) {
-                    const int col = colb + c0 + e;
-                    const float mo = mcur[col], mn = new_max(col);
-                    alpha[e] = (mo == -CUDART_INF_F) ? 0.f : ptx::ex2(mo - mn);
-                    lp[c0 + e] *= alpha[e];
-                    if (designated) mnext[col] = mn;
+                for (int j = 0; j < NC; ++j) {
+                    if (j >= n) break;
+                    uint32_t r[16];
+                    decode32<BITS>(sm + sj[j] * lay.stage + lay.rv + cgp * GB + tok * (4 * BITS), tlo, thi, r);
+                    ptx::tmem_st16(tKV + 64 * j + lane_off + cgp * 16, r);
                 }
-                if (i > 0 && has_ch) {  // O^T columns (MMA2(i-1) is done)
-                    uint32_t r[CH];
-                    ptx::tmem_ldn<CH>(tO + lane_off + colb + c0, r);
+            }
+
+            // (e) exact maxima of the chunk's rows: this thread's token over its
+            //     tiles, then across lanes (redux) and lane quarters (shared memory)
+            {
+                float cmax[CPT];
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) cmax[e] = -CUDART_INF_F;
+#pragma unroll
+                for (int j = 0; j < NC; ++j) {
+                    if (j >= n) break;
+                    const bool valid = (t_begin + (c0 + j) * kTile + tok) < t_end;
+#pragma unroll
+                    for (int e0 = 0; e0 < CPT; e0 += CH) {
+                        float y[CH];
+                        tmem_ld_f<CH>(tS + j * W + lane_off + colb + e0, y);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < CH; ++e)
+                            if (valid) cmax[e0 + e] = fmaxf(cmax[e0 + e], y[e] * sCf[colb + e0 + e]);
+                    }
+                }
+#pragma unroll
+                for (int e = 0; e < CPT; ++e) {
+                    const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(cmax[e])));
+                    if (lane == (e & 31)) colmax[q * W + colb + e] = mx;
+                }
+            }
+            ptx::bar_sync(kBarWork, kWorkers);  // colmax complete
+            constexpr int RS = CPT < 8 ? CPT : 8;  // columns per O^T rescale access
+#pragma unroll
+            for (int e0 = 0; e0 < CPT; e0 += RS) {
+                float alpha[RS];
+                bool any = false;
+#pragma unroll
+                for (int e = 0; e < RS; ++e) {
+                    const int col = colb + e0 + e;
+                    const float mn = fmaxf(mrun[e0 + e], fmaxf(fmaxf(colmax[col], colmax[W + col]),
+                                                               fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
+                    alpha[e] = (mrun[e0 + e] == -CUDART_INF_F) ? 0.f : ptx::ex2(mrun[e0 + e] - mn);
+                    any |= alpha[e] != 1.f;
+                    lp[e0 + e] *= alpha[e];
+                    mrun[e0 + e] = mn;
+                }
+                if (k > 0 && has_ch && any) {  // O^T of earlier chunks (their MMAs are done)
+                    uint32_t r[RS];
+                    ptx::tmem_ldn<RS>(tO + lane_off + colb + e0, r);
                     ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < CH; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha[e]);
-                    ptx::tmem_stn<CH>(tO + lane_off + colb + c0, r);
+                    for (int e = 0; e < RS; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha[e]);
+                    ptx::tmem_stn<RS>(tO + lane_off + colb + e0, r);
                 }
             }
-        } else if (designated) {
+
+            // (f) per tile: P'^T = p * n_t / nref as fp16 hi + lo (MN-major, one
+            //     128-byte swizzled row of 64 query rows per token) and the
+            //     row-sum partials of p; then the issuer's P'.V MMAs
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) mnext[colb + j] = mcur[colb + j];
-        }
-        // P'^T = p * n_t / nref as fp16 hi + lo, MN-major (one 128-byte swizzled
-        // row of 64 query rows per token), and the row-sum partials of p
+            for (int j = 0; j < NC; ++j) {
+                if (j >= n) break;
+                const bool valid = (t_begin + (c0 + j) * kTile + tok) < t_end;
+                unsigned char* pj = sP + j * 2 * lay.plo;
 #pragma unroll
-        for (int c0 = 0; c0 < CPT; c0 += CH) {
-            float y[CH];
-            tmem_ld_f<CH>(tS + lane_off + colb + c0, y);
-            ptx::tmem_wait_ld();
-            uint32_t hw[CH / 2], lw[CH / 2];
+                for (int e0 = 0; e0 < CPT; e0 += CH) {
+                    float y[CH];
+                    tmem_ld_f<CH>(tS + j * W + lane_off + colb + e0, y);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < CH; e += 2) {
-                float hi[2], lo[2];
+                    for (int e8 = 0; e8 < CH; e8 += 8) {
+                        constexpr int NW = CH < 8 ? CH / 2 : 4;  // fp16x2 words per store
+                        uint32_t hw[4], lw[4];
 #pragma unroll
-                for (int u = 0; u < 2; ++u) {
-                    const int col = colb + c0 + e + u;
-                    const float mc = slow ? new_max(col) : mcur[col];
-                    const float lg = valid ? y[e + u] * sCf[col] : -CUDART_INF_F;
-                    const float pv = ptx::ex2(lg - mc);  // 0 for invalid tokens
-                    lp[c0 + e + u] += pv;
-                    const float pp = pv * ns;
-                    hi[u] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
-                    lo[u] = pp - hi[u];                                          // exact
+                        for (int e = 0; e < 2 * NW; e += 2) {
+                            float hi[2], lo[2];
+#pragma unroll
+                            for (int u = 0; u < 2; ++u) {
+                                const int ee = e8 + e + u;
+                                const int col = colb + e0 + ee;
+                                const float pv = valid ? ptx::ex2(fmaf(y[ee], sCf[col], -mrun[e0 + ee])) : 0.f;
+                                lp[e0 + ee] += pv;
+                                const float pp = pv * nsj[j];
+                                hi[u] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
+                                lo[u] = pp - hi[u];                                          // exact
+                            }
+                            hw[e / 2] = pack_h2(hi[0], hi[1]);
+                            lw[e / 2] = pack_h2(lo[0], lo[1]);
+                        }
+                        const int col0 = colb + e0 + e8;
+                        const int off = (col0 >> 6) * 16384 + (tok >> 3) * 1024 + (tok & 7) * 128 +
+                                        ((((col0 & 63) >> 3) ^ (tok & 7)) << 4) + (col0 & 7) * 2;
+                        if constexpr (NW == 4) {
+                            *reinterpret_cast<uint4*>(pj + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                            *reinterpret_cast<uint4*>(pj + lay.plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+                        } else {
+                            *reinterpret_cast<uint2*>(pj + off) = make_uint2(hw[0], hw[1]);
+                            *reinterpret_cast<uint2*>(pj + lay.plo + off) = make_uint2(lw[0], lw[1]);
+                        }
+                    }
                 }
-                hw[e / 2] = pack_h2(hi[0], hi[1]);
-                lw[e / 2] = pack_h2(lo[0], lo[1]);
-            }
-            const int col0 = colb + c0;
-            const int off = (col0 >> 6) * 16384 + (tok >> 3) * 1024 + (tok & 7) * 128 +
-                            ((((col0 & 63) >> 3) ^ (tok & 7)) << 4) + (col0 & 7) * 2;
-            if constexpr (CH == 8) {
-                *reinterpret_cast<uint4*>(sP + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                *reinterpret_cast<uint4*>(sP + lay.plo + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            } else if constexpr (CH == 4) {
-                *reinterpret_cast<uint2*>(sP + off) = make_uint2(hw[0], hw[1]);
-                *reinterpret_cast<uint2*>(sP + lay.plo + off) = make_uint2(lw[0], lw[1]);
-            } else {
-                *reinterpret_cast<uint32_t*>(sP + off) = hw[0];
-                *reinterpret_cast<uint32_t*>(sP + lay.plo + off) = lw[0];
+                if (j == 0) ptx::tmem_wait_st();  // V^T and any O^T rescale
+                ptx::fence_proxy_async();
+                warp_arrive(bar_p + 8 * j);
             }
         }
-        ptx::tmem_wait_st();  // K^/V^T(i+1) and any O^T rescale
-        ptx::fence_proxy_async();
-        ptx::tc_fence_before();
-        __syncthreads();  // P'(i), K^/V^T(i+1) ready; the raw stage of tile i is consumed
-        if (tid == 0) {
-            ptx::tc_fence_after();
-            // O^T += V^T (P'_hi + P'_lo)^T
+        wwait(bar_o, (nchunk - 1) & 1);
+        ptx::bar_sync(kBarWork, kWorkers);
+        ptx::tc_fence_after();
+        if (q == 0 && lane == 0) {  // final row maxima for the merge
 #pragma unroll
-            for (int ks = 0; ks < kTile / 16; ++ks) {
-                const uint64_t bh = ptx::sdesc(aP + ks * 2048, 16384, 1024);
-                const uint64_t bl = ptx::sdesc(aP + lay.plo + ks * 2048, 16384, 1024);
-                ptx::mma_f16_ta(tO, tV + 128 * b + ks * 8, bh, idesc2, (i > 0 || ks > 0) ? 1u : 0u);
-                ptx::mma_f16_ta(tO, tV + 128 * b + ks * 8, bl, idesc2, 1u);
-            }
-            ptx::mma_commit(bar_o);
-            if (i + 1 < ntile) mma1(b ^ 1);
-            if (i + p.nstage < ntile) issue_tile(i + p.nstage);
+            for (int j = 0; j < CPT; ++j) sMx[colb + j] = mrun[j];
         }
-    }
-    // the last P.V commit covers every MMA issued; waited for even after a
-    // timeout, so that no MMA is still running when TMEM is released
-    if (tid == 0 && !ptx::mbar_wait(bar_o, (ntile - 1) & 1, kWaitNs)) timed_out = true;
-    if (tid == 0 && timed_out) {
-        // give the copies still in flight a bounded chance to land before the
-        // stages are reused and the CTA exits
-        for (int i = max(0, ntile - p.nstage); i < ntile; ++i)
-            ptx::mbar_wait(bar_full + 8 * (i % p.nstage), (i / p.nstage) & 1, kWaitNs);
     }
 
     // this CTA is done with its stages, Q and P': other CTAs may write merge
@@ -755,34 +818,38 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     ptx::cluster_arrive();
 
     // 4. epilogue: row sums and O^T columns into the staging rows, TMEM released
-    warp_reduce_scatter<CPT>(lp, lane);
-    if (lane % (32 / CPT) == 0) lsum[q * W + cgp * CPT + lane / (32 / CPT)] = lp[0];
     float o[CPT];
-    if (has_ch) {
+    if (worker) {
+        warp_reduce_scatter<CPT>(lp, lane);
+        constexpr int REP = CPT >= 32 ? 1 : 32 / CPT;  // lanes holding the same sum
+        if (lane % REP == 0) lsum[q * W + colb + lane / REP] = lp[0];
+        __syncwarp();
+        if (has_ch) {
 #pragma unroll
-        for (int c0 = 0; c0 < CPT; c0 += CH) {
-            float y[CH];
-            tmem_ld_f<CH>(tO + lane_off + cgp * CPT + c0, y);
-            ptx::tmem_wait_ld();
+            for (int e0 = 0; e0 < CPT; e0 += CH) {
+                float y[CH];
+                tmem_ld_f<CH>(tO + lane_off + colb + e0, y);
+                ptx::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < CH; ++e) o[c0 + e] = y[e];
+                for (int e = 0; e < CH; ++e) o[e0 + e] = y[e];
+            }
         }
     }
     ptx::tc_fence_before();
     __syncthreads();  // every MMA is done: the stage area becomes staging rows
-    if (warp == 0) {
+    if (warp == kIssuer) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kCols);
     }
     if (has_ch) {
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
-            const int r = cgp * CPT + j;
+            const int r = colb + j;
             if (r < nrows) sO[r * ROWF + tok] = o[j];
         }
     }
     if (tid < nrows) {
-        sO[tid * ROWF + D] = sMx[(ntile & 1) * W + tid];
+        sO[tid * ROWF + D] = sMx[tid];
         sO[tid * ROWF + D + 1] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
     }
     if (timed_out) atomicOr(p.status, kStTimeout);
@@ -801,7 +868,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 
     // 6. merge the owned rows once all S copies of each have landed, one warp per row
     if (own_cnt > 0) {
-        const bool bad = tid == 0 && (timed_out || !ptx::mbar_wait(bar_m, 0, kWaitNs));
+        const bool bad = tid == 0 && !ptx::mbar_wait(bar_m, 0, kWaitNs);
         const bool ok = !__syncthreads_or(bad);
         if (bad) atomicOr(p.status, kStTimeout);
         const int G = p.G;
@@ -883,6 +950,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     if (tid < nrows) ptx::bulk_wait_read();  // the staging row may be released
 }
 
+
 template <int D, int W, int BITS>
 void configure() {
     static bool done = false;
@@ -962,6 +1030,8 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk
     prm.tps = per * kTile;
     prm.own = (agents_cta + S - 1) / S * prm.G;
     prm.nstage = std::min(max_ns, per);
+    // tiles per chunk: as many as TMEM holds, all resident in their stages
+    prm.nc = std::min(W <= 64 ? 3 : 2, prm.nstage);
     const Layout lay = make_layout(D, BITS, W, prm.nstage);
     if (staging_bytes(D, W) + (size_t)S * prm.own * (D + 4) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
     const size_t smem = std::max<size_t>(lay.total + 1024, kFloor);

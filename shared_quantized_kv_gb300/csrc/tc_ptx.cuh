@@ -38,14 +38,15 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 // Wait for phase `parity` of the barrier, giving up after ~`limit_ns`
-// nanoseconds. Returns false on timeout (the caller records the error and
+// nanoseconds (the clock is read after every try; a try may suspend the
+// thread for a while). Returns false on timeout (the caller records the error and
 // unwinds); never traps.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 0; it < (1u << 26); ++it) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 255) == 255 && globaltimer() - t0 > limit_ns) return false;
+        if (globaltimer() - t0 > limit_ns) return false;
     }
     return false;
 }
@@ -83,8 +84,11 @@ __device__ __forceinline__ void grid_dep_launch() {
 }
 
 // ------------------------------------------------------------- named barriers
+// Named barrier over `n` threads. The non-aligned form: threads of a warp may
+// arrive separately (callers still reconverge the warp first).
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t n) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+    __syncwarp();
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 // Barrier over `n` threads that also returns the OR of `pred` across them.
 __device__ __forceinline__ bool bar_or(uint32_t id, uint32_t n, bool pred) {
@@ -96,12 +100,17 @@ __device__ __forceinline__ bool bar_or(uint32_t id, uint32_t n, bool pred) {
 }
 
 // ---------------------------------------------------------------- tcgen05
+// Whole-warp operations: the warp is reconverged first, since a lane that
+// arrives late would otherwise issue a second allocation (which waits for
+// columns the first one holds).
 __device__ __forceinline__ void tmem_alloc(uint32_t slot_smem, uint32_t ncols) {
+    __syncwarp();
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  ::"r"(slot_smem), "r"(ncols) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    __syncwarp();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
