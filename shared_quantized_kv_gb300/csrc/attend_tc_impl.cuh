@@ -125,7 +125,7 @@ __host__ __device__ inline Layout make_layout(int D, int bits, int W, int nstage
     L.plo = W <= 64 ? 16384 : 32768;  // per chunk tile: P' hi, then P' lo
     o += chunk_tiles(W) * 2 * L.plo;
     L.misc = o;
-    o += 14 * W * 4;
+    o += 15 * W * 4;
     L.bars = align_up(o, 8);
     o = L.bars + 8 * (nstage + 4 + kMaxChunk) + 8;
     L.total = align_up(o, 1024);
@@ -426,10 +426,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     unsigned char* sP = sm + lay.p;
     float* sO = reinterpret_cast<float*>(sm);                             // epilogue: [W][ROWF]
     float* slots = reinterpret_cast<float*>(sm + staging_bytes(D, W));    // epilogue: [S][own][ROWF]
-    float* sMx = reinterpret_cast<float*>(sm + lay.misc);  // [W] final row maxima (log2 units)
-    float* sCf = sMx + W;                                  // [W] logit factor per row
-    float* lsum = sCf + W;                                 // [4][W] row-sum partials
-    float* colmax = lsum + 4 * W;                          // [4][W]
+    // [2][W] (logit factor, running maximum in log2 units) per row, one copy
+    // per chunk parity: chunk k reads copy k & 1 and writes copy (k + 1) & 1
+    float2* sFM = reinterpret_cast<float2*>(sm + lay.misc);
+    float* lsum = reinterpret_cast<float*>(sFM + 2 * W);   // [4][W] row-sum partials
+    float* colmax = lsum + 4 * W;                          // [4][W] chunk maxima; then alpha per row
     float* tailml = colmax + 4 * W;                        // [W][2]
     uint32_t* sOwn = reinterpret_cast<uint32_t*>(tailml + 2 * W);  // [W] owner << 16 | slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
@@ -491,7 +492,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     }
     if (warp == kIssuer) ptx::tmem_alloc(ptx::smem_u32(tslot), kCols);  // overlaps the Q load
     if (tid < W) {
-        sMx[tid] = -CUDART_INF_F;
+        sFM[tid].y = -CUDART_INF_F;
         const int ar = tid / p.G;  // agent of row tid, relative to the CTA's first agent
         sOwn[tid] = ((uint32_t)(ar % S) << 16) | (uint32_t)((ar / S) * p.G + tid % p.G);
     }
@@ -543,7 +544,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
                 v.w = pack_h2(bf2f(u.w & 0xFFFF) * qmul, bf2f(u.w >> 16) * qmul);
                 *reinterpret_cast<uint4*>(sQ + (c / 8) * (W * 128) + (r / 8) * 1024 + (r % 8) * 128 +
                                           (((c % 8) ^ (r % 8)) * 16)) = v;
-                if (c == 0) sCf[r] = r < nrows ? p.scale_log2 * kscale * ldexpf(1.0f, -qe) : 0.f;
+                if (c == 0) {
+                    const float cf = r < nrows ? p.scale_log2 * kscale * ldexpf(1.0f, -qe) : 0.f;
+                    sFM[r].x = cf;
+                    sFM[W + r].x = cf;
+                }
             }
         }
     }
@@ -570,9 +575,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     const uint32_t tS = tmem + kColS;          // S^T of chunk tile j: W columns at tS + j*W
     const uint32_t tKV = tmem + kColKV;        // K^, then V^T, of chunk tile j: 64 columns at tKV + 64*j
     float lp[CPT];     // worker: row-sum partials of its token
-    float mrun[CPT];   // worker: running row maxima of its columns (the same in every worker)
 #pragma unroll
-    for (int j = 0; j < CPT; ++j) { lp[j] = 0.f; mrun[j] = -CUDART_INF_F; }
+    for (int j = 0; j < CPT; ++j) lp[j] = 0.f;
     const int colb = cgp * CPT;
 
     if (warp == kIssuer) {
@@ -700,46 +704,51 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             }
 
             // (e) exact maxima of the chunk's rows: this thread's token over its
-            //     tiles, then across lanes (redux) and lane quarters (shared memory)
-            {
-                float cmax[CPT];
+            //     tiles, then across lanes (redux) and lane quarters (shared
+            //     memory); thread r < W then raises the running maximum of row r
+            const float2* fmo = sFM + (k & 1) * W;  // before the chunk
+            float2* fmn = sFM + ((k + 1) & 1) * W;  // after it
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) cmax[e] = -CUDART_INF_F;
+            for (int e0 = 0; e0 < CPT; e0 += CH) {
+                float cmax[CH];
+#pragma unroll
+                for (int e = 0; e < CH; ++e) cmax[e] = -CUDART_INF_F;
 #pragma unroll
                 for (int j = 0; j < NC; ++j) {
                     if (j >= n) break;
                     const bool valid = (t_begin + (c0 + j) * kTile + tok) < t_end;
+                    float y[CH];
+                    tmem_ld_f<CH>(tS + j * W + lane_off + colb + e0, y);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-                    for (int e0 = 0; e0 < CPT; e0 += CH) {
-                        float y[CH];
-                        tmem_ld_f<CH>(tS + j * W + lane_off + colb + e0, y);
-                        ptx::tmem_wait_ld();
-#pragma unroll
-                        for (int e = 0; e < CH; ++e)
-                            if (valid) cmax[e0 + e] = fmaxf(cmax[e0 + e], y[e] * sCf[colb + e0 + e]);
-                    }
+                    for (int e = 0; e < CH; ++e)
+                        if (valid) cmax[e] = fmaxf(cmax[e], y[e] * fmo[colb + e0 + e].x);
                 }
 #pragma unroll
-                for (int e = 0; e < CPT; ++e) {
+                for (int e = 0; e < CH; ++e) {
                     const float mx = ord2f(__reduce_max_sync(0xffffffffu, f2ord(cmax[e])));
-                    if (lane == (e & 31)) colmax[q * W + colb + e] = mx;
+                    if (lane == (e & 31)) colmax[q * W + colb + e0 + e] = mx;
                 }
             }
             ptx::bar_sync(kBarWork, kWorkers);  // colmax complete
+            if (tid < W) {
+                const float2 fo = fmo[tid];
+                const float mn = fmaxf(fo.y, fmaxf(fmaxf(colmax[tid], colmax[W + tid]),
+                                                   fmaxf(colmax[2 * W + tid], colmax[3 * W + tid])));
+                fmn[tid] = make_float2(fo.x, mn);
+                colmax[tid] = (fo.y == -CUDART_INF_F) ? 0.f : ptx::ex2(fo.y - mn);  // alpha of row tid
+            }
+            ptx::bar_sync(kBarWork, kWorkers);  // new maxima and alphas published
             constexpr int RS = CPT < 8 ? CPT : 8;  // columns per O^T rescale access
 #pragma unroll
             for (int e0 = 0; e0 < CPT; e0 += RS) {
                 float alpha[RS];
-                bool any = false;
+                bool any = false;  // the same in every lane (the warp's columns)
 #pragma unroll
                 for (int e = 0; e < RS; ++e) {
-                    const int col = colb + e0 + e;
-                    const float mn = fmaxf(mrun[e0 + e], fmaxf(fmaxf(colmax[col], colmax[W + col]),
-                                                               fmaxf(colmax[2 * W + col], colmax[3 * W + col])));
-                    alpha[e] = (mrun[e0 + e] == -CUDART_INF_F) ? 0.f : ptx::ex2(mrun[e0 + e] - mn);
+                    alpha[e] = colmax[colb + e0 + e];
                     any |= alpha[e] != 1.f;
                     lp[e0 + e] *= alpha[e];
-                    mrun[e0 + e] = mn;
                 }
                 if (k > 0 && has_ch && any) {  // O^T of earlier chunks (their MMAs are done)
                     uint32_t r[RS];
@@ -775,7 +784,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
                             for (int u = 0; u < 2; ++u) {
                                 const int ee = e8 + e + u;
                                 const int col = colb + e0 + ee;
-                                const float pv = valid ? ptx::ex2(fmaf(y[ee], sCf[col], -mrun[e0 + ee])) : 0.f;
+                                const float2 fm = fmn[col];
+                                const float pv = valid ? ptx::ex2(fmaf(y[ee], fm.x, -fm.y)) : 0.f;
                                 lp[e0 + ee] += pv;
                                 const float pp = pv * nsj[j];
                                 hi[u] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
@@ -804,10 +814,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
         wwait(bar_o, (nchunk - 1) & 1);
         ptx::bar_sync(kBarWork, kWorkers);
         ptx::tc_fence_after();
-        if (q == 0 && lane == 0) {  // final row maxima for the merge
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) sMx[colb + j] = mrun[j];
-        }
     }
 
     // this CTA is done with its stages, Q and P': other CTAs may write merge
@@ -849,7 +855,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
         }
     }
     if (tid < nrows) {
-        sO[tid * ROWF + D] = sMx[tid];
+        sO[tid * ROWF + D] = sFM[(nchunk & 1) * W + tid].y;  // final row maximum
         sO[tid * ROWF + D + 1] = lsum[tid] + lsum[W + tid] + lsum[2 * W + tid] + lsum[3 * W + tid];
     }
     if (timed_out) atomicOr(p.status, kStTimeout);
