@@ -7,36 +7,46 @@
 //      for N(0,1) per rotated coordinate (3 bits; 2 or 4 bits per layer in the
 //      CoMixKV article's mixed-precision setting).
 //
-// Two kernels:
-//   encode_v_kmax: D/32 threads per head-vector, 32 coordinates each, loaded
-//     straight from global memory with coalesced 16-byte loads; grid (token
-//     chunks, kv heads). On the way it reduces max|K| over the same
-//     coordinates of K and the largest norm of the layer (per CTA, then one
-//     atomicMax per CTA only while the CTA's value is still larger).
-//     Per vector: the norm by the pairwise tree (the first levels cross
-//     threads by shuffles), the FWHT (stages h < 32 in registers, h = 32, 64
-//     by shfl.xor), one float32 threshold per midpoint (m_j * n), the codes by
-//     a branchless binary search over the sorted thresholds. The codes are
-//     then regrouped through shared memory into the pool layout: per group of
-//     32 tokens, one packed sequence per coordinate (the 32 tokens' codes in
-//     token order, 4*BITS bytes), so that a reader holding one coordinate of
-//     many tokens finds them in consecutive bytes.
-//   encode_k_pack: s = max|K| / 127, q = clamp(rint(k / s), -127, 127), 16
-//     elements per thread. k / s is formed as k * (1/s) and the correctly
-//     rounded quotient is recomputed with an IEEE division only when the
-//     product lies within 2^-15 of a half-integer, where the two could round
-//     to different integers; elsewhere both give the same q.
+// One cooperative kernel per layer; every CTA is resident at once. An item is
+// 32 (head_dim 128) or 64 (head_dim 64) consecutive tokens of one KV head:
+// 8 KB of K and 8 KB of V, brought into shared memory by bulk copies (one
+// mbarrier per tile). CTA i takes items i, i + G, ... (G = grid size); all
+// copies of the first item are requested at launch.
+//   phase A: max|K| over the CTA's items (the first from its tile, the
+//     others straight from global memory), one atomic per CTA into the
+//     launch's word, then a grid barrier: a 64-bit counter that only grows
+//     (launch g waits for (g + 1) * G arrivals; launch g raises kmax[g & 1]
+//     and clears the other word for launch g + 1), so nothing is
+//     reset between launches. The barrier comes early, while the CTAs are
+//     still nearly in step.
+//   phase B, per item: s = max|K| / 127, q = clamp(rint(k / s), -127, 127)
+//     from the K tile: k / s is formed as k * (1/s) and rounded by the
+//     1.5 * 2^23 addition; where the product lies within 2^-15 of a
+//     half-integer (the two could round to different integers) the chunk's
+//     8 elements are recomputed with IEEE divisions. Then per head-vector,
+//     D/32 threads with 32 coordinates each: the norm by the pairwise tree
+//     (the first levels cross threads by shuffles), the FWHT (stages h < 32
+//     in registers, h = 32, 64 by shfl.xor and one exact FMA), one float32
+//     threshold per midpoint (m_j * n), the codes by a branchless binary
+//     search over the sorted thresholds, regrouped through shared memory
+//     into the pool layout: per group of 32 tokens, one packed sequence per
+//     coordinate (the 32 tokens' codes in token order, 4*BITS bytes). The
+//     next item's copies are requested as soon as the tiles are in registers.
 // Every float operation that decides a code uses an explicit IEEE round-to-
 // nearest intrinsic, in the fixed order of the definition, so the codes are
 // reproducible bit for bit (no contraction into FMA, no approximate division).
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "kvpool_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace kvp {
 namespace {
 
-constexpr int kEncThreads = 256;
+constexpr int kEncThreads = 128;
+constexpr uint64_t kEncWaitNs = 200ull * 1000 * 1000;  // bounded waits: copies, grid barrier
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -69,211 +79,328 @@ __device__ __forceinline__ uint32_t bucket(float x, const float (&t)[16]) {
     }
 }
 
-// Raise *word to the maximum of `val` over the CTA: warp redux, then one
-// thread per CTA, and an atomic only when the word is still smaller (the
-// maximum stabilises after a few CTAs, so almost all CTAs skip the atomic).
-__device__ __forceinline__ void cta_max_to(uint32_t val, uint32_t* word, uint32_t* red) {
-    val = __reduce_max_sync(0xffffffffu, val);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = val;
+// int8 codes of 8 bf16 values (one 16-byte chunk) as two little-endian words
+__device__ __forceinline__ uint2 quant8(uint4 u, float s, float r) {
+    constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds |y| < 2^22 to an integer
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    uint32_t b[8];
+    bool amb = false;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float k = (j & 1) ? bf_hi(w[j / 2]) : bf_lo(w[j / 2]);
+        // k * (1/s) is within ~1.5 ulp of k / s; unless that lands within
+        // 2^-15 of a half-integer both round to the same integer
+        const float y = __fmul_rn(k, r);
+        const float t = __fadd_rn(y, kMagic);                // kMagic + rint(y), ties to even
+        const float e = __fsub_rn(y, __fsub_rn(t, kMagic));  // y - rint(y), exact
+        amb |= !(fabsf(e) < 0.499969482421875f);             // 0.5 - 2^-15 (also taken for NaN)
+        b[j] = __float_as_uint(t);                           // low byte: rint(y) mod 256
+    }
+    if (amb) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float k = (j & 1) ? bf_hi(w[j / 2]) : bf_lo(w[j / 2]);
+            const int q = max(-127, min(127, __float2int_rn(__fdiv_rn(k, s))));
+            b[j] = (uint32_t)q;
+        }
+    }
+    const uint32_t lo = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+    const uint32_t hi = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+    return make_uint2(lo, hi);
+}
+
+// |bf16| bit patterns order like their values, and Inf/NaN patterns exceed
+// every finite one, so a non-finite K survives the maximum.
+__device__ __forceinline__ uint32_t absmax8(uint4 u) {
+    const uint32_t m = 0x7FFF7FFFu;
+    const uint32_t a = __vmaxu2(__vmaxu2(u.x & m, u.y & m), __vmaxu2(u.z & m, u.w & m));
+    return max(a & 0xFFFFu, a >> 16);
+}
+
+// max|K| of one layer: CTA b reduces the b-th contiguous slice of the K
+// tensor (16-byte chunks) to part[b]. It releases the encode kernel at once.
+__global__ void __launch_bounds__(256)
+kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, uint32_t* __restrict__ part,
+            uint32_t* __restrict__ vnmax) {
+    ptx::grid_dep_launch();
+    __shared__ uint32_t red[8];
+    const long long c0 = (long long)blockIdx.x * per_cta;
+    const long long c1 = min(nchunk, c0 + per_cta);
+    uint32_t m = 0;
+    long long c = c0 + threadIdx.x;
+    for (; c + 3 * 256 < c1; c += 4 * 256) {
+        const uint4 u0 = __ldg(K + c), u1 = __ldg(K + c + 256), u2 = __ldg(K + c + 512), u3 = __ldg(K + c + 768);
+        m = max(m, max(max(absmax8(u0), absmax8(u1)), max(absmax8(u2), absmax8(u3))));
+    }
+    for (; c < c1; c += 256) m = max(m, absmax8(__ldg(K + c)));
+    m = __reduce_max_sync(0xffffffffu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
     __syncthreads();
     if (threadIdx.x == 0) {
-        uint32_t m = 0;
-        for (int w = 0; w < (int)(blockDim.x / 32); ++w) m = max(m, red[w]);
-        if (m > *reinterpret_cast<volatile uint32_t*>(word)) atomicMax(word, m);
+#pragma unroll
+        for (int w = 1; w < 8; ++w) m = max(m, red[w]);
+        part[blockIdx.x] = m;
+        if (blockIdx.x == 0) *vnmax = 0;  // raised by the encode kernel after its dependency wait
     }
 }
 
-// grid: (token chunks, kv heads)
 template <int D, int BITS>
 __global__ void __launch_bounds__(kEncThreads)
-encode_v_kmax_kernel(const uint4* __restrict__ K, const uint4* __restrict__ V, int ctx, int ctx_pad,
-                     uint8_t* __restrict__ vcodes, float* __restrict__ vnorm,
-                     uint32_t* __restrict__ scratch, int* __restrict__ status, Codebook cb) {
-    constexpr int TPV = D / 32;          // threads per head-vector
+encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int ctx, int ctx_pad,
+              int items_per_head, int items, int8_t* __restrict__ kq, uint8_t* __restrict__ vcodes,
+              float* __restrict__ vnorm, float* __restrict__ kscale, uint32_t* __restrict__ maxima,
+              const uint32_t* __restrict__ kpart, int nparts, int* __restrict__ status, Codebook cb) {
+    constexpr int TPV = D / 32;              // threads per head-vector
+    constexpr int VPI = kEncThreads / TPV;   // tokens per item (a multiple of 32)
+    constexpr uint32_t kTile = VPI * D * 2;  // bytes of K (and of V) per item: 8 KB
+    constexpr int kChunks = (int)(kTile / 16 / kEncThreads);  // 16-byte chunks per thread and tile
     constexpr int L = 1 << BITS;
-    __shared__ uint32_t red[2][kEncThreads / 32];
-    constexpr int VPB = kEncThreads / TPV;  // head-vectors per block (a multiple of 32)
-    __shared__ __align__(16) uint8_t codes8[VPB * D];
+    __shared__ __align__(128) unsigned char sK[kTile];
+    __shared__ __align__(128) unsigned char sV[kTile];
+    __shared__ __align__(16) uint8_t codes8[VPI * D];
+    __shared__ uint32_t red[kEncThreads / 32];
+    __shared__ __align__(8) uint64_t bars[2];  // K tile, V tile
+    __shared__ uint32_t sDep[kEncThreads];
     const int tid = threadIdx.x, lane = tid % 32;
-    const int lt = tid % TPV;            // this thread's 32-coordinate slice
-    const int t = blockIdx.x * (kEncThreads / TPV) + tid / TPV;  // token
-    const bool live = t < ctx;
-    const long long v = (long long)blockIdx.y * ctx + t;         // input head-vector
+    const int lt = tid % TPV;  // this thread's 32-coordinate slice
+    const int tl = tid / TPV;  // its token within the item
+    const int G = (int)gridDim.x;
     const unsigned gmask = 0xffffffffu;
+    const uint32_t barK = ptx::smem_u32(&bars[0]), barV = ptx::smem_u32(&bars[1]);
 
-    // 1. load 32 coordinates of V and K
-    uint4 vv[4], kk[4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        vv[c] = live ? __ldg(V + v * (D / 8) + lt * 4 + c) : make_uint4(0, 0, 0, 0);
-        kk[c] = live ? __ldg(K + v * (D / 8) + lt * 4 + c) : make_uint4(0, 0, 0, 0);
-    }
-    uint32_t kmax = 0;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t m = 0x7FFF7FFFu;
-        const uint32_t a = __vmaxu2(__vmaxu2(kk[c].x & m, kk[c].y & m), __vmaxu2(kk[c].z & m, kk[c].w & m));
-        kmax = max(kmax, max(a & 0xFFFFu, a >> 16));
-    }
-    // |bf16| bit patterns order like their values; Inf/NaN patterns exceed
-    // every finite one, so a non-finite K survives the maximum.
-    cta_max_to(kmax, &scratch[0], red[0]);
-
-    float x[32];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        const uint32_t w[4] = {vv[c].x, vv[c].y, vv[c].z, vv[c].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            x[c * 8 + 2 * j] = bf_lo(w[j]);
-            x[c * 8 + 2 * j + 1] = bf_hi(w[j]);
-        }
-    }
-
-    // 2. norm: pairwise tree sq_i += sq_{i+w}, w = D/2, ..., 1 (squares exact)
-    float s[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) s[i] = __fmul_rn(x[i], x[i]);
-    // levels w >= 32 pair slices lt and lt + w/32 (the lower slice keeps the sum)
-#pragma unroll
-    for (int w = D / 2; w >= 32; w >>= 1) {
-        const int off = w / 32;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float o = __shfl_down_sync(gmask, s[i], off, TPV);
-            s[i] = __fadd_rn(s[i], o);  // meaningful on slices lt < off
-        }
-    }
-#pragma unroll
-    for (int w = 16; w >= 1; w >>= 1) {
-#pragma unroll
-        for (int i = 0; i < w; ++i) s[i] = __fadd_rn(s[i], s[i + w]);
-    }
-    const float n = __shfl_sync(gmask, __fsqrt_rn(s[0]), lane - lt);  // slice 0 holds the sum
-    cta_max_to(__float_as_uint(n), &scratch[1], red[1]);  // largest norm of the layer
-
-    // 3. FWHT, stages h = 1, 2, ..., D/2, lower index first
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (!(i & h)) {
-                const float a = x[i], b = x[i + h];
-                x[i] = __fadd_rn(a, b);
-                x[i + h] = __fsub_rn(a, b);
-            }
-        }
-    }
-#pragma unroll
-    for (int h = 32; h < D; h <<= 1) {
-        const int off = h / 32;
-        const bool upper = (lt & off) != 0;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
-            // lower slice: own + partner; upper slice: partner (lower) - own
-            x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
-        }
-    }
-
-    // 4. thresholds m_j * n, 5. codes = number of thresholds exceeded (0 past the context)
-    float tau[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) tau[j] = (j < L - 1) ? __fmul_rn(cb.m[j], n) : 0.f;
-    uint32_t cw[8];
-#pragma unroll
-    for (int w = 0; w < 8; ++w) cw[w] = 0;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const uint32_t code = live ? bucket<L>(x[i], tau) : 0u;
-        cw[i / 4] |= code << (8 * (i % 4));
-    }
-    // this slice's codes as bytes [token][coordinate] in shared memory
-    uint4* c8 = reinterpret_cast<uint4*>(codes8 + (tid / TPV) * D + lt * 32);
-    c8[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-    c8[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-    if (live && lt == 0) {
-        vnorm[(long long)blockIdx.y * ctx_pad + t] = n;
-        if (!isfinite(n)) atomicOr(status, kStNonfinite);
+    auto item_h = [&](int it) { return it / items_per_head; };
+    auto item_t0 = [&](int it) { return (it % items_per_head) * VPI; };
+    // K and V are inputs of the launch, written by no kernel that may still
+    // run (the max|K| kernel before this one only reads K): the copies start
+    // before the dependency wait
+    auto issue = [&](int it) {
+        const int t0 = item_t0(it);
+        const uint32_t bytes = (uint32_t)min(VPI, ctx - t0) * D * 2;
+        const long long src = ((long long)item_h(it) * ctx + t0) * D;
+        ptx::mbar_expect_tx(barV, bytes);
+        ptx::bulk_g2s(ptx::smem_u32(sV), V + src, bytes, barV);
+        ptx::mbar_expect_tx(barK, bytes);
+        ptx::bulk_g2s(ptx::smem_u32(sK), K + src, bytes, barK);
+    };
+    if (tid == 0) {
+        ptx::mbar_init(barK, 1);
+        ptx::mbar_init(barV, 1);
+        ptx::mbar_init_fence();
+        issue(blockIdx.x);
     }
     __syncthreads();
 
-    // 6. pool layout: one thread per (32-token group of this block, coordinate)
-    //    packs the group's 32 codes of that coordinate, in token order
-    {
-        const int gq = tid / D, c = tid % D;
-        uint32_t words[BITS + 1];
+    bool ok = true, have_s = false;
+    float s = 1.0f, r = 1.0f;
+    uint32_t nmax = 0;
+    uint32_t phase = 0;
+    for (int it = blockIdx.x; it < items; it += G) {
+        const int h = item_h(it), t0 = item_t0(it);
+        const int ntok = min(VPI, ctx - t0);
+        if (!have_s) {
+            // s = max|K| / 127 (1 when K is all zero) from the partial maxima
+            // of the max|K| kernel, complete once the dependency wait returns
+            ptx::grid_dep_wait();
+            uint32_t m = 0;
+            for (int i = tid; i < nparts; i += kEncThreads) m = max(m, kpart[i]);
+            m = __reduce_max_sync(gmask, m);
+            if (lane == 0) red[tid / 32] = m;
+            __syncthreads();
 #pragma unroll
-        for (int w = 0; w <= BITS; ++w) words[w] = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const uint32_t code = codes8[(gq * 32 + j) * D + c];
-            const int bit = j * BITS, w = bit / 32, off = bit % 32;
-            words[w] |= code << off;
-            if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
+            for (int w = 0; w < kEncThreads / 32; ++w) m = max(m, red[w]);
+            s = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
+            r = __frcp_rn(s);
+            have_s = true;
+            if (blockIdx.x == 0 && tid == 0) {
+                *kscale = s;
+                maxima[0] = m;
+                if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
+            }
         }
-        const long long grp = ((long long)blockIdx.y * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
-        uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+        uint32_t dep = 0;  // depends on every word this thread reads from the tiles
+        // K: q = clamp(rint(k / s), -127, 127), 8 elements per 16-byte chunk
+        if (ok && !ptx::mbar_wait(barK, phase, kEncWaitNs)) ok = false;
 #pragma unroll
-        for (int w = 0; w < BITS; ++w) out[w] = words[w];
-    }
-}
+        for (int c = 0; c < kChunks; ++c) {
+            const int idx = tid + c * kEncThreads;
+            const int row = idx / (D / 8);
+            if (row < ntok) {
+                const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
+                const uint2 q = quant8(u, s, r);
+                dep ^= q.x;
+                *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t0 + row) * D + (idx % (D / 8)) * 8) = q;
+            }
+        }
+        if (ok && !ptx::mbar_wait(barV, phase, kEncWaitNs)) ok = false;
+        const bool live = tl < ntok;
+        float x[32];
+        {
+            const uint4* vs = reinterpret_cast<const uint4*>(sV + tl * (D * 2) + lt * 64);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const uint4 vv = vs[c];
+                dep ^= vv.x ^ vv.y ^ vv.z ^ vv.w;
+                const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    x[c * 8 + 2 * j] = bf_lo(w[j]);
+                    x[c * 8 + 2 * j + 1] = bf_hi(w[j]);
+                }
+            }
+        }
+        phase ^= 1;
+        // The next item's bulk copies overwrite both tiles. A barrier does not
+        // wait for shared-memory loads still in flight, and the copies write
+        // through the async proxy: every thread first stores a word that
+        // depends on all its loads (so they have returned), and the issuing
+        // thread fences the proxies before the copies.
+        sDep[tid] = dep;
+        __syncthreads();
+        if (tid == 0 && ok && it + G < items) {
+            ptx::fence_proxy_async();
+            issue(it + G);
+        }
 
-// grid: (chunks of 16-element groups, kv heads)
-template <int D>
-__global__ void __launch_bounds__(256)
-encode_k_pack_kernel(const uint4* __restrict__ K, int ctx, int ctx_pad, int8_t* __restrict__ kq,
-                     const uint32_t* __restrict__ kabsmax, float* __restrict__ kscale,
-                     int* __restrict__ status) {
-    const uint32_t am = *kabsmax;
-    const float s = (am == 0) ? 1.0f : __fdiv_rn(__uint_as_float(am << 16), 127.0f);
-    const float r = __frcp_rn(s);
-    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-        *kscale = s;
-        if (am >= 0x7F80u) atomicOr(status, kStNonfinite);
-    }
-    const int g = blockIdx.x * blockDim.x + threadIdx.x;  // 16-element group within the head
-    if (g < ctx * (D / 16)) {
-        const long long src = (long long)blockIdx.y * ctx * (D / 8) + 2LL * g;
-        const uint4 a = __ldg(K + src), b = __ldg(K + src + 1);
-        const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-        uint32_t o[4] = {0, 0, 0, 0};
+        // norm: pairwise tree sq_i += sq_{i+w}, w = D/2, ..., 1 (squares exact)
+        float sq[32];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float k = (j & 1) ? bf_hi(w[j / 2]) : bf_lo(w[j / 2]);
-            // k * (1/s) is within ~1.5 ulp of k / s; unless that lands within
-            // 2^-15 of a half-integer both round to the same integer
-            float y = __fmul_rn(k, r);
-            const float fr = y - floorf(y);
-            // (also taken when 1/s overflowed and y is not finite)
-            if (!(fabsf(fr - 0.5f) > 3.0517578125e-05f)) y = __fdiv_rn(k, s);
-            int q = __float2int_rn(y);  // ties to even
-            q = max(-127, min(127, q));
-            o[j / 4] |= (uint32_t)(q & 0xFF) << (8 * (j % 4));
+        for (int i = 0; i < 32; ++i) sq[i] = __fmul_rn(x[i], x[i]);
+        // levels w >= 32 pair slices lt and lt + w/32 (the lower slice keeps the sum)
+#pragma unroll
+        for (int w = D / 2; w >= 32; w >>= 1) {
+            const int off = w / 32;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float o = __shfl_down_sync(gmask, sq[i], off, TPV);
+                sq[i] = __fadd_rn(sq[i], o);  // meaningful on slices lt < off
+            }
         }
-        const int t = g / (D / 16), c = g % (D / 16);
-        *reinterpret_cast<uint4*>(kq + ((long long)blockIdx.y * ctx_pad + t) * D + c * 16) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+        for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+            for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
+        }
+        const float n = __shfl_sync(gmask, __fsqrt_rn(sq[0]), lane - lt);  // slice 0 holds the sum
+        if (live) nmax = max(nmax, __float_as_uint(n));
+
+        // FWHT, stages h = 1, 2, ..., D/2, lower index first
+#pragma unroll
+        for (int hh = 1; hh < 32; hh <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                if (!(i & hh)) {
+                    const float a = x[i], b = x[i + hh];
+                    x[i] = __fadd_rn(a, b);
+                    x[i + hh] = __fsub_rn(a, b);
+                }
+            }
+        }
+#pragma unroll
+        for (int hh = 32; hh < D; hh <<= 1) {
+            const int off = hh / 32;
+            // lower slice: own + partner; upper slice: partner - own (one
+            // rounding either way, exactly the add or the subtraction)
+            const float sg = (lt & off) ? -1.0f : 1.0f;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
+                x[i] = __fmaf_rn(sg, x[i], o);
+            }
+        }
+
+        // thresholds m_j * n; codes = number of thresholds exceeded (0 past the context)
+        float tau[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) tau[j] = (j < L - 1) ? __fmul_rn(cb.m[j], n) : 0.f;
+        uint32_t cw[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) cw[w] = 0;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const uint32_t code = live ? bucket<L>(x[i], tau) : 0u;
+            cw[i / 4] |= code << (8 * (i % 4));
+        }
+        uint4* c8 = reinterpret_cast<uint4*>(codes8 + tl * D + lt * 32);
+        c8[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+        c8[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        if (live && lt == 0) vnorm[(long long)h * ctx_pad + t0 + tl] = n;
+        __syncthreads();
+
+        // pool layout: one thread per (32-token group of the item, coordinate)
+        {
+            const int gq = tid / D, c = tid % D;
+            uint32_t words[BITS + 1];
+#pragma unroll
+            for (int w = 0; w <= BITS; ++w) words[w] = 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t code = codes8[(gq * 32 + j) * D + c];
+                const int bit = j * BITS, w = bit / 32, off = bit % 32;
+                words[w] |= code << off;
+                if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
+            }
+            const long long grp = ((long long)h * ctx_pad + t0) / 32 + gq;
+            uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+#pragma unroll
+            for (int w = 0; w < BITS; ++w) out[w] = words[w];
+        }
+        // the next iteration writes codes8 only after its own barrier
+    }
+
+    // the largest V norm of the layer (zeroed by the max|K| kernel, which
+    // completed before the dependency wait above)
+    nmax = __reduce_max_sync(gmask, nmax);
+    __syncthreads();  // red[] is free again
+    if (lane == 0) red[tid / 32] = nmax;
+    __syncthreads();
+    if (tid == 0) {
+        uint32_t nm = 0;
+#pragma unroll
+        for (int w = 0; w < kEncThreads / 32; ++w) nm = max(nm, red[w]);
+        if (nm > *reinterpret_cast<volatile uint32_t*>(&maxima[1])) atomicMax(&maxima[1], nm);
+        if (nm >= 0x7F800000u) atomicOr(status, kStNonfinite);
+        if (!ok) atomicOr(status, kStTimeout);
     }
 }
 
 template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V, int* status,
-                cudaStream_t st) {
-    // the layer's two scratch words {max|K| bits, largest norm bits} are adjacent
-    cudaError_t e = cudaMemsetAsync(L.kabsmax, 0, 2 * sizeof(uint32_t), st);
+                int sm_count, cudaStream_t st) {
+    constexpr int VPI = kEncThreads / (D / 32);
+    static int per_sm = -1;
+    if (per_sm < 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<D, BITS>,
+                                                                      kEncThreads, 0);
+        if (e != cudaSuccess || per_sm < 1) {
+            per_sm = -1;
+            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
+        }
+    }
+    // max|K|: about two CTAs per SM, contiguous slices of whole 16-byte chunks
+    const long long nchunk = (long long)s.kv_heads * s.ctx * (D / 8);
+    const int ga = (int)std::min<long long>({(long long)kKmaxParts, 2LL * sm_count, (nchunk + 1023) / 1024});
+    const long long per_cta = (nchunk + ga - 1) / ga;
+    kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    constexpr int VPB = kEncThreads / (D / 32);
-    const dim3 grid_v((s.ctx + VPB - 1) / VPB, s.kv_heads);
-    encode_v_kmax_kernel<D, BITS><<<grid_v, kEncThreads, 0, st>>>(
-        (const uint4*)K, (const uint4*)V, s.ctx, s.ctx_pad, L.vcodes, L.vnorm, L.kabsmax, status,
-        codebook(BITS));
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    const dim3 grid_k((s.ctx * (D / 16) + 255) / 256, s.kv_heads);
-    encode_k_pack_kernel<D><<<grid_k, 256, 0, st>>>((const uint4*)K, s.ctx, s.ctx_pad, L.kq, L.kabsmax,
-                                                     L.kscale, status);
-    return cudaGetLastError();
+    // encode: starts while the max|K| kernel runs (programmatic dependent
+    // launch); waits for it only before its first K codes
+    const int items_per_head = (s.ctx + VPI - 1) / VPI;
+    const int items = s.kv_heads * items_per_head;
+    const int G = std::min(items, per_sm * sm_count);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(G, 1, 1);
+    cfg.blockDim = dim3(kEncThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, encode_kernel<D, BITS>, (const uint16_t*)K, (const uint16_t*)V, s.ctx,
+                              s.ctx_pad, items_per_head, items, L.kq, L.vcodes, L.vnorm, L.kscale, L.kabsmax,
+                              (const uint32_t*)L.kpart, ga, status, codebook(BITS));
 }
 
 __global__ void __launch_bounds__(256)
@@ -300,15 +427,15 @@ cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st)
 }
 
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, cudaStream_t st) {
+                          int* status, int sm_count, cudaStream_t st) {
     if (s.head_dim == 64) {
-        if (L.bits == 2) return run<64, 2>(s, L, K, V, status, st);
-        if (L.bits == 3) return run<64, 3>(s, L, K, V, status, st);
-        return run<64, 4>(s, L, K, V, status, st);
+        if (L.bits == 2) return run<64, 2>(s, L, K, V, status, sm_count, st);
+        if (L.bits == 3) return run<64, 3>(s, L, K, V, status, sm_count, st);
+        return run<64, 4>(s, L, K, V, status, sm_count, st);
     }
-    if (L.bits == 2) return run<128, 2>(s, L, K, V, status, st);
-    if (L.bits == 3) return run<128, 3>(s, L, K, V, status, st);
-    return run<128, 4>(s, L, K, V, status, st);
+    if (L.bits == 2) return run<128, 2>(s, L, K, V, status, sm_count, st);
+    if (L.bits == 3) return run<128, 3>(s, L, K, V, status, sm_count, st);
+    return run<128, 4>(s, L, K, V, status, sm_count, st);
 }
 
 }  // namespace kvp

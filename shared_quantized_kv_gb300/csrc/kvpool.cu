@@ -6,8 +6,9 @@
 //   per layer l:  kq     int8  [Hk][ctx_pad][D]
 //                 vcodes uint8 [Hk][ctx_pad/32][D][4*bits_l] (32-token groups)
 //                 vnorm  f32   [Hk][ctx_pad]
-//   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits (encode
-//   scratch), largest V norm float bits}, status int32.
+//   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits, largest
+//   V norm float bits}, per layer 512 partial maxima of max|K| (compress
+//   scratch), status int32.
 // Attention needs no scratch: the CTAs of a cluster merge their context
 // splits through distributed shared memory. Each layer also has a TMA tensor
 // map of its kq (rows of head_dim bytes) for the attention kernel.
@@ -152,13 +153,14 @@ struct kvpool {
     size_t bytes = 0;
     float* kscale = nullptr;
     uint32_t* kabsmax = nullptr;
+    uint32_t* kpart = nullptr;
     int* status = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
                 reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
-                kabsmax + 2 * l + 1, &kmaps[l]};
+                kabsmax + 2 * l + 1, &kmaps[l], kpart + (size_t)l * kvp::kKmaxParts};
     }
 };
 
@@ -278,6 +280,8 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     off = align256(off + 4 * (size_t)layers);
     const size_t off_absmax = off;  // per layer {max|K| bits, largest V norm bits}
     off = align256(off + 8 * (size_t)layers);
+    const size_t off_kpart = off;  // per layer: partial maxima of max|K| (compress scratch)
+    off = align256(off + 4 * (size_t)kvp::kKmaxParts * layers);
     const size_t off_status = off;
     off = align256(off + 4);
     p->bytes = off;
@@ -295,6 +299,7 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     }
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
+    p->kpart = reinterpret_cast<uint32_t*>(p->base + off_kpart);
     p->status = reinterpret_cast<int*>(p->base + off_status);
     p->fresh.assign(layers, 1);
     p->kmaps.resize(layers);
@@ -322,7 +327,7 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
     if (rc) return rc;
     if (!K || !V || !aligned16(K) || !aligned16(V)) return KVPOOL_ERR_INVALID_ARG;
     if (p->compressed[layer]) return KVPOOL_ERR_STATE;
-    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status,
+    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status, p->sm_count,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     p->compressed[layer] = 1;

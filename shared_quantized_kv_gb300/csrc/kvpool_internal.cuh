@@ -31,6 +31,10 @@ struct Codebook {
 // Host: the library's own table for `bits` in {2,3,4} (derived once).
 const Codebook& codebook(int bits);
 
+// Most CTAs of the max|K| kernel that runs ahead of the encode kernel: one
+// partial maximum (bf16 bits of |k|) per CTA, kept per layer.
+constexpr int kKmaxParts = 512;
+
 // Device buffers of one layer.
 struct LayerBufs {
     int8_t* kq;        // [Hk][ctx_pad][D]
@@ -41,6 +45,7 @@ struct LayerBufs {
     int bits;
     uint32_t* vnmax;   // 1 word right after kabsmax: float bits of the largest V norm
     const CUtensorMap* kmap;  // TMA map of kq as rows of D bytes (128 / 64-byte swizzle), or null
+    uint32_t* kpart;          // [kKmaxParts] partial maxima of max|K| (compress scratch)
 };
 
 struct Shape {
@@ -49,7 +54,7 @@ struct Shape {
 
 // ---- encode (write-once compress of one layer)
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, cudaStream_t st);
+                          int* status, int sm_count, cudaStream_t st);
 
 // ---- decompress
 cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out,
