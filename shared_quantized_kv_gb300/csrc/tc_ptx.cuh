@@ -254,10 +254,13 @@ __device__ __forceinline__ void st_dsmem2(uint32_t addr, float a, float b) {
 }
 // Cluster-wide barrier in two halves (every thread of every CTA takes part):
 // writes before arrive are visible to reads after wait.
+// (aligned forms: the warp is reconverged first)
 __device__ __forceinline__ void cluster_arrive() {
+    __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
+    __syncwarp();
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
