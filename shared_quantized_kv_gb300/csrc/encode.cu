@@ -127,12 +127,13 @@ kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, ui
     const long long c0 = (long long)blockIdx.x * per_cta;
     const long long c1 = min(nchunk, c0 + per_cta);
     uint32_t m = 0;
-    long long c = c0 + threadIdx.x;
-    for (; c + 3 * 256 < c1; c += 4 * 256) {
-        const uint4 u0 = __ldg(K + c), u1 = __ldg(K + c + 256), u2 = __ldg(K + c + 512), u3 = __ldg(K + c + 768);
-        m = max(m, max(max(absmax8(u0), absmax8(u1)), max(absmax8(u2), absmax8(u3))));
+    for (long long base = c0 + threadIdx.x; base < c1; base += 8 * 256) {
+        uint4 u[8];  // all of a batch's loads in flight at once
+#pragma unroll
+        for (int j = 0; j < 8; ++j) u[j] = (base + j * 256 < c1) ? __ldg(K + base + j * 256) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = max(m, absmax8(u[j]));
     }
-    for (; c < c1; c += 256) m = max(m, absmax8(__ldg(K + c)));
     m = __reduce_max_sync(0xffffffffu, m);
     if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
     __syncthreads();
@@ -173,20 +174,22 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
     // K and V are inputs of the launch, written by no kernel that may still
     // run (the max|K| kernel before this one only reads K): the copies start
     // before the dependency wait
-    auto issue = [&](int it) {
-        const int t0 = item_t0(it);
-        const uint32_t bytes = (uint32_t)min(VPI, ctx - t0) * D * 2;
-        const long long src = ((long long)item_h(it) * ctx + t0) * D;
-        ptx::mbar_expect_tx(barV, bytes);
-        ptx::bulk_g2s(ptx::smem_u32(sV), V + src, bytes, barV);
-        ptx::mbar_expect_tx(barK, bytes);
-        ptx::bulk_g2s(ptx::smem_u32(sK), K + src, bytes, barK);
+    auto item_bytes = [&](int it) { return (uint32_t)min(VPI, ctx - item_t0(it)) * D * 2; };
+    auto item_src = [&](int it) { return ((long long)item_h(it) * ctx + item_t0(it)) * D; };
+    auto issueV = [&](int it) {
+        ptx::mbar_expect_tx(barV, item_bytes(it));
+        ptx::bulk_g2s(ptx::smem_u32(sV), V + item_src(it), item_bytes(it), barV);
+    };
+    auto issueK = [&](int it) {
+        ptx::mbar_expect_tx(barK, item_bytes(it));
+        ptx::bulk_g2s(ptx::smem_u32(sK), K + item_src(it), item_bytes(it), barK);
     };
     if (tid == 0) {
         ptx::mbar_init(barK, 1);
         ptx::mbar_init(barV, 1);
         ptx::mbar_init_fence();
-        issue(blockIdx.x);
+        issueV(blockIdx.x);
+        issueK(blockIdx.x);
     }
     __syncthreads();
 
@@ -197,44 +200,11 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
     for (int it = blockIdx.x; it < items; it += G) {
         const int h = item_h(it), t0 = item_t0(it);
         const int ntok = min(VPI, ctx - t0);
-        if (!have_s) {
-            // s = max|K| / 127 (1 when K is all zero) from the partial maxima
-            // of the max|K| kernel, complete once the dependency wait returns
-            ptx::grid_dep_wait();
-            uint32_t m = 0;
-            for (int i = tid; i < nparts; i += kEncThreads) m = max(m, kpart[i]);
-            m = __reduce_max_sync(gmask, m);
-            if (lane == 0) red[tid / 32] = m;
-            __syncthreads();
-#pragma unroll
-            for (int w = 0; w < kEncThreads / 32; ++w) m = max(m, red[w]);
-            s = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
-            r = __frcp_rn(s);
-            have_s = true;
-            if (blockIdx.x == 0 && tid == 0) {
-                *kscale = s;
-                maxima[0] = m;
-                if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
-            }
-        }
-        uint32_t dep = 0;  // depends on every word this thread reads from the tiles
-        // K: q = clamp(rint(k / s), -127, 127), 8 elements per 16-byte chunk
-        if (ok && !ptx::mbar_wait(barK, phase, kEncWaitNs)) ok = false;
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) {
-            const int idx = tid + c * kEncThreads;
-            const int row = idx / (D / 8);
-            if (row < ntok) {
-                const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
-                const uint2 q = quant8(u, s, r);
-                dep ^= q.x;
-                *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t0 + row) * D + (idx % (D / 8)) * 8) = q;
-            }
-        }
         if (ok && !ptx::mbar_wait(barV, phase, kEncWaitNs)) ok = false;
         const bool live = tl < ntok;
         float x[32];
         {
+            uint32_t dep = 0;  // depends on every word this thread reads from the V tile
             const uint4* vs = reinterpret_cast<const uint4*>(sV + tl * (D * 2) + lt * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
@@ -247,18 +217,17 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                     x[c * 8 + 2 * j + 1] = bf_hi(w[j]);
                 }
             }
+            // The next item's copy overwrites the tile. A barrier does not
+            // wait for shared-memory loads still in flight, and the copy
+            // writes through the async proxy: every thread first stores a word
+            // that depends on all its loads (so they have returned), and the
+            // issuing thread fences the proxies before the copy.
+            sDep[tid] = dep;
         }
-        phase ^= 1;
-        // The next item's bulk copies overwrite both tiles. A barrier does not
-        // wait for shared-memory loads still in flight, and the copies write
-        // through the async proxy: every thread first stores a word that
-        // depends on all its loads (so they have returned), and the issuing
-        // thread fences the proxies before the copies.
-        sDep[tid] = dep;
         __syncthreads();
         if (tid == 0 && ok && it + G < items) {
             ptx::fence_proxy_async();
-            issue(it + G);
+            issueV(it + G);
         }
 
         // norm: pairwise tree sq_i += sq_{i+w}, w = D/2, ..., 1 (squares exact)
@@ -344,7 +313,51 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
 #pragma unroll
             for (int w = 0; w < BITS; ++w) out[w] = words[w];
         }
-        // the next iteration writes codes8 only after its own barrier
+
+        // K: s = max|K| / 127 (1 when K is all zero) from the partial maxima of
+        // the max|K| kernel, complete once the dependency wait returns (by now
+        // it has long finished: it ran beside the V work above)
+        if (!have_s) {
+            ptx::grid_dep_wait();
+            uint32_t m = 0;
+            for (int i = tid; i < nparts; i += kEncThreads) m = max(m, kpart[i]);
+            m = __reduce_max_sync(gmask, m);
+            if (lane == 0) red[tid / 32] = m;
+            __syncthreads();
+#pragma unroll
+            for (int w = 0; w < kEncThreads / 32; ++w) m = max(m, red[w]);
+            s = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
+            r = __frcp_rn(s);
+            have_s = true;
+            if (blockIdx.x == 0 && tid == 0) {
+                *kscale = s;
+                maxima[0] = m;
+                if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
+            }
+        }
+        // q = clamp(rint(k / s), -127, 127), 8 elements per 16-byte chunk
+        if (ok && !ptx::mbar_wait(barK, phase, kEncWaitNs)) ok = false;
+        phase ^= 1;
+        {
+            uint32_t dep = 0;
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) {
+                const int idx = tid + c * kEncThreads;
+                const int row = idx / (D / 8);
+                if (row < ntok) {
+                    const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
+                    const uint2 q = quant8(u, s, r);
+                    dep ^= q.x;
+                    *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t0 + row) * D + (idx % (D / 8)) * 8) = q;
+                }
+            }
+            sDep[tid] = dep;  // as for the V tile
+        }
+        __syncthreads();  // also: red[] and codes8 are free for the next item
+        if (tid == 0 && ok && it + G < items) {
+            ptx::fence_proxy_async();
+            issueK(it + G);
+        }
     }
 
     // the largest V norm of the layer (zeroed by the max|K| kernel, which
@@ -378,7 +391,8 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     }
     // max|K|: about two CTAs per SM, contiguous slices of whole 16-byte chunks
     const long long nchunk = (long long)s.kv_heads * s.ctx * (D / 8);
-    const int ga = (int)std::min<long long>({(long long)kKmaxParts, 2LL * sm_count, (nchunk + 1023) / 1024});
+    const int ga = (int)std::min<long long>(
+        kKmaxParts, std::max<long long>(2LL * sm_count, (nchunk + 2047) / 2048));  // one batch per thread
     const long long per_cta = (nchunk + ga - 1) / ga;
     kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
     cudaError_t e = cudaGetLastError();
