@@ -11,8 +11,10 @@
 //     [coordinate] in shared memory; then D/32 threads per head-vector, 32
 //     coordinates each, look the centroids up in a shared-memory table, FWHT in
 //     the encoder's stage order (h < 32 in registers, h = 32, 64 by
-//     shfl.xor), V_i = bf16(fl(fl(z_i * n) * (1/d))), coalesced 16-byte stores.
-//   K blocks: K = bf16(fl(q * s)), 16 elements per thread.
+//     shfl.xor and one exact FMA), V_i = bf16(fl(fl(z_i * n) * (1/d))),
+//     coalesced 16-byte stores.
+//   K blocks: K = bf16(fl(q * s)), 16 elements per thread (the int8 to float
+//     conversion by an integer add and one exact subtraction).
 #include <cuda_bf16.h>
 
 #include "kvpool_internal.cuh"
@@ -22,8 +24,15 @@ namespace {
 
 constexpr int kDecThreads = 256;
 
-__device__ __forceinline__ uint32_t bf16_bits(float f) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(f));
+// bf16 bits of (lo, hi), each rounded to nearest even, lo in the low half
+__device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+// the int8 in byte k of w as a float (exact: 1.5 * 2^23 + q has q in its low bits)
+__device__ __forceinline__ float i8_to_f(uint32_t w, int k) {
+    const int q = (int)(int8_t)((w >> (8 * k)) & 0xFF);
+    return __fsub_rn(__int_as_float(0x4B400000 + q), 12582912.0f);
 }
 
 // One launch for both halves, grid (blocks, kv heads): the first nbv blocks of
@@ -50,9 +59,8 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
         uint32_t o[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const int b0 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2))) & 0xFF);
-            const int b1 = (int)(int8_t)((w[j / 2] >> (16 * (j % 2) + 8)) & 0xFF);
-            o[j] = bf16_bits(__fmul_rn((float)b0, s)) | (bf16_bits(__fmul_rn((float)b1, s)) << 16);
+            const float k0 = i8_to_f(w[j / 2], 2 * (j % 2)), k1 = i8_to_f(w[j / 2], 2 * (j % 2) + 1);
+            o[j] = bf16x2_bits(__fmul_rn(k0, s), __fmul_rn(k1, s));
         }
         uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
         out[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -66,6 +74,10 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     __shared__ float cen[16];
     __shared__ __align__(16) uint8_t codes8[VPB * D];
     if (tid < 16) cen[tid] = cb.c[tid];
+    const int lt = tid % TPV;
+    const int t = blockIdx.x * VPB + tid / TPV;
+    const bool live = t < ctx;
+    const float n = live ? __ldg(vnorm + head * ctx_pad + t) : 0.f;  // in flight during the unpacking
     {
         const int gq = tid / D, c = tid % D;
         const long long grp = (head * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
@@ -81,15 +93,10 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
         }
     }
     __syncthreads();
-    const int lt = tid % TPV;
-    const int t = blockIdx.x * VPB + tid / TPV;
-    const bool live = t < ctx;
     const unsigned gmask = 0xffffffffu;
-    const long long src = head * ctx_pad + (live ? t : 0);
     const uint4* c8 = reinterpret_cast<const uint4*>(codes8 + (tid / TPV) * D + lt * 32);
     const uint4 ca = c8[0], cb8 = c8[1];
     const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb8.x, cb8.y, cb8.z, cb8.w};
-    const float n = live ? __ldg(vnorm + src) : 0.f;
     float x[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) x[i] = cen[(cw[i / 4] >> (8 * (i % 4))) & 0xFF];
@@ -107,11 +114,13 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
 #pragma unroll
     for (int h = 32; h < D; h <<= 1) {
         const int off = h / 32;
-        const bool upper = (lt & off) != 0;
+        // lower slice: own + partner; upper slice: partner - own (one
+        // rounding either way, exactly the add or the subtraction)
+        const float sg = (lt & off) ? -1.0f : 1.0f;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
             const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
-            x[i] = upper ? __fsub_rn(o, x[i]) : __fadd_rn(x[i], o);
+            x[i] = __fmaf_rn(sg, x[i], o);
         }
     }
     if (!live) return;
@@ -124,7 +133,7 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
         for (int j = 0; j < 4; ++j) {
             const float lo = __fmul_rn(__fmul_rn(x[8 * q + 2 * j], n), inv_d);
             const float hi = __fmul_rn(__fmul_rn(x[8 * q + 2 * j + 1], n), inv_d);
-            o[j] = bf16_bits(lo) | (bf16_bits(hi) << 16);
+            o[j] = bf16x2_bits(lo, hi);
         }
         out[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }
