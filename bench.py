@@ -287,8 +287,8 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": ph_info[dom]["hbm_frac"],
                      "traffic": _traffic(dom_file), "peak_source": peak_kind,
                      "algo_bytes_per_launch": int(algo[dom])},
-        # per layer: encode (one cooperative kernel), attend_tc, decompress
-        "gpu_launches": args.steps * L * 3,
+        # per layer: kmax + encode (compress), attend_tc, decompress
+        "gpu_launches": args.steps * L * 4,
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
         "e2e": e2e,
