@@ -47,6 +47,20 @@ def _peaks():
     return FALLBACK_HBM, "fallback"
 
 
+def max_over_ranks(step_ms, ph_ms, phases, device=None):
+    """(step time, per-phase times) as the maximum over the ranks of the
+    default process group (unchanged when no group is initialised). Ranks are
+    replicas: the job takes as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return step_ms, dict(ph_ms)
+    t = torch.tensor([step_ms] + [ph_ms[p] for p in phases], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t[0]), {p: float(t[i + 1]) for i, p in enumerate(phases)}
+
+
 def _dist():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -240,12 +254,7 @@ def run_gpu(args):
         for ph, e0, e1 in ev:
             ph_ms[ph] += e0.elapsed_time(e1)
     ph_ms = {ph: v / args.steps for ph, v in ph_ms.items()}
-    step_ms = sum(ph_ms.values())
-    if ws > 1:
-        t = torch.tensor([step_ms] + [ph_ms[p] for p in phases], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        step_ms = float(t[0])
-        ph_ms = {p: float(t[i + 1]) for i, p in enumerate(phases)}
+    step_ms, ph_ms = max_over_ranks(sum(ph_ms.values()), ph_ms, phases, dev if ws > 1 else None)
 
     # algorithmic bytes per layer
     nvec = w.kv_heads * w.ctx

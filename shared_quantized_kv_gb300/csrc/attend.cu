@@ -124,7 +124,7 @@ attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ v
             float dot = 0.f;
 #pragma unroll 16
             for (int i = 0; i < D; ++i) dot = fmaf(Qs[rr][i], Ks[lane][i], dot);
-            const float lg = valid ? dot * lscale : -CUDART_INF_F;
+            const float lg = valid ? __fmul_rn(dot, lscale) : -CUDART_INF_F;  // never fused with - m
             const float mnew = fmaxf(m[r4], warp_max(lg));
             if (mnew == -CUDART_INF_F) continue;  // warp-uniform
             const float corr = exp2f(m[r4] - mnew);
@@ -213,7 +213,7 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
 #pragma unroll
             for (int w = 0; w < D / 32; ++w) dot += red[w];
             __syncthreads();
-            const float lg = dot * scale_log2;
+            const float lg = __fmul_rn(dot, scale_log2);
             const float mnew = fmaxf(mt, lg);
             const float corr = exp2f(mt - mnew), p = exp2f(lg - mnew);
             lt = lt * corr + p;

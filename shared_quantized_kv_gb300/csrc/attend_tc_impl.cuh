@@ -336,7 +336,7 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
                             dot = fmaf(qq[cc + 6], bf2f(u.w & 0xFFFF), dot);
                             dot = fmaf(qq[cc + 7], bf2f(u.w >> 16), dot);
                         }
-                        lg[kk] = dot * p.scale_log2;
+                        lg[kk] = __fmul_rn(dot, p.scale_log2);
                     }
                     if (worker) tl[k * TCH + t] = lg[kk];
                 }
@@ -722,7 +722,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
                     ptx::tmem_wait_ld();
 #pragma unroll
                     for (int e = 0; e < CH; ++e)
-                        if (valid) cmax[e] = fmaxf(cmax[e], y[e] * fmo[colb + e0 + e].x);
+                        if (valid) cmax[e] = fmaxf(cmax[e], __fmul_rn(y[e], fmo[colb + e0 + e].x));
                 }
 #pragma unroll
                 for (int e = 0; e < CH; ++e) {
@@ -785,7 +785,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
                                 const int ee = e8 + e + u;
                                 const int col = colb + e0 + ee;
                                 const float2 fm = fmn[col];
-                                const float pv = valid ? ptx::ex2(fmaf(y[ee], fm.x, -fm.y)) : 0.f;
+                                // the logit rounded exactly as for the row maximum, so that
+                                // it never exceeds the maximum (a fused product would, by up
+                                // to half an ulp of the logit, which is large for huge logits)
+                                const float pv = valid ? ptx::ex2(__fmul_rn(y[ee], fm.x) - fm.y) : 0.f;
                                 lp[e0 + ee] += pv;
                                 const float pp = pv * nsj[j];
                                 hi[u] = __uint_as_float(__float_as_uint(pp) & 0xFFFFE000u);  // 11 significant bits
