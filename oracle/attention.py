@@ -43,7 +43,12 @@ def dequantise_f64(enc: dict):
     cen, _ = lloyd_max.tables_f32(enc["bits"])
     codes = enc["codes"]
     d = codes.shape[-1]
-    K = enc["kq"].astype(np.float64) * float(enc["scale"])
+    if enc.get("k_block"):
+        kb = enc["k_block"]
+        q = enc["kq"].astype(np.float64)
+        K = (q.reshape(q.shape[:-1] + (d // kb, kb)) * enc["kscales"].astype(np.float64)[..., None]).reshape(q.shape)
+    else:
+        K = enc["kq"].astype(np.float64) * float(enc["scale"])
     rot = cen.astype(np.float64)[codes] * enc["norms"].astype(np.float64)[..., None]
     V = rot @ hadamard(d) / d
     return K, V

@@ -133,6 +133,37 @@ def k_dequantize_bf16(q: np.ndarray, scale) -> np.ndarray:
     return f32_to_bf16(q.astype(np.float32) * F32(scale))
 
 
+# Block-scaled K (the "q8_0" reading of the PolyKV summary's section 2.B, a
+# per-pool option): one scale per block of 32 consecutive elements of a
+# head-vector, s_b = max|k| / 127 over the block (float32 division; 1 for an
+# all-zero block), q = clamp(round_half_even(k / s_b), -127, 127) with a
+# float32 division. Scales are kept as float32 (not q8_0's fp16: a bf16 K
+# spans a range that fp16 cannot hold).
+K_BLOCK = 32
+
+
+def k_scales_block(K_bf16) -> np.ndarray:
+    """Scales [..., d / 32] float32 of a K tensor [..., d]."""
+    k = bf16_to_f32(K_bf16)
+    if not np.all(np.isfinite(k)):
+        raise ValueError("K holds a non-finite value")
+    b = k.reshape(k.shape[:-1] + (k.shape[-1] // K_BLOCK, K_BLOCK))
+    absmax = np.max(np.abs(b), axis=-1).astype(np.float32)
+    return np.where(absmax > 0, absmax / F32(127), F32(1)).astype(np.float32)
+
+
+def k_quantize_block(K_bf16, scales) -> np.ndarray:
+    k = bf16_to_f32(K_bf16)
+    b = k.reshape(k.shape[:-1] + (k.shape[-1] // K_BLOCK, K_BLOCK))
+    r = np.rint(b / np.asarray(scales, dtype=np.float32)[..., None])  # float32 division, ties to even
+    return np.clip(r, -127, 127).astype(np.int8).reshape(k.shape)
+
+
+def k_dequantize_block_bf16(q: np.ndarray, scales) -> np.ndarray:
+    b = q.astype(np.float32).reshape(q.shape[:-1] + (q.shape[-1] // K_BLOCK, K_BLOCK))
+    return f32_to_bf16(b * np.asarray(scales, dtype=np.float32)[..., None]).reshape(q.shape)
+
+
 # ---------------------------------------------------------------------- V side
 
 def v_codes(V_bf16, bits: int):
@@ -222,18 +253,28 @@ def v_decompress_bf16(codes: np.ndarray, norms: np.ndarray, bits: int) -> np.nda
 
 # --------------------------------------------------------------------- a layer
 
-def encode_layer(K_bf16, V_bf16, bits: int) -> dict:
-    """Everything the pool stores for one layer."""
-    absmax, scale = k_scale(K_bf16)
-    q = k_quantize(K_bf16, scale)
+def encode_layer(K_bf16, V_bf16, bits: int, k_block: int = 0) -> dict:
+    """Everything the pool stores for one layer. k_block = 32: block-scaled K
+    (per-tensor scale 1, the block scales in "kscales")."""
     codes, norms = v_codes(V_bf16, bits)
-    return dict(bits=bits, absmax=absmax, scale=scale, kq=q, codes=codes,
-                packed=pack_pool_v(codes, bits), norms=norms)
+    enc = dict(bits=bits, codes=codes, packed=pack_pool_v(codes, bits), norms=norms, k_block=k_block)
+    if k_block:
+        if k_block != K_BLOCK:
+            raise ValueError("k_block must be 0 or 32")
+        sc = k_scales_block(K_bf16)
+        enc.update(absmax=F32(0), scale=F32(1), kscales=sc, kq=k_quantize_block(K_bf16, sc))
+    else:
+        absmax, scale = k_scale(K_bf16)
+        enc.update(absmax=absmax, scale=scale, kq=k_quantize(K_bf16, scale))
+    return enc
 
 
 def decompress_layer(enc: dict):
-    return (k_dequantize_bf16(enc["kq"], enc["scale"]),
-            v_decompress_bf16(enc["codes"], enc["norms"], enc["bits"]))
+    if enc.get("k_block"):
+        K = k_dequantize_block_bf16(enc["kq"], enc["kscales"])
+    else:
+        K = k_dequantize_bf16(enc["kq"], enc["scale"])
+    return K, v_decompress_bf16(enc["codes"], enc["norms"], enc["bits"])
 
 
 def layer_bytes(kv_heads: int, ctx: int, head_dim: int, bits: int) -> int:

@@ -374,3 +374,84 @@ def test_encode_nonfinite_v():
     V[0, 0, 3] = 0x7FC0  # NaN
     with pytest.raises(ValueError):
         codec.v_codes(V, 3)
+
+
+# ----------------------------------------------------- block-scaled K (option)
+
+def _rand_k(shape, seed):
+    rng = np.random.default_rng(seed)
+    return codec.f32_to_bf16(rng.standard_normal(shape).astype(np.float32) * np.float32(3))
+
+
+def test_k_block_max_maps_to_127_and_error_bound():
+    K = _rand_k((2, 5, 128), 11)
+    s = codec.k_scales_block(K)
+    q = codec.k_quantize_block(K, s)
+    k = codec.bf16_to_f32(K).reshape(2, 5, 4, 32)
+    qb = q.reshape(2, 5, 4, 32).astype(np.int32)
+    assert s.shape == (2, 5, 4) and s.dtype == np.float32
+    # the largest |k| of every block lands on +-127
+    arg = np.abs(k).argmax(axis=-1)
+    top = np.take_along_axis(qb, arg[..., None], axis=-1)[..., 0]
+    assert np.all(np.abs(top) == 127)
+    # nearest-integer error: |k/s - q| <= 1/2 (+ float32 slack)
+    assert np.all(np.abs(k / s[..., None] - qb) <= 0.5 + 1e-5)
+    assert qb.min() >= -127 and qb.max() <= 127
+
+
+def test_k_block_zero_block_and_ties_to_even():
+    K = np.zeros((1, 1, 64), dtype=np.uint16)
+    vals = np.zeros(32, dtype=np.float32)
+    vals[0] = 127.0  # s = 1 exactly
+    vals[1:6] = [2.5, 3.5, -2.5, -0.5, 0.5]
+    K[0, 0, 32:] = codec.f32_to_bf16(vals)
+    s = codec.k_scales_block(K)
+    q = codec.k_quantize_block(K, s).astype(np.int32)
+    assert s[0, 0, 0] == 1.0 and not q[0, 0, :32].any()  # all-zero block
+    assert s[0, 0, 1] == 1.0
+    assert list(q[0, 0, 32:38]) == [127, 2, 4, -2, 0, 0]
+
+
+def test_k_block_power_of_two_scaling_is_local_to_its_block():
+    K = _rand_k((1, 3, 128), 12)
+    s0 = codec.k_scales_block(K)
+    q0 = codec.k_quantize_block(K, s0)
+    k = codec.bf16_to_f32(K).copy()
+    k[0, 1, 64:96] *= np.float32(2.0 ** 7)  # one block of one token
+    K2 = codec.f32_to_bf16(k)
+    s2 = codec.k_scales_block(K2)
+    q2 = codec.k_quantize_block(K2, s2)
+    assert np.array_equal(q2, q0)  # codes are scale-invariant per block
+    ratio = s2 / s0
+    assert ratio[0, 1, 2] == 2.0 ** 7
+    ratio[0, 1, 2] = 1.0
+    assert np.all(ratio == 1.0)  # no other block (token or coordinate) moved
+
+
+def test_k_block_equals_per_tensor_when_every_block_holds_the_maximum():
+    K = _rand_k((2, 4, 64), 13)
+    k = codec.bf16_to_f32(K).copy()
+    m = np.float32(np.abs(k).max() * 2)
+    k[..., ::32] = m  # the first element of every block is the tensor maximum
+    K2 = codec.f32_to_bf16(k)
+    _, st = codec.k_scale(K2)
+    sb = codec.k_scales_block(K2)
+    assert np.all(sb == st)
+    assert np.array_equal(codec.k_quantize_block(K2, sb), codec.k_quantize(K2, st))
+
+
+def test_k_block_layer_round_trip_and_dequantisation():
+    K = _rand_k((2, 7, 64), 14)
+    V = _rand_k((2, 7, 64), 15)
+    enc = codec.encode_layer(K, V, 3, k_block=32)
+    assert enc["scale"] == 1.0 and enc["kscales"].shape == (2, 7, 2)
+    Kd, _ = codec.decompress_layer(enc)
+    want = codec.f32_to_bf16(enc["kq"].astype(np.float32).reshape(2, 7, 2, 32)
+                             * enc["kscales"][..., None]).reshape(2, 7, 64)
+    assert np.array_equal(Kd, want)
+    # block scales never lose to the per-tensor scale on the same K
+    err_t = np.abs(codec.bf16_to_f32(codec.decompress_layer(codec.encode_layer(K, V, 3))[0]) - codec.bf16_to_f32(K)).max()
+    err_b = np.abs(codec.bf16_to_f32(Kd) - codec.bf16_to_f32(K)).max()
+    assert err_b <= err_t
+    with pytest.raises(ValueError):
+        codec.encode_layer(K, V, 3, k_block=16)
