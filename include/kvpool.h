@@ -88,6 +88,11 @@ typedef struct {
     int ctx_padded;
     int bits;
     int compressed;        /* 1 once kvpool_compress succeeded for the layer   */
+    const float* kscales;  /* block-scaled pools (kvpool_create_ex, k_block 32):
+                              float [kv_heads][ctx_padded][head_dim/32], one
+                              scale per 32 elements (*kscale is then 1); NULL
+                              for per-tensor pools                            */
+    int k_block;           /* 0 (per-tensor scale) or 32                       */
 } kvpool_layer_view_t;
 
 /* Create a pool for `layers` layers of a shared context of `ctx` tokens with
@@ -99,6 +104,31 @@ typedef struct {
  * section 2.A (one shared object, O(1) in the number of agents). */
 int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
                   const uint8_t* bits_per_layer, int max_rows);
+
+/* kvpool_create with a choice of K scaling. k_block = 0 is kvpool_create (one
+ * scale per layer's K tensor). k_block = 32 gives every block of 32
+ * consecutive elements of a K head-vector its own float32 scale: s_b =
+ * max|k| / 127 over the block (float32 division; 1 for an all-zero block),
+ * q = clamp(round-half-even(k / s_b), -127, 127) with a float32 division,
+ * K_hat = q * s_b. This is the "q8_0" reading of the PolyKV summary's section
+ * 2.B (which names both a per-tensor scale and q8_0); the scales are float32,
+ * not q8_0's fp16, because a bf16 K can exceed the fp16 range. The pool then
+ * holds head_dim/32 scales per token and head (kvpool_layer_view_t.kscales).
+ * Attention over such a pool runs on CUDA cores (the split-context kernels)
+ * with a split scratch sized here for max_rows; attend calls on one such
+ * pool share that scratch and must be ordered on one stream by the caller.
+ * kvpool_export_layer exports such a layer with *kscale = 1 and
+ * kvpool_export_kscales copies its block scales; kvpool_import_layer returns
+ * KVPOOL_ERR_UNSUPPORTED for these pools. Other k_block values:
+ * KVPOOL_ERR_INVALID_ARG. */
+int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
+                     const uint8_t* bits_per_layer, int max_rows, int k_block);
+
+/* Copy the block scales of one compressed layer of a block-scaled pool to
+ * `kscales` (host or device), float [kv_heads][ctx][head_dim/32], on
+ * `stream`. KVPOOL_ERR_UNSUPPORTED for per-tensor pools, KVPOOL_ERR_STATE if
+ * the layer is not compressed. */
+int kvpool_export_kscales(const kvpool_t* pool, int layer, float* kscales, void* stream);
 
 /* Free all device memory of the pool. Waits for the device first. NULL is a
  * no-op. */

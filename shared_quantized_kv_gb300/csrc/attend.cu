@@ -48,7 +48,8 @@ __device__ __forceinline__ float warp_sum(float v) {
 template <int D, int BITS>
 __global__ void __launch_bounds__(kWarps * 32)
 attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ vcodes,
-                    const float* __restrict__ vnorm, const float* __restrict__ kscale, int ctx,
+                    const float* __restrict__ vnorm, const float* __restrict__ kscale,
+                    const float* __restrict__ kscales, int ctx,
                     int ctx_pad, const uint16_t* __restrict__ Q, int Hq, int G, int R,
                     float scale_log2, int tok_per_split, float* __restrict__ part_acc,
                     float* __restrict__ part_ml, int nsplit, int max_rows, Codebook cb) {
@@ -91,14 +92,16 @@ attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ v
     __syncthreads();
 
     for (int t0 = t_begin; t0 < t_end; t0 += kTileTok) {
-        // K tile: int8 -> float (the scale s joins the logit scale)
+        // K tile: int8 -> float (the layer's scale s joins the logit scale; a
+        // block-scaled pool's 32-element scales multiply here, s being 1)
         for (int i = tid; i < kTileTok * D / 16; i += blockDim.x) {
             const int tt = i / (D / 16), c = i % (D / 16);
             const uint4 w = *reinterpret_cast<const uint4*>(kbase + (long long)(t0 + tt) * D + c * 16);
             const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            const float sb = kscales ? kscales[((long long)g * ctx_pad + t0 + tt) * (D / 32) + c / 2] : 1.0f;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                Ks[tt][c * 16 + e] = (float)(int8_t)((ws[e / 4] >> (8 * (e % 4))) & 0xFF);
+                Ks[tt][c * 16 + e] = (float)(int8_t)((ws[e / 4] >> (8 * (e % 4))) & 0xFF) * sb;
         }
         // V tile (one 32-token code group, t0 % 32 == 0): a task is 8 tokens of
         // one coordinate, BITS bytes of that coordinate's code sequence -> n_t * c[code]
@@ -236,7 +239,7 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
     const int nsplit = (s.ctx + tok_per_split - 1) / tok_per_split;
     dim3 grid(nsplit, s.kv_heads, (a.rows + kRowsPerBlock - 1) / kRowsPerBlock);
     attend_split_kernel<D, BITS><<<grid, kWarps * 32, 0, st>>>(
-        Lb.kq, Lb.vcodes, Lb.vnorm, Lb.kscale, s.ctx, s.ctx_pad, (const uint16_t*)a.Q, a.q_heads,
+        Lb.kq, Lb.vcodes, Lb.vnorm, Lb.kscale, Lb.kscales, s.ctx, s.ctx_pad, (const uint16_t*)a.Q, a.q_heads,
         a.group, a.rows, a.scale_log2, tok_per_split, scr.acc, scr.ml, nsplit, scr.max_rows,
         codebook(BITS));
     cudaError_t e = cudaGetLastError();

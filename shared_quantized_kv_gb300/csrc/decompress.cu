@@ -14,7 +14,8 @@
 //     shfl.xor and one exact FMA), V_i = bf16(fl(fl(z_i * n) * (1/d))),
 //     coalesced 16-byte stores.
 //   K blocks: K = bf16(fl(q * s)), 16 elements per thread (the int8 to float
-//     conversion by an integer add and one exact subtraction).
+//     conversion by an integer add and one exact subtraction); s is the
+//     layer's scale or, in block-scaled pools, the element's 32-block scale.
 #include <cuda_bf16.h>
 
 #include "kvpool_internal.cuh"
@@ -41,6 +42,7 @@ __device__ __forceinline__ float i8_to_f(uint32_t w, int k) {
 template <int D, int BITS>
 __global__ void __launch_bounds__(kDecThreads)
 decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscale,
+                  const float* __restrict__ kscales,
                   const uint8_t* __restrict__ vcodes, const float* __restrict__ vnorm, int ctx,
                   int ctx_pad, int nbv, uint4* __restrict__ Kout, uint4* __restrict__ Vout,
                   Codebook cb) {
@@ -49,11 +51,12 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     const int tid = threadIdx.x;
     const long long head = blockIdx.y;
     if ((int)blockIdx.x >= nbv) {
-        // ---- K = bf16(q * s)
-        const float s = *kscale;
+        // ---- K = bf16(q * s): the layer's scale, or the scale of the 32-element
+        //      block holding this thread's 16 elements
         const int g = (blockIdx.x - nbv) * kDecThreads + tid;  // 16-element group in the head
         if (g >= ctx * (D / 16)) return;
         const int t = g / (D / 16), c = g % (D / 16);
+        const float s = kscales ? __ldg(kscales + (head * ctx_pad + t) * (D / 32) + c / 2) : *kscale;
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(kq + (head * ctx_pad + t) * D + c * 16));
         const uint32_t w[4] = {q.x, q.y, q.z, q.w};
         uint32_t o[8];
@@ -146,7 +149,7 @@ cudaError_t run(const Shape& s, const LayerBufs& L, void* K_out, void* V_out, cu
     const int nbk = K_out ? (s.ctx * (D / 16) + kDecThreads - 1) / kDecThreads : 0;
     if (nbv + nbk == 0) return cudaSuccess;
     decompress_kernel<D, BITS><<<dim3(nbv + nbk, s.kv_heads), kDecThreads, 0, st>>>(
-        L.kq, L.kscale, L.vcodes, L.vnorm, s.ctx, s.ctx_pad, nbv, (uint4*)K_out, (uint4*)V_out,
+        L.kq, L.kscale, L.kscales, L.vcodes, L.vnorm, s.ctx, s.ctx_pad, nbv, (uint4*)K_out, (uint4*)V_out,
         codebook(BITS));
     return cudaGetLastError();
 }

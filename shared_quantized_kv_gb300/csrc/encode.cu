@@ -145,12 +145,15 @@ kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, ui
     }
 }
 
-template <int D, int BITS>
+// KB: block-scaled K (one scale per 32 elements, written to kscales; no
+// max|K| kernel before this one and *kscale = 1)
+template <int D, int BITS, bool KB>
 __global__ void __launch_bounds__(kEncThreads)
 encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int ctx, int ctx_pad,
               int items_per_head, int items, int8_t* __restrict__ kq, uint8_t* __restrict__ vcodes,
               float* __restrict__ vnorm, float* __restrict__ kscale, uint32_t* __restrict__ maxima,
-              const uint32_t* __restrict__ kpart, int nparts, int* __restrict__ status, Codebook cb) {
+              const uint32_t* __restrict__ kpart, int nparts, float* __restrict__ kscales,
+              int* __restrict__ status, Codebook cb) {
     constexpr int TPV = D / 32;              // threads per head-vector
     constexpr int VPI = kEncThreads / TPV;   // tokens per item (a multiple of 32)
     constexpr uint32_t kTile = VPI * D * 2;  // bytes of K (and of V) per item: 8 KB
@@ -317,6 +320,13 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
         // K: s = max|K| / 127 (1 when K is all zero) from the partial maxima of
         // the max|K| kernel, complete once the dependency wait returns (by now
         // it has long finished: it ran beside the V work above)
+        if (KB && !have_s) {
+            have_s = true;
+            if (blockIdx.x == 0 && tid == 0) {
+                *kscale = 1.0f;
+                maxima[0] = 0;
+            }
+        }
         if (!have_s) {
             ptx::grid_dep_wait();
             uint32_t m = 0;
@@ -344,7 +354,23 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
             for (int c = 0; c < kChunks; ++c) {
                 const int idx = tid + c * kEncThreads;
                 const int row = idx / (D / 8);
-                if (row < ntok) {
+                if constexpr (KB) {
+                    // the 4 chunks of a 32-element block sit in lanes 4j..4j+3
+                    // (same row); every lane takes part in the shuffles
+                    const uint4 u = (row < ntok) ? reinterpret_cast<const uint4*>(sK)[idx] : make_uint4(0, 0, 0, 0);
+                    uint32_t m = absmax8(u);
+                    m = max(m, __shfl_xor_sync(gmask, m, 1));
+                    m = max(m, __shfl_xor_sync(gmask, m, 2));
+                    const float sb = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
+                    if (row < ntok) {
+                        const uint2 q = quant8(u, sb, __frcp_rn(sb));
+                        dep ^= q.x ^ u.x;
+                        const long long tok_i = (long long)h * ctx_pad + t0 + row;
+                        *reinterpret_cast<uint2*>(kq + tok_i * D + (idx % (D / 8)) * 8) = q;
+                        if ((idx & 3) == 0) kscales[tok_i * (D / 32) + (idx % (D / 8)) / 4] = sb;
+                        if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
+                    }
+                } else if (row < ntok) {
                     const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
                     const uint2 q = quant8(u, s, r);
                     dep ^= q.x;
@@ -380,12 +406,14 @@ template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V, int* status,
                 int sm_count, cudaStream_t st) {
     constexpr int VPI = kEncThreads / (D / 32);
-    static int per_sm = -1;
-    if (per_sm < 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, encode_kernel<D, BITS>,
-                                                                      kEncThreads, 0);
-        if (e != cudaSuccess || per_sm < 1) {
-            per_sm = -1;
+    const bool kb = L.kscales != nullptr;
+    static int per_sm[2] = {-1, -1};
+    int& occ = per_sm[kb ? 1 : 0];
+    if (occ < 0) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+            &occ, kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>, kEncThreads, 0);
+        if (e != cudaSuccess || occ < 1) {
+            occ = -1;
             return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
         }
     }
@@ -394,14 +422,21 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     const int ga = (int)std::min<long long>(
         kKmaxParts, std::max<long long>(2LL * sm_count, (nchunk + 2047) / 2048));  // one batch per thread
     const long long per_cta = (nchunk + ga - 1) / ga;
-    kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (kb) {
+        // block scales need no max|K| kernel; the largest-norm word is raised
+        // with atomics by the encode kernel
+        e = cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st);
+    } else {
+        kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
+        e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     // encode: starts while the max|K| kernel runs (programmatic dependent
     // launch); waits for it only before its first K codes
     const int items_per_head = (s.ctx + VPI - 1) / VPI;
     const int items = s.kv_heads * items_per_head;
-    const int G = std::min(items, per_sm * sm_count);
+    const int G = std::min(items, occ * sm_count);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
     cfg.blockDim = dim3(kEncThreads, 1, 1);
@@ -411,10 +446,11 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, encode_kernel<D, BITS>, (const uint16_t*)K, (const uint16_t*)V, s.ctx,
-                              s.ctx_pad, items_per_head, items, L.kq, L.vcodes, L.vnorm, L.kscale, L.kabsmax,
-                              (const uint32_t*)L.kpart, ga, status, codebook(BITS));
+    cfg.numAttrs = kb ? 0 : 1;
+    return cudaLaunchKernelEx(&cfg, kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>,
+                              (const uint16_t*)K, (const uint16_t*)V, s.ctx, s.ctx_pad, items_per_head, items,
+                              L.kq, L.vcodes, L.vnorm, L.kscale, L.kabsmax, (const uint32_t*)L.kpart, ga,
+                              L.kscales, status, codebook(BITS));
 }
 
 __global__ void __launch_bounds__(256)

@@ -8,7 +8,9 @@
 //                 vnorm  f32   [Hk][ctx_pad]
 //   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits, largest
 //   V norm float bits}, per layer 512 partial maxima of max|K| (compress
-//   scratch), status int32.
+//   scratch), status int32. Block-scaled pools (kvpool_create_ex, k_block 32)
+//   also hold per layer kscales f32 [Hk][ctx_pad][D/32] and a split-context
+//   attention scratch.
 // Attention needs no scratch: the CTAs of a cluster merge their context
 // splits through distributed shared memory. Each layer also has a TMA tensor
 // map of its kq (rows of head_dim bytes) for the attention kernel.
@@ -17,6 +19,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <algorithm>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -141,8 +144,9 @@ const Codebook& codebook(int bits) {
 struct kvpool {
     int layers = 0, kv_heads = 0, head_dim = 0, ctx = 0, ctx_pad = 0, max_rows = 0;
     int device = 0, sm_count = 0;
+    int k_block = 0;  // 0: one K scale per layer; 32: one per 32 elements
     std::vector<int> bits;
-    std::vector<size_t> off_kq, off_vc, off_vn;
+    std::vector<size_t> off_kq, off_vc, off_vn, off_ks;
     std::vector<unsigned char> compressed;
     // 1 while the layer was written (compress, import, reset) after the last
     // attend launched on it: that attend must not read the layer before its
@@ -154,13 +158,17 @@ struct kvpool {
     float* kscale = nullptr;
     uint32_t* kabsmax = nullptr;
     uint32_t* kpart = nullptr;
+    float* split_acc = nullptr;  // block-scaled pools: split-context attention scratch
+    float* split_ml = nullptr;
+    int split_n = 0;
     int* status = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
                 reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
-                kabsmax + 2 * l + 1, &kmaps[l], kpart + (size_t)l * kvp::kKmaxParts};
+                kabsmax + 2 * l + 1, &kmaps[l], kpart + (size_t)l * kvp::kKmaxParts,
+                k_block ? reinterpret_cast<float*>(base + off_ks[l]) : nullptr};
     }
 };
 
@@ -234,7 +242,13 @@ int kvpool_codebook(int bits, float* centroids, float* midpoints) {
 
 int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
                   const uint8_t* bits_per_layer, int max_rows) {
+    return kvpool_create_ex(out, layers, kv_heads, head_dim, ctx, bits_per_layer, max_rows, 0);
+}
+
+int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
+                     const uint8_t* bits_per_layer, int max_rows, int k_block) {
     if (!out) return KVPOOL_ERR_INVALID_ARG;
+    if (k_block != 0 && k_block != 32) return KVPOOL_ERR_INVALID_ARG;
     *out = nullptr;
     if (layers < 1 || kv_heads < 1 || ctx < 1 || (head_dim != 64 && head_dim != 128))
         return KVPOOL_ERR_INVALID_ARG;
@@ -261,6 +275,7 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     p->ctx = ctx;
     p->ctx_pad = (ctx + kvp::kTokenPad - 1) / kvp::kTokenPad * kvp::kTokenPad;
     p->max_rows = max_rows;
+    p->k_block = k_block;
     p->device = dev;
     p->sm_count = prop.multiProcessorCount;
     p->bits.resize(layers);
@@ -275,6 +290,8 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
         off = align256(off + nvec * head_dim * p->bits[l] / 8);
         p->off_vn.push_back(off);
         off = align256(off + nvec * 4);
+        p->off_ks.push_back(off);
+        if (k_block) off = align256(off + nvec * (head_dim / k_block) * 4);
     }
     const size_t off_scale = off;
     off = align256(off + 4 * (size_t)layers);
@@ -282,6 +299,18 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     off = align256(off + 8 * (size_t)layers);
     const size_t off_kpart = off;  // per layer: partial maxima of max|K| (compress scratch)
     off = align256(off + 4 * (size_t)kvp::kKmaxParts * layers);
+    // block-scaled pools attend on CUDA cores: split scratch for max_rows rows,
+    // about two splits per SM over the KV heads
+    size_t off_sacc = off, off_sml = off;
+    if (k_block) {
+        const int ntile = (p->ctx + 31) / 32;
+        p->split_n = std::max(1, std::min(ntile, (2 * p->sm_count + kv_heads - 1) / kv_heads));
+        const size_t rows = (size_t)kv_heads * p->split_n * max_rows;
+        off_sacc = off;
+        off = align256(off + rows * head_dim * 4);
+        off_sml = off;
+        off = align256(off + rows * 2 * 4);
+    }
     const size_t off_status = off;
     off = align256(off + 4);
     p->bytes = off;
@@ -300,6 +329,10 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
     p->kpart = reinterpret_cast<uint32_t*>(p->base + off_kpart);
+    if (k_block) {
+        p->split_acc = reinterpret_cast<float*>(p->base + off_sacc);
+        p->split_ml = reinterpret_cast<float*>(p->base + off_sml);
+    }
     p->status = reinterpret_cast<int*>(p->base + off_status);
     p->fresh.assign(layers, 1);
     p->kmaps.resize(layers);
@@ -366,8 +399,18 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
     a.early = p->fresh[layer] ? 0 : 1;
-    cudaError_t e = kvp::launch_attend_tc(p->shape(), p->layer(layer), a, p->status, p->sm_count,
-                                          static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (p->k_block) {  // block-scaled K: CUDA-core split kernels, the pool's own scratch
+        kvp::AttendScratch scr;
+        scr.acc = p->split_acc;
+        scr.ml = p->split_ml;
+        scr.nsplit = p->split_n;
+        scr.max_rows = p->max_rows;
+        e = kvp::launch_attend_split(p->shape(), p->layer(layer), a, scr, static_cast<cudaStream_t>(stream));
+    } else {
+        e = kvp::launch_attend_tc(p->shape(), p->layer(layer), a, p->status, p->sm_count,
+                                  static_cast<cudaStream_t>(stream));
+    }
     if (e == cudaSuccess) p->fresh[layer] = 0;
     return map_cuda(e);
 }
@@ -385,8 +428,10 @@ size_t kvpool_pool_bytes(const kvpool_t* p) {
     if (!p) return 0;
     size_t total = 0;
     const size_t nvec = (size_t)p->kv_heads * p->ctx;
-    for (int l = 0; l < p->layers; ++l)
+    for (int l = 0; l < p->layers; ++l) {
         total += nvec * p->head_dim + nvec * p->head_dim * p->bits[l] / 8 + 4 * nvec + 4;
+        if (p->k_block) total += nvec * (p->head_dim / p->k_block) * 4;
+    }
     return total;
 }
 
@@ -429,6 +474,8 @@ int kvpool_layer_view(const kvpool_t* p, int layer, kvpool_layer_view_t* v) {
     v->ctx_padded = p->ctx_pad;
     v->bits = L.bits;
     v->compressed = p->compressed[layer];
+    v->kscales = L.kscales;
+    v->k_block = p->k_block;
     return KVPOOL_OK;
 }
 
@@ -474,6 +521,7 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
                         const void* vnorm, const void* kscale, void* stream) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
+    if (p->k_block) return KVPOOL_ERR_UNSUPPORTED;
     if (!kq || !vcodes || !vnorm || !kscale) return KVPOOL_ERR_INVALID_ARG;
     if (p->compressed[layer]) return KVPOOL_ERR_STATE;
     rc = copy_layer(p, layer, true, const_cast<void*>(kq), const_cast<void*>(vcodes),
@@ -484,6 +532,19 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
     p->fresh[layer] = 1;
     if (rc == KVPOOL_OK) p->compressed[layer] = 1;
     return rc;
+}
+
+int kvpool_export_kscales(const kvpool_t* p, int layer, float* kscales, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!kscales) return KVPOOL_ERR_INVALID_ARG;
+    if (!p->k_block) return KVPOOL_ERR_UNSUPPORTED;
+    if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
+    const kvp::LayerBufs L = p->layer(layer);
+    const size_t per = (size_t)(p->head_dim / p->k_block) * 4;  // bytes per token
+    return map_cuda(cudaMemcpy2DAsync(kscales, (size_t)p->ctx * per, L.kscales, (size_t)p->ctx_pad * per,
+                                      (size_t)p->ctx * per, (size_t)p->kv_heads, cudaMemcpyDefault,
+                                      static_cast<cudaStream_t>(stream)));
 }
 
 const char* kvpool_strerror(int code) {

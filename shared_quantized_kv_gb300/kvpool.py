@@ -35,7 +35,8 @@ class Tail(ctypes.Structure):
 class LayerView(ctypes.Structure):
     _fields_ = [("kq", ctypes.c_void_p), ("vcodes", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
                 ("kscale", ctypes.c_void_p), ("ctx", ctypes.c_int), ("ctx_padded", ctypes.c_int),
-                ("bits", ctypes.c_int), ("compressed", ctypes.c_int)]
+                ("bits", ctypes.c_int), ("compressed", ctypes.c_int),
+                ("kscales", ctypes.c_void_p), ("k_block", ctypes.c_int)]
 
 
 _LIB = None
@@ -44,6 +45,10 @@ _LIB = None
 _SIGS = {
     "kvpool_create": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int,
                                      ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]),
+    "kvpool_create_ex": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_int]),
+    "kvpool_export_kscales": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "kvpool_destroy": (None, [ctypes.c_void_p]),
     "kvpool_compress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
@@ -122,13 +127,16 @@ def codebook(bits: int):
 class KVPool:
     """One shared pool (a ``kvpool_t``) on the current CUDA device."""
 
-    def __init__(self, layers, kv_heads, head_dim, ctx, bits=None, max_rows=0):
+    def __init__(self, layers, kv_heads, head_dim, ctx, bits=None, max_rows=0, k_block=0):
+        """k_block: 0 (one K scale per layer) or 32 (one per 32 elements)."""
         self.layers, self.kv_heads, self.head_dim, self.ctx = layers, kv_heads, head_dim, ctx
         self.bits = list(bits) if bits is not None else [3] * layers
+        self.k_block = k_block
         arr = (ctypes.c_uint8 * layers)(*self.bits)
         h = ctypes.c_void_p()
-        _check(_lib().kvpool_create(ctypes.byref(h), layers, kv_heads, head_dim, ctx,
-                                    ctypes.cast(arr, ctypes.c_void_p), max_rows), "kvpool_create")
+        _check(_lib().kvpool_create_ex(ctypes.byref(h), layers, kv_heads, head_dim, ctx,
+                                       ctypes.cast(arr, ctypes.c_void_p), max_rows, k_block),
+               "kvpool_create_ex")
         self._h = h
 
     @property
@@ -230,8 +238,20 @@ class KVPool:
                                           vnorm.data_ptr(), kscale.data_ptr(),
                                           _stream_ptr(stream)), "kvpool_import_layer")
 
+    def export_kscales(self, layer, stream=None):
+        """Block scales of a block-scaled pool's layer: float32 [Hk, ctx, d/32]."""
+        import torch
+
+        out = torch.empty((self.kv_heads, self.ctx, self.head_dim // 32), dtype=torch.float32, device="cuda")
+        _check(_lib().kvpool_export_kscales(self._h, layer, out.data_ptr(), _stream_ptr(stream)),
+               "kvpool_export_kscales")
+        return out
+
     def read_layer(self, layer):
         """Host numpy copies of one layer's stored bytes (see export_layer)."""
         kq, vc, vn, ks = self.export_layer(layer)
-        return dict(kq=kq.cpu().numpy(), vcodes=vc.cpu().numpy(), vnorm=vn.cpu().numpy(),
-                    kscale=ks.cpu().numpy()[0])
+        d = dict(kq=kq.cpu().numpy(), vcodes=vc.cpu().numpy(), vnorm=vn.cpu().numpy(),
+                 kscale=ks.cpu().numpy()[0])
+        if self.k_block:
+            d["kscales"] = self.export_kscales(layer).cpu().numpy()
+        return d

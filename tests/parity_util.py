@@ -31,6 +31,9 @@ def check_encode(pool, layer, enc):
     assert np.array_equal(got["vnorm"].view(np.uint32), enc["norms"].view(np.uint32)), \
         _first_diff(got["vnorm"], enc["norms"])
     assert np.array_equal(got["vcodes"], enc["packed"]), _first_diff(got["vcodes"], enc["packed"])
+    if enc.get("k_block"):
+        assert np.array_equal(got["kscales"].view(np.uint32), enc["kscales"].view(np.uint32)), \
+            _first_diff(got["kscales"], enc["kscales"])
 
 
 def check_decompress(pool, layer, enc):

@@ -62,6 +62,9 @@ def test_create_rejects_bad_arguments_without_a_device(kp):
     bad_bits = (ctypes.c_uint8 * 2)(3, 5)
     assert lib.kvpool_create(ctypes.byref(h), 2, 2, 64, 256, ctypes.cast(bad_bits, ctypes.c_void_p), 0) == -1
     assert lib.kvpool_create(None, 1, 2, 64, 256, None, 0) == -1
+    for kb in (1, 16, 64, -32):  # only 0 and 32 are K block sizes
+        assert lib.kvpool_create_ex(ctypes.byref(h), 1, 2, 64, 256, None, 0, kb) == -1
+    assert lib.kvpool_export_kscales(None, 0, None, None) == -1
 
 
 def test_null_pool_calls(kp):
