@@ -93,6 +93,8 @@ typedef struct {
                               scale per 32 elements (*kscale is then 1); NULL
                               for per-tensor pools                            */
     int k_block;           /* 0 (per-tensor scale) or 32                       */
+    int len;               /* tokens the layer holds: ctx once compressed or
+                              imported; appends (kvpool_append) grow it         */
 } kvpool_layer_view_t;
 
 /* Create a pool for `layers` layers of a shared context of `ctx` tokens with
@@ -130,6 +132,25 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
  * the layer is not compressed. */
 int kvpool_export_kscales(const kvpool_t* pool, int layer, float* kscales, void* stream);
 
+/* Incremental pool append (CoMixKV article: aged recent-state blocks are
+ * quantised into new pool blocks; earlier blocks are never rewritten) for
+ * block-scaled pools: encode n new tokens K, V bf16 [kv_heads][n][head_dim]
+ * (device, 16-byte aligned) as tokens [len, len + n) of the layer, exactly as
+ * kvpool_compress encodes each token (with block-scaled K every stored byte
+ * depends on its own token only, so the layer equals the encode of all its
+ * tokens at once). A layer starts empty (len 0, also after
+ * kvpool_reset_layer); kvpool_compress on an empty block-scaled layer is the
+ * append of all ctx tokens. Attend, decompress and export read tokens
+ * [0, len) (decompress writes [kv_heads][len][head_dim]). Before an append
+ * len must be a multiple of 32 (an append of a length that is not a multiple
+ * of 32 closes the layer: KVPOOL_ERR_STATE), and len + n <= ctx
+ * (KVPOOL_ERR_INVALID_ARG). Per-tensor pools: KVPOOL_ERR_UNSUPPORTED (one K
+ * scale cannot take new tokens without re-encoding the old ones). */
+int kvpool_append(kvpool_t* pool, int layer, const void* K, const void* V, int n, void* stream);
+
+/* Tokens layer `layer` holds (see kvpool_append), or a negative error code. */
+int kvpool_layer_len(const kvpool_t* pool, int layer);
+
 /* Free all device memory of the pool. Waits for the device first. NULL is a
  * no-op. */
 void kvpool_destroy(kvpool_t* pool);
@@ -160,7 +181,8 @@ int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_he
 
 /* Materialise one layer as bf16: K_out = bf16(q*s), V_out_i = bf16(fl(z_i*n)
  * * (1/d)) with z = FWHT(c[codes]) in float32. K_out, V_out: bf16
- * [kv_heads][ctx][head_dim], device. This is the per-agent decompression of
+ * [kv_heads][len][head_dim], device (len = kvpool_layer_len: ctx unless the
+ * layer was built by appends). This is the per-agent decompression of
  * the PolyKV summary, section 2.A (each agent injects the decompressed KV into
  * its own cache). */
 int kvpool_decompress(kvpool_t* pool, int layer, void* K_out, void* V_out, void* stream);

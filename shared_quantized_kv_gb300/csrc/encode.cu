@@ -150,7 +150,7 @@ kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, ui
 template <int D, int BITS, bool KB>
 __global__ void __launch_bounds__(kEncThreads)
 encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int ctx, int ctx_pad,
-              int items_per_head, int items, int8_t* __restrict__ kq, uint8_t* __restrict__ vcodes,
+              int t_base, int items_per_head, int items, int8_t* __restrict__ kq, uint8_t* __restrict__ vcodes,
               float* __restrict__ vnorm, float* __restrict__ kscale, uint32_t* __restrict__ maxima,
               const uint32_t* __restrict__ kpart, int nparts, float* __restrict__ kscales,
               int* __restrict__ status, Codebook cb) {
@@ -295,7 +295,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
         uint4* c8 = reinterpret_cast<uint4*>(codes8 + tl * D + lt * 32);
         c8[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
         c8[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        if (live && lt == 0) vnorm[(long long)h * ctx_pad + t0 + tl] = n;
+        if (live && lt == 0) vnorm[(long long)h * ctx_pad + t_base + t0 + tl] = n;
         __syncthreads();
 
         // pool layout: one thread per (32-token group of the item, coordinate)
@@ -311,7 +311,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                 words[w] |= code << off;
                 if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
             }
-            const long long grp = ((long long)h * ctx_pad + t0) / 32 + gq;
+            const long long grp = ((long long)h * ctx_pad + t_base + t0) / 32 + gq;
             uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
 #pragma unroll
             for (int w = 0; w < BITS; ++w) out[w] = words[w];
@@ -365,7 +365,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                     if (row < ntok) {
                         const uint2 q = quant8(u, sb, __frcp_rn(sb));
                         dep ^= q.x ^ u.x;
-                        const long long tok_i = (long long)h * ctx_pad + t0 + row;
+                        const long long tok_i = (long long)h * ctx_pad + t_base + t0 + row;
                         *reinterpret_cast<uint2*>(kq + tok_i * D + (idx % (D / 8)) * 8) = q;
                         if ((idx & 3) == 0) kscales[tok_i * (D / 32) + (idx % (D / 8)) / 4] = sb;
                         if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
@@ -374,7 +374,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                     const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
                     const uint2 q = quant8(u, s, r);
                     dep ^= q.x;
-                    *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t0 + row) * D + (idx % (D / 8)) * 8) = q;
+                    *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t_base + t0 + row) * D + (idx % (D / 8)) * 8) = q;
                 }
             }
             sDep[tid] = dep;  // as for the V tile
@@ -402,9 +402,11 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
     }
 }
 
+// s.ctx: tokens of this call (the inputs' token axis); t_base: the pool token
+// they start at (0, or a multiple of 32 for appends to block-scaled pools)
 template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V, int* status,
-                int sm_count, cudaStream_t st) {
+                int sm_count, int t_base, cudaStream_t st) {
     constexpr int VPI = kEncThreads / (D / 32);
     const bool kb = L.kscales != nullptr;
     static int per_sm[2] = {-1, -1};
@@ -425,8 +427,8 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     cudaError_t e;
     if (kb) {
         // block scales need no max|K| kernel; the largest-norm word is raised
-        // with atomics by the encode kernel
-        e = cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st);
+        // with atomics by the encode kernel (over every append of the layer)
+        e = t_base == 0 ? cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st) : cudaSuccess;
     } else {
         kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
         e = cudaGetLastError();
@@ -448,7 +450,7 @@ cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V
     cfg.attrs = attr;
     cfg.numAttrs = kb ? 0 : 1;
     return cudaLaunchKernelEx(&cfg, kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>,
-                              (const uint16_t*)K, (const uint16_t*)V, s.ctx, s.ctx_pad, items_per_head, items,
+                              (const uint16_t*)K, (const uint16_t*)V, s.ctx, s.ctx_pad, t_base, items_per_head, items,
                               L.kq, L.vcodes, L.vnorm, L.kscale, L.kabsmax, (const uint32_t*)L.kpart, ga,
                               L.kscales, status, codebook(BITS));
 }
@@ -477,15 +479,16 @@ cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st)
 }
 
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, int sm_count, cudaStream_t st) {
+                          int* status, int sm_count, int t_base, cudaStream_t st) {
+    if (t_base != 0 && (L.kscales == nullptr || t_base % 32 != 0)) return cudaErrorInvalidValue;
     if (s.head_dim == 64) {
-        if (L.bits == 2) return run<64, 2>(s, L, K, V, status, sm_count, st);
-        if (L.bits == 3) return run<64, 3>(s, L, K, V, status, sm_count, st);
-        return run<64, 4>(s, L, K, V, status, sm_count, st);
+        if (L.bits == 2) return run<64, 2>(s, L, K, V, status, sm_count, t_base, st);
+        if (L.bits == 3) return run<64, 3>(s, L, K, V, status, sm_count, t_base, st);
+        return run<64, 4>(s, L, K, V, status, sm_count, t_base, st);
     }
-    if (L.bits == 2) return run<128, 2>(s, L, K, V, status, sm_count, st);
-    if (L.bits == 3) return run<128, 3>(s, L, K, V, status, sm_count, st);
-    return run<128, 4>(s, L, K, V, status, sm_count, st);
+    if (L.bits == 2) return run<128, 2>(s, L, K, V, status, sm_count, t_base, st);
+    if (L.bits == 3) return run<128, 3>(s, L, K, V, status, sm_count, t_base, st);
+    return run<128, 4>(s, L, K, V, status, sm_count, t_base, st);
 }
 
 }  // namespace kvp

@@ -148,6 +148,7 @@ struct kvpool {
     std::vector<int> bits;
     std::vector<size_t> off_kq, off_vc, off_vn, off_ks;
     std::vector<unsigned char> compressed;
+    std::vector<int> len;  // tokens the layer holds: ctx once compressed; grows by appends
     // 1 while the layer was written (compress, import, reset) after the last
     // attend launched on it: that attend must not read the layer before its
     // grid-dependency wait
@@ -164,6 +165,8 @@ struct kvpool {
     int* status = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
+    // the layer's current tokens (attend, decompress, export read [0, len))
+    kvp::Shape shape_of(int l) const { return {kv_heads, head_dim, len[l], ctx_pad}; }
     kvp::LayerBufs layer(int l) const {
         return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
                 reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
@@ -280,6 +283,7 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
     p->sm_count = prop.multiProcessorCount;
     p->bits.resize(layers);
     p->compressed.assign(layers, 0);
+    p->len.assign(layers, 0);
     size_t off = 0;
     const size_t nvec = (size_t)kv_heads * p->ctx_pad;
     for (int l = 0; l < layers; ++l) {
@@ -360,12 +364,37 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
     if (rc) return rc;
     if (!K || !V || !aligned16(K) || !aligned16(V)) return KVPOOL_ERR_INVALID_ARG;
     if (p->compressed[layer]) return KVPOOL_ERR_STATE;
-    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status, p->sm_count,
+    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status, p->sm_count, 0,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     p->compressed[layer] = 1;
+    p->len[layer] = p->ctx;
     p->fresh[layer] = 1;
     return KVPOOL_OK;
+}
+
+int kvpool_append(kvpool_t* p, int layer, const void* K, const void* V, int n, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!K || !V || !aligned16(K) || !aligned16(V) || n < 1) return KVPOOL_ERR_INVALID_ARG;
+    if (!p->k_block) return KVPOOL_ERR_UNSUPPORTED;
+    const int len = p->len[layer];
+    if (len % 32 != 0) return KVPOOL_ERR_STATE;  // a ragged append closed the layer
+    if ((long long)len + n > p->ctx) return KVPOOL_ERR_INVALID_ARG;
+    const kvp::Shape s{p->kv_heads, p->head_dim, n, p->ctx_pad};
+    cudaError_t e = kvp::launch_encode(s, p->layer(layer), K, V, p->status, p->sm_count, len,
+                                       static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return map_cuda(e);
+    p->len[layer] = len + n;
+    p->compressed[layer] = 1;
+    p->fresh[layer] = 1;
+    return KVPOOL_OK;
+}
+
+int kvpool_layer_len(const kvpool_t* p, int layer) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    return p->len[layer];
 }
 
 int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads,
@@ -406,9 +435,9 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
         scr.ml = p->split_ml;
         scr.nsplit = p->split_n;
         scr.max_rows = p->max_rows;
-        e = kvp::launch_attend_split(p->shape(), p->layer(layer), a, scr, static_cast<cudaStream_t>(stream));
+        e = kvp::launch_attend_split(p->shape_of(layer), p->layer(layer), a, scr, static_cast<cudaStream_t>(stream));
     } else {
-        e = kvp::launch_attend_tc(p->shape(), p->layer(layer), a, p->status, p->sm_count,
+        e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
                                   static_cast<cudaStream_t>(stream));
     }
     if (e == cudaSuccess) p->fresh[layer] = 0;
@@ -420,7 +449,7 @@ int kvpool_decompress(kvpool_t* p, int layer, void* K_out, void* V_out, void* st
     if (rc) return rc;
     if ((!K_out && !V_out) || !aligned16(K_out) || !aligned16(V_out)) return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
-    return map_cuda(kvp::launch_decompress(p->shape(), p->layer(layer), K_out, V_out,
+    return map_cuda(kvp::launch_decompress(p->shape_of(layer), p->layer(layer), K_out, V_out,
                                            static_cast<cudaStream_t>(stream)));
 }
 
@@ -457,6 +486,7 @@ int kvpool_reset_layer(kvpool_t* p, int layer) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
     p->compressed[layer] = 0;
+    p->len[layer] = 0;
     p->fresh[layer] = 1;
     return KVPOOL_OK;
 }
@@ -476,6 +506,7 @@ int kvpool_layer_view(const kvpool_t* p, int layer, kvpool_layer_view_t* v) {
     v->compressed = p->compressed[layer];
     v->kscales = L.kscales;
     v->k_block = p->k_block;
+    v->len = p->len[layer];
     return KVPOOL_OK;
 }
 
@@ -486,11 +517,12 @@ int copy_layer(const kvpool* p, int layer, bool to_pool, void* kq, void* vc, voi
                void* ks, cudaStream_t st) {
     const kvp::LayerBufs L = p->layer(layer);
     const size_t rows = (size_t)p->kv_heads;
-    const size_t kw = (size_t)p->ctx * p->head_dim, kp = (size_t)p->ctx_pad * p->head_dim;
+    const int T = to_pool ? p->ctx : p->len[layer];  // tokens moved
+    const size_t kw = (size_t)T * p->head_dim, kp = (size_t)p->ctx_pad * p->head_dim;
     const size_t vb = (size_t)p->head_dim * L.bits / 8;
     // V codes travel in whole 32-token groups (the pool layout)
-    const size_t vw = (size_t)((p->ctx + 31) / 32 * 32) * vb, vp = (size_t)p->ctx_pad * vb;
-    const size_t nw = (size_t)p->ctx * 4, np_ = (size_t)p->ctx_pad * 4;
+    const size_t vw = (size_t)((T + 31) / 32 * 32) * vb, vp = (size_t)p->ctx_pad * vb;
+    const size_t nw = (size_t)T * 4, np_ = (size_t)p->ctx_pad * 4;
     cudaError_t e = cudaSuccess;
     if (kq && e == cudaSuccess)
         e = to_pool ? cudaMemcpy2DAsync(L.kq, kp, kq, kw, kw, rows, cudaMemcpyDefault, st)
@@ -530,7 +562,10 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
     if (rc != KVPOOL_OK) return rc;
     rc = map_cuda(kvp::launch_norm_max(p->shape(), p->layer(layer), static_cast<cudaStream_t>(stream)));
     p->fresh[layer] = 1;
-    if (rc == KVPOOL_OK) p->compressed[layer] = 1;
+    if (rc == KVPOOL_OK) {
+        p->compressed[layer] = 1;
+        p->len[layer] = p->ctx;
+    }
     return rc;
 }
 
@@ -542,8 +577,9 @@ int kvpool_export_kscales(const kvpool_t* p, int layer, float* kscales, void* st
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
     const kvp::LayerBufs L = p->layer(layer);
     const size_t per = (size_t)(p->head_dim / p->k_block) * 4;  // bytes per token
-    return map_cuda(cudaMemcpy2DAsync(kscales, (size_t)p->ctx * per, L.kscales, (size_t)p->ctx_pad * per,
-                                      (size_t)p->ctx * per, (size_t)p->kv_heads, cudaMemcpyDefault,
+    const size_t T = (size_t)p->len[layer];
+    return map_cuda(cudaMemcpy2DAsync(kscales, T * per, L.kscales, (size_t)p->ctx_pad * per,
+                                      T * per, (size_t)p->kv_heads, cudaMemcpyDefault,
                                       static_cast<cudaStream_t>(stream)));
 }
 

@@ -54,8 +54,10 @@ struct Shape {
 };
 
 // ---- encode (write-once compress of one layer)
+// s.ctx is the token count of K and V; t_base the pool token they start at
+// (non-zero only for appends to block-scaled layers, a multiple of 32).
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, int sm_count, cudaStream_t st);
+                          int* status, int sm_count, int t_base, cudaStream_t st);
 
 // ---- decompress
 cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out,

@@ -36,7 +36,7 @@ class LayerView(ctypes.Structure):
     _fields_ = [("kq", ctypes.c_void_p), ("vcodes", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
                 ("kscale", ctypes.c_void_p), ("ctx", ctypes.c_int), ("ctx_padded", ctypes.c_int),
                 ("bits", ctypes.c_int), ("compressed", ctypes.c_int),
-                ("kscales", ctypes.c_void_p), ("k_block", ctypes.c_int)]
+                ("kscales", ctypes.c_void_p), ("k_block", ctypes.c_int), ("len", ctypes.c_int)]
 
 
 _LIB = None
@@ -49,6 +49,9 @@ _SIGS = {
                                         ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                         ctypes.c_int]),
     "kvpool_export_kscales": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_int, ctypes.c_void_p]),
+    "kvpool_layer_len": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "kvpool_destroy": (None, [ctypes.c_void_p]),
     "kvpool_compress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
@@ -161,6 +164,22 @@ class KVPool:
                                       _dev_ptr(V, torch.bfloat16, "V"), _stream_ptr(stream)),
                "kvpool_compress")
 
+    def append(self, layer, K, V, stream=None):
+        """Append tokens to a block-scaled layer: K, V bf16 [kv_heads, n, d]
+        (device) become tokens [len, len + n) of the layer."""
+        import torch
+
+        _check(_lib().kvpool_append(self._h, layer, _dev_ptr(K, torch.bfloat16, "K"),
+                                    _dev_ptr(V, torch.bfloat16, "V"), int(K.shape[1]),
+                                    _stream_ptr(stream)), "kvpool_append")
+
+    def layer_len(self, layer) -> int:
+        """Tokens the layer holds (ctx once compressed)."""
+        n = int(_lib().kvpool_layer_len(self._h, layer))
+        if n < 0:
+            raise KVPoolError(n, "kvpool_layer_len")
+        return n
+
     def attend(self, layer, Q, out=None, tail=None, softmax_scale=0.0, stream=None):
         """Q: bf16 [agents, q_heads, d]; tail: None or (K, V, lens) with K, V
         bf16 [agents, kv_heads, T_max, d] and lens int32 [agents] (device).
@@ -185,7 +204,7 @@ class KVPool:
     def decompress(self, layer, K_out=None, V_out=None, stream=None):
         import torch
 
-        shape = (self.kv_heads, self.ctx, self.head_dim)
+        shape = (self.kv_heads, self.layer_len(layer), self.head_dim)
         dev = torch.device("cuda", torch.cuda.current_device())
         if K_out is None:
             K_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
@@ -223,7 +242,7 @@ class KVPool:
 
         bits = self.bits[layer]
         dev = torch.device("cuda", torch.cuda.current_device())
-        Hk, T, d = self.kv_heads, self.ctx, self.head_dim
+        Hk, T, d = self.kv_heads, self.layer_len(layer), self.head_dim
         kq = torch.empty((Hk, T, d), dtype=torch.int8, device=dev)
         vc = torch.empty((Hk, (T + 31) // 32, d, 4 * bits), dtype=torch.uint8, device=dev)
         vn = torch.empty((Hk, T), dtype=torch.float32, device=dev)
@@ -242,7 +261,8 @@ class KVPool:
         """Block scales of a block-scaled pool's layer: float32 [Hk, ctx, d/32]."""
         import torch
 
-        out = torch.empty((self.kv_heads, self.ctx, self.head_dim // 32), dtype=torch.float32, device="cuda")
+        out = torch.empty((self.kv_heads, self.layer_len(layer), self.head_dim // 32), dtype=torch.float32,
+                          device="cuda")
         _check(_lib().kvpool_export_kscales(self._h, layer, out.data_ptr(), _stream_ptr(stream)),
                "kvpool_export_kscales")
         return out

@@ -455,3 +455,19 @@ def test_k_block_layer_round_trip_and_dequantisation():
     assert err_b <= err_t
     with pytest.raises(ValueError):
         codec.encode_layer(K, V, 3, k_block=16)
+
+
+def test_block_k_encoding_concatenates_at_group_boundaries():
+    # incremental append reads: with block-scaled K every stored byte depends
+    # only on its own token, so encoding a context in parts (split at 32-token
+    # group boundaries) gives the bytes of encoding it at once; a per-tensor
+    # K scale depends on every token, which is why appends need block scales
+    K = _rand_k((2, 100, 64), 21)
+    V = _rand_k((2, 100, 64), 22)
+    whole = codec.encode_layer(K, V, 3, k_block=32)
+    parts = [codec.encode_layer(K[:, a:b], V[:, a:b], 3, k_block=32) for a, b in ((0, 32), (32, 96), (96, 100))]
+    for key in ("kq", "kscales", "norms", "codes"):
+        assert np.array_equal(np.concatenate([p[key] for p in parts], axis=1), whole[key]), key
+    assert np.array_equal(np.concatenate([p["packed"] for p in parts], axis=1), whole["packed"])
+    tensor = [codec.encode_layer(K[:, a:b], V[:, a:b], 3) for a, b in ((0, 32), (32, 100))]
+    assert not np.array_equal(np.concatenate([p["kq"] for p in tensor], axis=1), codec.encode_layer(K, V, 3)["kq"])
