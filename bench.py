@@ -165,7 +165,8 @@ def run_gpu(args):
 
     w = wl.WORKLOADS[args.workload]
     L, A = w.layers, w.agents
-    pool = kvpool.KVPool(L, w.kv_heads, w.head_dim, w.ctx, w.bits_list(), max_rows=max(w.rows, 1))
+    pool = kvpool.KVPool(L, w.kv_heads, w.head_dim, w.ctx, w.bits_list(), max_rows=max(w.rows, 1),
+                         k_block=args.k_block)
     seed = rank  # each rank serves its own agents over its own pool
     K, V = [], []
     for l in range(L):
@@ -285,7 +286,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/u3+f32",
         "data": "synthetic (seeded; bf16 K/V with LogNormal(0,0.5) channel std and 1% x10 outlier "
                 "channels, Q ~ N(0,1))",
-        "config": {"workload": w.name, "layers": L, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
+        "config": {"workload": w.name, "k_scales": "per 32 elements" if args.k_block else "per layer",
+                   "layers": L, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
                    "head_dim": w.head_dim, "ctx": w.ctx, "agents": A,
                    "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
                    "step": "compress+attend+decompress, all layers",
@@ -296,7 +298,8 @@ def run_gpu(args):
                      "peak": peak, "unit": "GB/s", "frac": ph_info[dom]["hbm_frac"],
                      "traffic": _traffic(dom_file), "peak_source": peak_kind,
                      "algo_bytes_per_launch": int(algo[dom])},
-        # per layer: kmax + encode (compress), attend_tc, decompress
+        # per layer: kmax + encode (compress), attend_tc, decompress; with
+        # --k-block 32: encode, attend_split + attend_combine, decompress
         "gpu_launches": args.steps * L * 4,
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
@@ -473,6 +476,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--k-block", type=int, default=0, choices=[0, 32],
+                    help="K scales: 0 = one per layer (default), 32 = one per 32 elements")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
