@@ -13,7 +13,8 @@
 //     the encoder's stage order (h < 32 in registers, h = 32, 64 by
 //     shfl.xor and one exact FMA), V_i = bf16(fl(fl(z_i * n) * (1/d))),
 //     coalesced 16-byte stores.
-//   K blocks: K = bf16(fl(q * s)), 16 elements per thread (the int8 to float
+//   K blocks: K = bf16(fl(q * s)), four 16-element groups per thread, loads
+//     first, so that the V and K blocks fit one wave (the int8 to float
 //     conversion by an integer add and one exact subtraction); s is the
 //     layer's scale or, in block-scaled pools, the element's 32-block scale.
 #include <cuda_bf16.h>
@@ -24,6 +25,7 @@ namespace kvp {
 namespace {
 
 constexpr int kDecThreads = 256;
+constexpr int kKGroups = 4;  // K blocks: 16-element groups per thread (V and K blocks fit one wave)
 
 // bf16 bits of (lo, hi), each rounded to nearest even, lo in the low half
 __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
@@ -52,22 +54,36 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     const long long head = blockIdx.y;
     if ((int)blockIdx.x >= nbv) {
         // ---- K = bf16(q * s): the layer's scale, or the scale of the 32-element
-        //      block holding this thread's 16 elements
-        const int g = (blockIdx.x - nbv) * kDecThreads + tid;  // 16-element group in the head
-        if (g >= ctx * (D / 16)) return;
-        const int t = g / (D / 16), c = g % (D / 16);
-        const float s = kscales ? __ldg(kscales + (head * ctx_pad + t) * (D / 32) + c / 2) : *kscale;
-        const uint4 q = __ldg(reinterpret_cast<const uint4*>(kq + (head * ctx_pad + t) * D + c * 16));
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-        uint32_t o[8];
+        //      block holding a 16-element group. kKGroups groups per thread,
+        //      all loads in flight before any conversion.
+        const int n16 = ctx * (D / 16);  // 16-element groups in the head
+        const float s0 = kscales ? 1.0f : *kscale;
+        uint4 q[kKGroups];
+        float sc[kKGroups];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float k0 = i8_to_f(w[j / 2], 2 * (j % 2)), k1 = i8_to_f(w[j / 2], 2 * (j % 2) + 1);
-            o[j] = bf16x2_bits(__fmul_rn(k0, s), __fmul_rn(k1, s));
+        for (int u = 0; u < kKGroups; ++u) {
+            const int g = (blockIdx.x - nbv) * (kDecThreads * kKGroups) + u * kDecThreads + tid;
+            const int t = g / (D / 16), c = g % (D / 16);
+            q[u] = g < n16 ? __ldg(reinterpret_cast<const uint4*>(kq + (head * ctx_pad + t) * D + c * 16))
+                           : make_uint4(0, 0, 0, 0);
+            sc[u] = (kscales && g < n16) ? __ldg(kscales + (head * ctx_pad + t) * (D / 32) + c / 2) : s0;
         }
-        uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
-        out[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+#pragma unroll
+        for (int u = 0; u < kKGroups; ++u) {
+            const int g = (blockIdx.x - nbv) * (kDecThreads * kKGroups) + u * kDecThreads + tid;
+            if (g >= n16) break;
+            const int t = g / (D / 16), c = g % (D / 16);
+            const uint32_t w[4] = {q[u].x, q[u].y, q[u].z, q[u].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float k0 = i8_to_f(w[j / 2], 2 * (j % 2)), k1 = i8_to_f(w[j / 2], 2 * (j % 2) + 1);
+                o[j] = bf16x2_bits(__fmul_rn(k0, sc[u]), __fmul_rn(k1, sc[u]));
+            }
+            uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
+            out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+        }
         return;
     }
     // ---- V = bf16(fl(fl(z * n) * (1/d))), z = FWHT(c[codes])
@@ -146,7 +162,7 @@ template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& L, void* K_out, void* V_out, cudaStream_t st) {
     constexpr int VPB = kDecThreads / (D / 32);
     const int nbv = V_out ? (s.ctx + VPB - 1) / VPB : 0;
-    const int nbk = K_out ? (s.ctx * (D / 16) + kDecThreads - 1) / kDecThreads : 0;
+    const int nbk = K_out ? (s.ctx * (D / 16) + kDecThreads * kKGroups - 1) / (kDecThreads * kKGroups) : 0;
     if (nbv + nbk == 0) return cudaSuccess;
     decompress_kernel<D, BITS><<<dim3(nbv + nbk, s.kv_heads), kDecThreads, 0, st>>>(
         L.kq, L.kscale, L.kscales, L.vcodes, L.vnorm, s.ctx, s.ctx_pad, nbv, (uint4*)K_out, (uint4*)V_out,
