@@ -21,6 +21,7 @@
 
 #include <algorithm>
 #include <mutex>
+#include <unordered_map>
 #include <new>
 #include <vector>
 
@@ -149,10 +150,23 @@ struct kvpool {
     std::vector<size_t> off_kq, off_vc, off_vn, off_ks;
     std::vector<unsigned char> compressed;
     std::vector<int> len;  // tokens the layer holds: ctx once compressed; grows by appends
-    // 1 while the layer was written (compress, import, reset) after the last
-    // attend launched on it: that attend must not read the layer before its
-    // grid-dependency wait
-    std::vector<unsigned char> fresh;
+    // Per stream: the layer that this pool's most recent launch on it wrote,
+    // or -1. An attend may read its layer before the grid-dependency wait
+    // (programmatic dependent launch) unless the launch right before it on
+    // the same stream wrote that layer: only the immediately preceding kernel
+    // can still be running when it starts, and that one cannot have started
+    // before the kernels ahead of it finished.
+    std::unordered_map<void*, int> last_write;
+    std::mutex mu;  // last_write: attends may come from several host threads
+    void wrote(void* stream, int layer) {
+        std::lock_guard<std::mutex> g(mu);
+        last_write[stream] = layer;
+    }
+    bool may_read_early(void* stream, int layer) {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = last_write.find(stream);
+        return it == last_write.end() || it->second != layer;
+    }
     std::vector<CUtensorMap> kmaps;
     unsigned char* base = nullptr;
     size_t bytes = 0;
@@ -338,7 +352,6 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
         p->split_ml = reinterpret_cast<float*>(p->base + off_sml);
     }
     p->status = reinterpret_cast<int*>(p->base + off_status);
-    p->fresh.assign(layers, 1);
     p->kmaps.resize(layers);
     for (int l = 0; l < layers; ++l) {
         if (!make_kmap(&p->kmaps[l], p->base + p->off_kq[l], head_dim, (long long)nvec)) {
@@ -369,7 +382,7 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
     if (e != cudaSuccess) return map_cuda(e);
     p->compressed[layer] = 1;
     p->len[layer] = p->ctx;
-    p->fresh[layer] = 1;
+    p->wrote(stream, layer);
     return KVPOOL_OK;
 }
 
@@ -387,7 +400,7 @@ int kvpool_append(kvpool_t* p, int layer, const void* K, const void* V, int n, v
     if (e != cudaSuccess) return map_cuda(e);
     p->len[layer] = len + n;
     p->compressed[layer] = 1;
-    p->fresh[layer] = 1;
+    p->wrote(stream, layer);
     return KVPOOL_OK;
 }
 
@@ -427,7 +440,7 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     a.out = out;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
-    a.early = p->fresh[layer] ? 0 : 1;
+    a.early = p->may_read_early(stream, layer) ? 1 : 0;
     cudaError_t e;
     if (p->k_block) {  // block-scaled K: CUDA-core split kernels, the pool's own scratch
         kvp::AttendScratch scr;
@@ -440,7 +453,7 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
         e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
                                   static_cast<cudaStream_t>(stream));
     }
-    if (e == cudaSuccess) p->fresh[layer] = 0;
+    if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
 }
 
@@ -449,8 +462,10 @@ int kvpool_decompress(kvpool_t* p, int layer, void* K_out, void* V_out, void* st
     if (rc) return rc;
     if ((!K_out && !V_out) || !aligned16(K_out) || !aligned16(V_out)) return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
-    return map_cuda(kvp::launch_decompress(p->shape_of(layer), p->layer(layer), K_out, V_out,
-                                           static_cast<cudaStream_t>(stream)));
+    const cudaError_t e = kvp::launch_decompress(p->shape_of(layer), p->layer(layer), K_out, V_out,
+                                                 static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) p->wrote(stream, -1);
+    return map_cuda(e);
 }
 
 size_t kvpool_pool_bytes(const kvpool_t* p) {
@@ -487,7 +502,6 @@ int kvpool_reset_layer(kvpool_t* p, int layer) {
     if (rc) return rc;
     p->compressed[layer] = 0;
     p->len[layer] = 0;
-    p->fresh[layer] = 1;
     return KVPOOL_OK;
 }
 
@@ -561,7 +575,7 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
                     static_cast<cudaStream_t>(stream));
     if (rc != KVPOOL_OK) return rc;
     rc = map_cuda(kvp::launch_norm_max(p->shape(), p->layer(layer), static_cast<cudaStream_t>(stream)));
-    p->fresh[layer] = 1;
+    p->wrote(stream, layer);
     if (rc == KVPOOL_OK) {
         p->compressed[layer] = 1;
         p->len[layer] = p->ctx;

@@ -73,7 +73,7 @@ struct AttendArgs {
     int tail_max;
     float* out;          // f32 [A][Hq][D]
     float scale_log2;    // softmax scale * log2(e)
-    int early;           // 1: no kernel before this one in the stream writes the layer
+    int early;           // 1: the launch right before this one on its stream did not write the layer
 };
 
 struct AttendScratch {
