@@ -151,6 +151,36 @@ int kvpool_append(kvpool_t* pool, int layer, const void* K, const void* V, int n
 /* Tokens layer `layer` holds (see kvpool_append), or a negative error code. */
 int kvpool_layer_len(const kvpool_t* pool, int layer);
 
+/* Local attention-error estimate of one layer from recently observed queries,
+ * keys and values (CoMixKV article, online sensitivity estimation: no
+ * calibration set, no trial quantisation). The article prints no formula; the
+ * one used: a V head-vector coded at b bits has E|v - v_hat|^2 = D_b |v|^2
+ * (D_b the Lloyd-Max distortion of N(0,1)), so a query row's relative output
+ * error is sqrt(D_b) * r with r = sqrt(sum_t p_t^2 |v_t|^2) / |sum_t p_t v_t|
+ * over the agent's recent tokens (p the softmax of the row's logits, scaled
+ * by softmax_scale, 0 meaning 1/sqrt(head_dim)). Writes r of every (agent,
+ * query head) row to row_r (device float [agents * q_heads]) and their mean,
+ * the layer's sensitivity s, to *score (device float); an agent with no
+ * recent token contributes 0. Q: bf16 [agents][q_heads][head_dim]; recent:
+ * the agents' recent tokens in the kvpool_tail_t layout (T_max <= 12288).
+ * Asynchronous on `stream`; needs no pool. */
+int kvpool_sensitivity(const void* Q, int agents, int q_heads, const kvpool_tail_t* recent, int kv_heads,
+                       int head_dim, float softmax_scale, float* row_r, float* score, void* stream);
+
+/* Joint V bit widths (CoMixKV article: the controller combines sensitivity,
+ * capacity and byte-level cost and picks every layer's width within one
+ * budget). Host only. Chooses bits[l] in {2, 3, 4} minimising
+ * sum_l D_{bits[l]} * sens[l]^2 subject to sum_l cost[l] * bits[l] <= budget,
+ * exactly (dynamic programming over the costs in units of their greatest
+ * common divisor); among allocations of equal error the one of fewer bytes,
+ * then the one with the smaller width at the first layer where they differ.
+ * cost[l] >= 1: the layer's V bytes per bit of width (kv_heads * tokens *
+ * head_dim / 8 for a pool layer). KVPOOL_ERR_INVALID_ARG when even 2 bits
+ * everywhere exceed the budget, KVPOOL_ERR_UNSUPPORTED when the table would
+ * exceed 2^26 entries. The widths apply to layers created or appended later
+ * (a pool's layer widths are fixed at kvpool_create). */
+int kvpool_allocate_bits(int layers, const double* sens, const int64_t* cost, int64_t budget, uint8_t* bits);
+
 /* Free all device memory of the pool. Waits for the device first. NULL is a
  * no-op. */
 void kvpool_destroy(kvpool_t* pool);

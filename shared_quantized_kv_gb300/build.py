@@ -24,8 +24,10 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvpool.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
-          "-I", INCLUDE, "-I", CSRC]
+# host code never contracts a*b+c into an FMA (the bit allocator's choices
+# follow a fixed float64 order, on x86 and Arm alike)
+CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]
 # the files whose float arithmetic decides codes also forbid FMA contraction
 EXACT = {"encode.cu", "decompress.cu"}
 

@@ -17,6 +17,8 @@
 // ctx_pad rounds the token axis up to a multiple of 128 so tiles never leave a
 // layer; the padding is zeroed once and never counted as tokens.
 #include <math.h>
+
+#include <cmath>
 #include <string.h>
 
 #include <algorithm>
@@ -138,6 +140,26 @@ const Codebook& codebook(int bits) {
     std::call_once(g_books_once, build_books);
     return g_books[bits];
 }
+
+// Mean squared error of the Lloyd-Max quantiser for N(0,1) at `bits` bits,
+// in closed form per cell: E[(X - y)^2; a < X < b] = P (1 + y^2)
+// - 2 y (pdf(a) - pdf(b)) + (a pdf(a) - b pdf(b)); twice the positive half.
+double lm_distortion(int bits) {
+    const int L = 1 << bits, K = L / 2;
+    double y[8];
+    lloyd_max(L, y);
+    double total = 0.0;
+    for (int k = 0; k < K; ++k) {
+        const double a = (k == 0) ? 0.0 : 0.5 * (y[k - 1] + y[k]);
+        const bool last = k + 1 == K;
+        const double b = last ? 0.0 : 0.5 * (y[k] + y[k + 1]);
+        const double P = ntail(a) - (last ? 0.0 : ntail(b));
+        const double pa = npdf(a), pb = last ? 0.0 : npdf(b);
+        total += P * (1.0 + y[k] * y[k]) - 2.0 * y[k] * (pa - pb) + (a * pa - (last ? 0.0 : b * pb));
+    }
+    return 2.0 * total;
+}
+
 
 }  // namespace kvp
 
@@ -595,6 +617,85 @@ int kvpool_export_kscales(const kvpool_t* p, int layer, float* kscales, void* st
     return map_cuda(cudaMemcpy2DAsync(kscales, T * per, L.kscales, (size_t)p->ctx_pad * per,
                                       T * per, (size_t)p->kv_heads, cudaMemcpyDefault,
                                       static_cast<cudaStream_t>(stream)));
+}
+
+int kvpool_sensitivity(const void* Q, int agents, int q_heads, const kvpool_tail_t* recent, int kv_heads,
+                       int head_dim, float softmax_scale, float* row_r, float* score, void* stream) {
+    if (!Q || !recent || !row_r || !score || agents < 1 || kv_heads < 1 || q_heads < kv_heads ||
+        q_heads % kv_heads || (head_dim != 64 && head_dim != 128))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (recent->T_max < 0 || recent->T_max > 12288 ||
+        (recent->T_max > 0 && (!recent->K || !recent->V || !recent->len)))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!(softmax_scale >= 0.0f) || isinf(softmax_scale)) return KVPOOL_ERR_INVALID_ARG;
+    if (recent->T_max == 0) {  // no recent token: every row counts 0
+        cudaError_t e = cudaMemsetAsync(score, 0, sizeof(float), static_cast<cudaStream_t>(stream));
+        return map_cuda(e);
+    }
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    return map_cuda(kvp::launch_sensitivity(Q, agents, q_heads, kv_heads, head_dim, recent->K, recent->V,
+                                            recent->len, recent->T_max, scale, row_r, score,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int kvpool_allocate_bits(int layers, const double* sens, const int64_t* cost, int64_t budget, uint8_t* bits) {
+    if (layers < 1 || !sens || !cost || !bits || budget < 0) return KVPOOL_ERR_INVALID_ARG;
+    int64_t g = 0;
+    for (int l = 0; l < layers; ++l) {
+        if (cost[l] < 1 || !(sens[l] >= 0.0) || std::isinf(sens[l])) return KVPOOL_ERR_INVALID_ARG;
+        int64_t a = g, b = cost[l];
+        while (b) {
+            const int64_t t = a % b;
+            a = b;
+            b = t;
+        }
+        g = a;
+    }
+    // integer units: every cost is a multiple of g
+    std::vector<int64_t> c(layers), rest(layers + 1, 0);
+    for (int l = 0; l < layers; ++l) c[l] = cost[l] / g;
+    for (int l = layers - 1; l >= 0; --l) rest[l] = rest[l + 1] + 2 * c[l];
+    const int64_t B = budget / g;
+    if (rest[0] > B) return KVPOOL_ERR_INVALID_ARG;  // even 2 bits everywhere do not fit
+    const int64_t need = std::min<int64_t>(B, 4 * rest[0] / 2);  // more units than 4 bits everywhere never matter
+    if ((int64_t)(layers + 1) * (need + 1) > (int64_t)1 << 26) return KVPOOL_ERR_UNSUPPORTED;
+    const double D[3] = {kvp::lm_distortion(2), kvp::lm_distortion(3), kvp::lm_distortion(4)};
+    // err/bytes/choice of layers l.. with u units left (u in [0, need])
+    const size_t W = (size_t)need + 1;
+    std::vector<double> err((size_t)(layers + 1) * W, 0.0);
+    std::vector<int64_t> by((size_t)(layers + 1) * W, 0);
+    std::vector<uint8_t> pick((size_t)layers * W, 0);
+    for (int l = layers - 1; l >= 0; --l) {
+        for (int64_t u = 0; u <= need; ++u) {
+            bool have = false;
+            double be = 0.0;
+            int64_t bb = 0;
+            uint8_t bbits = 0;
+            for (int b = 2; b <= 4; ++b) {
+                const int64_t cc = c[l] * b;
+                if (cc + rest[l + 1] > u) continue;
+                const double s2 = sens[l] * sens[l];
+                const double e = D[b - 2] * s2 + err[(size_t)(l + 1) * W + (size_t)(u - cc)];
+                const int64_t y = cc + by[(size_t)(l + 1) * W + (size_t)(u - cc)];
+                if (!have || e < be || (e == be && y < bb)) {
+                    have = true;
+                    be = e;
+                    bb = y;
+                    bbits = (uint8_t)b;
+                }
+            }
+            err[(size_t)l * W + u] = be;
+            by[(size_t)l * W + u] = bb;
+            pick[(size_t)l * W + u] = bbits;
+        }
+    }
+    int64_t u = need;
+    for (int l = 0; l < layers; ++l) {
+        const uint8_t b = pick[(size_t)l * W + u];
+        bits[l] = b;
+        u -= c[l] * b;
+    }
+    return KVPOOL_OK;
 }
 
 const char* kvpool_strerror(int code) {

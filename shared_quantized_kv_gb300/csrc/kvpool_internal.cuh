@@ -91,6 +91,15 @@ cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const Attend
 cudaError_t launch_attend_tc(const Shape& s, const LayerBufs& L, const AttendArgs& a, int* status,
                              int sm_count, cudaStream_t st);
 
+// Local attention-error estimate of one layer (see sensitivity.cu): r per
+// (agent, query head) row into row_r, their mean into *score.
+cudaError_t launch_sensitivity(const void* Q, int agents, int q_heads, int kv_heads, int head_dim,
+                               const void* tK, const void* tV, const int32_t* tlen, int T_max, float scale,
+                               float* row_r, float* score, cudaStream_t st);
+
+// Mean squared error of the library's Lloyd-Max quantiser for N(0,1).
+double lm_distortion(int bits);
+
 // Largest V norm of a layer (for layers loaded with kvpool_import_layer).
 cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st);
 

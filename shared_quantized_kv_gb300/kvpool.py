@@ -52,6 +52,11 @@ _SIGS = {
     "kvpool_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_void_p]),
     "kvpool_layer_len": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
+    "kvpool_sensitivity": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_allocate_bits": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                                            ctypes.c_void_p]),
     "kvpool_destroy": (None, [ctypes.c_void_p]),
     "kvpool_compress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                        ctypes.c_void_p, ctypes.c_void_p]),
@@ -125,6 +130,39 @@ def codebook(bits: int):
     m = np.zeros((1 << bits) - 1, np.float32)
     _check(_lib().kvpool_codebook(bits, c.ctypes.data, m.ctypes.data), "kvpool_codebook")
     return c, m
+
+
+def sensitivity(Q, recent, kv_heads, softmax_scale=0.0, stream=None):
+    """A layer's local attention-error estimate s (float) and the per-row
+    values r (float32 [agents * q_heads], device) from recent tokens: Q bf16
+    [agents, q_heads, d]; recent = (K, V, lens) with K, V bf16 [agents,
+    kv_heads, T_max, d] and lens int32 [agents] (device)."""
+    import torch
+
+    A, Hq, d = Q.shape
+    K, V, lens = recent
+    t = Tail(_dev_ptr(K, torch.bfloat16, "recent K").value, _dev_ptr(V, torch.bfloat16, "recent V").value,
+             _dev_ptr(lens, torch.int32, "recent len").value, K.shape[2])
+    rows = torch.empty(A * Hq, dtype=torch.float32, device=Q.device)
+    score = torch.empty(1, dtype=torch.float32, device=Q.device)
+    _check(_lib().kvpool_sensitivity(_dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, ctypes.byref(t), kv_heads, d,
+                                     softmax_scale, rows.data_ptr(), score.data_ptr(), _stream_ptr(stream)),
+           "kvpool_sensitivity")
+    return float(score.cpu()[0]), rows
+
+
+def allocate_bits(sens, cost, budget):
+    """Per-layer V widths (list of 2, 3, 4) minimising sum D_b s^2 within
+    sum cost * bits <= budget (host only)."""
+    import numpy as np
+
+    L = len(sens)
+    s = np.ascontiguousarray(sens, dtype=np.float64)
+    c = np.ascontiguousarray(cost, dtype=np.int64)
+    out = np.zeros(L, dtype=np.uint8)
+    _check(_lib().kvpool_allocate_bits(L, s.ctypes.data, c.ctypes.data, int(budget), out.ctypes.data),
+           "kvpool_allocate_bits")
+    return [int(b) for b in out]
 
 
 class KVPool:
