@@ -47,6 +47,16 @@ def _peaks():
     return FALLBACK_HBM, "fallback"
 
 
+def workload_config(w, ws, k_block):
+    """The workload part of both arms' `config` (identical for the GPU arm and
+    the reference arm)."""
+    return {"workload": w.name, "k_scales": "per 32 elements" if k_block else "per layer",
+            "layers": w.layers, "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim,
+            "ctx": w.ctx, "agents": w.agents, "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
+            "step": "compress+attend+decompress, all layers",
+            "parallelism": f"replicas x{ws} (independent pools, no collective)"}
+
+
 def max_over_ranks(step_ms, ph_ms, phases, device=None):
     """(step time, per-phase times) as the maximum over the ranks of the
     default process group (unchanged when no group is initialised). Ranks are
@@ -286,13 +296,8 @@ def run_gpu(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/u3+f32",
         "data": "synthetic (seeded; bf16 K/V with LogNormal(0,0.5) channel std and 1% x10 outlier "
                 "channels, Q ~ N(0,1))",
-        "config": {"workload": w.name, "k_scales": "per 32 elements" if args.k_block else "per layer",
-                   "layers": L, "kv_heads": w.kv_heads, "q_heads": w.q_heads,
-                   "head_dim": w.head_dim, "ctx": w.ctx, "agents": A,
-                   "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
-                   "step": "compress+attend+decompress, all layers",
-                   "l2": "flushed (512 MiB write) before every phase, outside the timed events",
-                   "parallelism": f"replicas x{ws} (independent pools, no collective)"},
+        "config": dict(workload_config(w, ws, args.k_block),
+                       l2="flushed (512 MiB write) before every phase, outside the timed events"),
         "phases": ph_info,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ph_info[dom]["GB_per_s"],
                      "peak": peak, "unit": "GB/s", "frac": ph_info[dom]["hbm_frac"],
@@ -306,7 +311,7 @@ def run_gpu(args):
         "e2e": e2e,
     }
     if rank == 0 and not args.no_cpu:
-        line["cpu_baseline"] = cpu_baseline(w)
+        line["cpu_baseline"] = cpu_baseline(w, k_block=args.k_block)
     if rank == 0:
         print(json.dumps(line), flush=True)
     pool.close()
@@ -389,7 +394,7 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
 
 # ------------------------------------------------------------------ CPU legs
 
-def _oracle_sample(name: str, layers: int) -> dict:
+def _oracle_sample(name: str, layers: int, k_block: int = 0) -> dict:
     """Time the oracle (as it stands) on the first `layers` layers of the
     workload: encode, float64 attention for all agents, decompress. Runs in a
     fresh interpreter with one BLAS thread."""
@@ -410,7 +415,7 @@ for l in range({layers}):
         import numpy as np
         tail = (Kt, Vt, np.full(w.agents, w.tail_len(w.decode_steps - 1)))
     t0 = time.perf_counter()
-    enc = codec.encode_layer(K, V, w.layer_bits(l))
+    enc = codec.encode_layer(K, V, w.layer_bits(l), k_block={k_block})
     Kh, Vh = attention.dequantise_f64(enc)
     attention.attend_f64(Kh, Vh, Q, tail)
     codec.decompress_layer(enc)
@@ -426,8 +431,8 @@ print(json.dumps({{"seconds": t, "layers": {layers}}}))
     return json.loads(r.stdout.strip().splitlines()[-1])
 
 
-def cpu_baseline(w, layers: int = 1) -> dict:
-    res = _oracle_sample(w.name, layers)
+def cpu_baseline(w, layers: int = 1, k_block: int = 0) -> dict:
+    res = _oracle_sample(w.name, layers, k_block)
     per_step = res["seconds"] / layers * w.layers
     return {"value": round(w.agents / per_step, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
             "sample": f"{layers} of {w.layers} layers (encode + float64 attention of all "
@@ -442,12 +447,12 @@ def run_reference(args):
     from shared_quantized_kv_gb300 import workloads as wl
 
     w = wl.WORKLOADS[args.workload]
-    _oracle_sample(w.name, 1)  # warm-up of the interpreter and tables
+    _oracle_sample(w.name, 1, args.k_block)  # warm-up of the interpreter and tables
     times = []
     for _ in range(args.warmup):
-        _oracle_sample(w.name, 1)
+        _oracle_sample(w.name, 1, args.k_block)
     for _ in range(args.steps):
-        r = _oracle_sample(w.name, 1)
+        r = _oracle_sample(w.name, 1, args.k_block)
         times.append(r["seconds"] * w.layers)  # one layer per step, scaled to all layers
     step_s = statistics.mean(times)
     value = w.agents / step_s
@@ -456,9 +461,8 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32 encode / f64 attention", "data": "synthetic (seeded)",
-        "config": {"workload": w.name, "layers": w.layers, "kv_heads": w.kv_heads,
-                   "q_heads": w.q_heads, "head_dim": w.head_dim, "ctx": w.ctx, "agents": w.agents,
-                   "step": "compress+attend+decompress, all layers (1 layer timed per step, scaled)"},
+        "config": dict(workload_config(w, ws, args.k_block),
+                       timing="one layer per step on the host CPU, scaled to all layers"),
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "1 layer per step scaled to all layers; one thread"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
