@@ -32,17 +32,19 @@ __device__ __forceinline__ uint32_t bf16x2_bits(float lo, float hi) {
     const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-// the int8 in byte k of w as a float (exact: 1.5 * 2^23 + q has q in its low bits)
-__device__ __forceinline__ float i8_to_f(uint32_t w, int k) {
-    const int q = (int)(int8_t)((w >> (8 * k)) & 0xFF);
-    return __fsub_rn(__int_as_float(0x4B400000 + q), 12582912.0f);
+// the int8s in bytes k, k + 1 of w as floats (exact: 1.5 * 2^23 + q has q in
+// its low bits); one paired subtraction
+__device__ __forceinline__ float2 i8x2_to_f2(uint32_t w, int k) {
+    const int q0 = (int)(int8_t)((w >> (8 * k)) & 0xFF), q1 = (int)(int8_t)((w >> (8 * k + 8)) & 0xFF);
+    return __fadd2_rn(make_float2(__int_as_float(0x4B400000 + q0), __int_as_float(0x4B400000 + q1)),
+                      make_float2(-12582912.0f, -12582912.0f));
 }
 
 // One launch for both halves, grid (blocks, kv heads): the first nbv blocks of
 // each head materialise V (D/32 threads per head-vector), the rest K (16
 // elements per thread).
 template <int D, int BITS>
-__global__ void __launch_bounds__(kDecThreads)
+__global__ void __launch_bounds__(kDecThreads, 5)  // five CTAs per SM: both halves in one wave
 decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscale,
                   const float* __restrict__ kscales,
                   const uint8_t* __restrict__ vcodes, const float* __restrict__ vnorm, int ctx,
@@ -77,8 +79,9 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
             uint32_t o[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float k0 = i8_to_f(w[j / 2], 2 * (j % 2)), k1 = i8_to_f(w[j / 2], 2 * (j % 2) + 1);
-                o[j] = bf16x2_bits(__fmul_rn(k0, sc[u]), __fmul_rn(k1, sc[u]));
+                const float2 k = i8x2_to_f2(w[j / 2], 2 * (j % 2));
+                const float2 v = __fmul2_rn(k, make_float2(sc[u], sc[u]));
+                o[j] = bf16x2_bits(v.x, v.y);
             }
             uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
             out[0] = make_uint4(o[0], o[1], o[2], o[3]);
@@ -116,17 +119,23 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     const uint4* c8 = reinterpret_cast<const uint4*>(codes8 + (tid / TPV) * D + lt * 32);
     const uint4 ca = c8[0], cb8 = c8[1];
     const uint32_t cw[8] = {ca.x, ca.y, ca.z, ca.w, cb8.x, cb8.y, cb8.z, cb8.w};
-    float x[32];
+    // the float steps run on coordinate pairs (2i, 2i + 1): one instruction,
+    // two IEEE round-to-nearest operations in the encoder's order
+    float2 x[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) x[i] = cen[(cw[i / 4] >> (8 * (i % 4))) & 0xFF];
+    for (int i = 0; i < 16; ++i)
+        x[i] = make_float2(cen[(cw[i / 2] >> (16 * (i % 2))) & 0xFF], cen[(cw[i / 2] >> (16 * (i % 2) + 8)) & 0xFF]);
+    // FWHT stages h = 1 (inside each pair), 2 ... 16 (pairs i and i + h/2)
 #pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
+    for (int i = 0; i < 16; ++i) x[i] = make_float2(__fadd_rn(x[i].x, x[i].y), __fsub_rn(x[i].x, x[i].y));
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            if (!(i & h)) {
-                const float a = x[i], b = x[i + h];
-                x[i] = __fadd_rn(a, b);
-                x[i + h] = __fsub_rn(a, b);
+    for (int hp = 1; hp < 16; hp <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if (!(i & hp)) {
+                const float2 a = x[i], b = x[i + hp];
+                x[i] = __fadd2_rn(a, b);
+                x[i + hp] = __fadd2_rn(a, make_float2(-b.x, -b.y));  // a - b, exact negation
             }
         }
     }
@@ -136,23 +145,25 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
         // lower slice: own + partner; upper slice: partner - own (one
         // rounding either way, exactly the add or the subtraction)
         const float sg = (lt & off) ? -1.0f : 1.0f;
+        const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
-            x[i] = __fmaf_rn(sg, x[i], o);
+        for (int i = 0; i < 16; ++i) {
+            const float2 o = make_float2(__shfl_xor_sync(gmask, x[i].x, off, TPV),
+                                         __shfl_xor_sync(gmask, x[i].y, off, TPV));
+            x[i] = __ffma2_rn(sg2, x[i], o);
         }
     }
     if (!live) return;
     const float inv_d = 1.0f / (float)D;  // a power of two: exact
+    const float2 n2 = make_float2(n, n), d2 = make_float2(inv_d, inv_d);
     uint4* out = Vout + (head * ctx + t) * (D / 8) + lt * 4;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t o[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const float lo = __fmul_rn(__fmul_rn(x[8 * q + 2 * j], n), inv_d);
-            const float hi = __fmul_rn(__fmul_rn(x[8 * q + 2 * j + 1], n), inv_d);
-            o[j] = bf16x2_bits(lo, hi);
+            const float2 v = __fmul2_rn(__fmul2_rn(x[4 * q + j], n2), d2);
+            o[j] = bf16x2_bits(v.x, v.y);
         }
         out[q] = make_uint4(o[0], o[1], o[2], o[3]);
     }

@@ -7,31 +7,31 @@
 //      for N(0,1) per rotated coordinate (3 bits; 2 or 4 bits per layer in the
 //      CoMixKV article's mixed-precision setting).
 //
-// One cooperative kernel per layer; every CTA is resident at once. An item is
-// 32 (head_dim 128) or 64 (head_dim 64) consecutive tokens of one KV head:
-// 8 KB of K and 8 KB of V, brought into shared memory by bulk copies (one
-// mbarrier per tile). CTA i takes items i, i + G, ... (G = grid size); all
-// copies of the first item are requested at launch.
-//   phase A: max|K| over the CTA's items (the first from its tile, the
-//     others straight from global memory), one atomic per CTA into the
-//     launch's word, then a grid barrier: a 64-bit counter that only grows
-//     (launch g waits for (g + 1) * G arrivals; launch g raises kmax[g & 1]
-//     and clears the other word for launch g + 1), so nothing is
-//     reset between launches. The barrier comes early, while the CTAs are
-//     still nearly in step.
-//   phase B, per item: s = max|K| / 127, q = clamp(rint(k / s), -127, 127)
-//     from the K tile: k / s is formed as k * (1/s) and rounded by the
-//     1.5 * 2^23 addition; where the product lies within 2^-15 of a
-//     half-integer (the two could round to different integers) the chunk's
-//     8 elements are recomputed with IEEE divisions. Then per head-vector,
-//     D/32 threads with 32 coordinates each: the norm by the pairwise tree
-//     (the first levels cross threads by shuffles), the FWHT (stages h < 32
-//     in registers, h = 32, 64 by shfl.xor and one exact FMA), one float32
-//     threshold per midpoint (m_j * n), the codes by a branchless binary
-//     search over the sorted thresholds, regrouped through shared memory
-//     into the pool layout: per group of 32 tokens, one packed sequence per
-//     coordinate (the 32 tokens' codes in token order, 4*BITS bytes). The
-//     next item's copies are requested as soon as the tiles are in registers.
+// Two kernels per layer. The max|K| kernel reduces slices of the K tensor to
+// partial maxima and releases the encode kernel at once (programmatic
+// dependent launch), so the encode kernel's V work runs beside it. In the
+// encode kernel an item is 32 (head_dim 128) or 64 (head_dim 64) consecutive
+// tokens of one KV head: 8 KB of K and 8 KB of V, brought into shared memory
+// by bulk copies (one mbarrier per tile). CTA i takes items i, i + G, ...
+// (G = grid size); the first item's copies are requested at launch (K and V
+// are inputs no earlier kernel writes).
+//   V, per item and head-vector, D/32 threads with 32 coordinates each: the
+//     norm by the pairwise tree (the first levels cross threads by shuffles),
+//     the FWHT (stages h < 32 in registers, h = 32, 64 by shfl.xor and one
+//     exact FMA), one float32 threshold per midpoint (m_j * n), the codes by a
+//     branchless binary search over the sorted thresholds, regrouped through
+//     shared memory into the pool layout: per group of 32 tokens, one packed
+//     sequence per coordinate (the 32 tokens' codes in token order, 4*BITS
+//     bytes).
+//   K: before its first K codes the kernel waits for the max|K| kernel and
+//     reduces the partial maxima: s = max|K| / 127, and per element
+//     q = clamp(rint(k / s), -127, 127) from the K tile: k / s is formed as
+//     k * (1/s) and rounded by the 1.5 * 2^23 addition; where the product lies
+//     within 2^-15 of a half-integer (the two could round to different
+//     integers) the chunk's 8 elements are recomputed with IEEE divisions.
+//     Block-scaled pools (one scale per 32 elements) take each block's scale
+//     from its own maximum and run no max|K| kernel.
+// The next item's copies are requested as soon as a tile is in registers.
 // Every float operation that decides a code uses an explicit IEEE round-to-
 // nearest intrinsic, in the fixed order of the definition, so the codes are
 // reproducible bit for bit (no contraction into FMA, no approximate division).
@@ -79,22 +79,27 @@ __device__ __forceinline__ uint32_t bucket(float x, const float (&t)[16]) {
     }
 }
 
-// int8 codes of 8 bf16 values (one 16-byte chunk) as two little-endian words
+// int8 codes of 8 bf16 values (one 16-byte chunk) as two little-endian words;
+// the float steps run on element pairs (two IEEE round-to-nearest operations
+// per instruction)
 __device__ __forceinline__ uint2 quant8(uint4 u, float s, float r) {
     constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: adding it rounds |y| < 2^22 to an integer
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const float2 r2 = make_float2(r, r), m2 = make_float2(kMagic, kMagic), nm2 = make_float2(-kMagic, -kMagic);
     uint32_t b[8];
     bool amb = false;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const float k = (j & 1) ? bf_hi(w[j / 2]) : bf_lo(w[j / 2]);
+    for (int j = 0; j < 4; ++j) {
         // k * (1/s) is within ~1.5 ulp of k / s; unless that lands within
         // 2^-15 of a half-integer both round to the same integer
-        const float y = __fmul_rn(k, r);
-        const float t = __fadd_rn(y, kMagic);                // kMagic + rint(y), ties to even
-        const float e = __fsub_rn(y, __fsub_rn(t, kMagic));  // y - rint(y), exact
-        amb |= !(fabsf(e) < 0.499969482421875f);             // 0.5 - 2^-15 (also taken for NaN)
-        b[j] = __float_as_uint(t);                           // low byte: rint(y) mod 256
+        const float2 y = __fmul2_rn(make_float2(bf_lo(w[j]), bf_hi(w[j])), r2);
+        const float2 t = __fadd2_rn(y, m2);                      // kMagic + rint(y), ties to even
+        const float2 i = __fadd2_rn(t, nm2);                     // rint(y), exact
+        const float2 e = __fadd2_rn(y, make_float2(-i.x, -i.y));  // y - rint(y), exact
+        amb |= !(fabsf(e.x) < 0.499969482421875f);               // 0.5 - 2^-15 (also taken for NaN)
+        amb |= !(fabsf(e.y) < 0.499969482421875f);
+        b[2 * j] = __float_as_uint(t.x);  // low byte: rint(y) mod 256
+        b[2 * j + 1] = __float_as_uint(t.y);
     }
     if (amb) {
 #pragma unroll
@@ -205,7 +210,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
         const int ntok = min(VPI, ctx - t0);
         if (ok && !ptx::mbar_wait(barV, phase, kEncWaitNs)) ok = false;
         const bool live = tl < ntok;
-        float x[32];
+        float2 x[16];  // coordinates (2i, 2i + 1) of this thread's slice
         {
             uint32_t dep = 0;  // depends on every word this thread reads from the V tile
             const uint4* vs = reinterpret_cast<const uint4*>(sV + tl * (D * 2) + lt * 64);
@@ -215,10 +220,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                 dep ^= vv.x ^ vv.y ^ vv.z ^ vv.w;
                 const uint32_t w[4] = {vv.x, vv.y, vv.z, vv.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    x[c * 8 + 2 * j] = bf_lo(w[j]);
-                    x[c * 8 + 2 * j + 1] = bf_hi(w[j]);
-                }
+                for (int j = 0; j < 4; ++j) x[c * 4 + j] = make_float2(bf_lo(w[j]), bf_hi(w[j]));
             }
             // The next item's copy overwrites the tile. A barrier does not
             // wait for shared-memory loads still in flight, and the copy
@@ -233,37 +235,44 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
             issueV(it + G);
         }
 
+        // The float steps below run on coordinate pairs (2i, 2i + 1): one
+        // instruction, two IEEE round-to-nearest operations in the same order.
         // norm: pairwise tree sq_i += sq_{i+w}, w = D/2, ..., 1 (squares exact)
-        float sq[32];
+        float2 sq[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sq[i] = __fmul_rn(x[i], x[i]);
+        for (int i = 0; i < 16; ++i) sq[i] = __fmul2_rn(x[i], x[i]);
         // levels w >= 32 pair slices lt and lt + w/32 (the lower slice keeps the sum)
 #pragma unroll
         for (int w = D / 2; w >= 32; w >>= 1) {
             const int off = w / 32;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float o = __shfl_down_sync(gmask, sq[i], off, TPV);
-                sq[i] = __fadd_rn(sq[i], o);  // meaningful on slices lt < off
+            for (int i = 0; i < 16; ++i) {
+                const float2 o = make_float2(__shfl_down_sync(gmask, sq[i].x, off, TPV),
+                                             __shfl_down_sync(gmask, sq[i].y, off, TPV));
+                sq[i] = __fadd2_rn(sq[i], o);  // meaningful on slices lt < off
             }
         }
+        // levels w = 16, ..., 2: element i + w is pair i/2 + w/2
 #pragma unroll
-        for (int w = 16; w >= 1; w >>= 1) {
+        for (int w = 16; w >= 2; w >>= 1) {
 #pragma unroll
-            for (int i = 0; i < w; ++i) sq[i] = __fadd_rn(sq[i], sq[i + w]);
+            for (int i = 0; i < w / 2; ++i) sq[i] = __fadd2_rn(sq[i], sq[i + w / 2]);
         }
-        const float n = __shfl_sync(gmask, __fsqrt_rn(sq[0]), lane - lt);  // slice 0 holds the sum
+        const float n = __shfl_sync(gmask, __fsqrt_rn(__fadd_rn(sq[0].x, sq[0].y)), lane - lt);  // slice 0 holds the sum
         if (live) nmax = max(nmax, __float_as_uint(n));
 
-        // FWHT, stages h = 1, 2, ..., D/2, lower index first
+        // FWHT, stages h = 1, 2, ..., D/2, lower index first; h = 1 inside
+        // each pair, h = 2 ... 16 between pairs i and i + h/2
 #pragma unroll
-        for (int hh = 1; hh < 32; hh <<= 1) {
+        for (int i = 0; i < 16; ++i) x[i] = make_float2(__fadd_rn(x[i].x, x[i].y), __fsub_rn(x[i].x, x[i].y));
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                if (!(i & hh)) {
-                    const float a = x[i], b = x[i + hh];
-                    x[i] = __fadd_rn(a, b);
-                    x[i + hh] = __fsub_rn(a, b);
+        for (int hp = 1; hp < 16; hp <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                if (!(i & hp)) {
+                    const float2 a = x[i], b = x[i + hp];
+                    x[i] = __fadd2_rn(a, b);
+                    x[i + hp] = __fadd2_rn(a, make_float2(-b.x, -b.y));  // a - b, exact negation
                 }
             }
         }
@@ -273,10 +282,12 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
             // lower slice: own + partner; upper slice: partner - own (one
             // rounding either way, exactly the add or the subtraction)
             const float sg = (lt & off) ? -1.0f : 1.0f;
+            const float2 sg2 = make_float2(sg, sg);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float o = __shfl_xor_sync(gmask, x[i], off, TPV);
-                x[i] = __fmaf_rn(sg, x[i], o);
+            for (int i = 0; i < 16; ++i) {
+                const float2 o = make_float2(__shfl_xor_sync(gmask, x[i].x, off, TPV),
+                                             __shfl_xor_sync(gmask, x[i].y, off, TPV));
+                x[i] = __ffma2_rn(sg2, x[i], o);
             }
         }
 
@@ -289,7 +300,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
         for (int w = 0; w < 8; ++w) cw[w] = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-            const uint32_t code = live ? bucket<L>(x[i], tau) : 0u;
+            const uint32_t code = live ? bucket<L>((i & 1) ? x[i / 2].y : x[i / 2].x, tau) : 0u;
             cw[i / 4] |= code << (8 * (i % 4));
         }
         uint4* c8 = reinterpret_cast<uint4*>(codes8 + tl * D + lt * 32);
