@@ -3,8 +3,10 @@
 One step = one pass of the whole path over one batch of synthetic input on
 the Llama-3-8B-shaped workload (32 layers, 8 KV heads, 32 query heads,
 head_dim 128, 4096 shared-context tokens, 15 agents x 1 decode query, int8 K,
-3-bit V): compress every layer (write-once encode), attend every layer for all
-agents, decompress every layer (the per-agent materialisation path). The three
+3-bit V): compress every layer (write-once encode of the shared context, all
+layers in one call), attend every layer for all agents (one call per layer:
+a layer's queries depend on the layer before), decompress every layer (the
+per-agent materialisation path, all layers in one call). The three
 phases are each captured once as a CUDA graph and replayed; CUDA events around
 each replay give the per-phase device time, and L2 is flushed (a 512 MiB
 write) before every phase, outside the events.
@@ -55,6 +57,23 @@ def workload_config(w, ws, k_block):
             "ctx": w.ctx, "agents": w.agents, "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
             "step": "compress+attend+decompress, all layers",
             "parallelism": f"replicas x{ws} (independent pools, no collective)"}
+
+
+def launches_per_step(w, k_block, per_layer_calls, batch=32):
+    """The library's kernel launches in one step, by phase. Compress: a max|K|
+    kernel and an encode kernel per layer, or, for all layers in one call, one
+    max|K| kernel and one encode kernel per V width per 32 layers. Attend: the
+    tensor-core kernel per layer, or the split and combine kernels (block-
+    scaled K). Decompress: one kernel per layer, or one per V width per 32
+    layers."""
+    bits = w.bits_list()
+    chunks = [bits[i:i + batch] for i in range(0, len(bits), batch)]
+    widths = sum(len(set(c)) for c in chunks)
+    if per_layer_calls:
+        comp, dec = 2 * len(bits), len(bits)
+    else:
+        comp, dec = len(chunks) + widths, widths
+    return {"compress": comp, "attend": len(bits) * (2 if k_block else 1), "decompress": dec}
 
 
 def max_over_ranks(step_ms, ph_ms, phases, device=None):
@@ -198,18 +217,27 @@ def run_gpu(args):
     Vd = [torch.empty_like(V[0]) for _ in range(L)]
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
 
-    def compress():
-        for l in range(L):
-            pool.reset_layer(l)
-            pool.compress(l, K[l], V[l])
+    layers = list(range(L))
 
-    def attend():
-        for l in range(L):
+    def compress():
+        for l in layers:
+            pool.reset_layer(l)
+        if args.per_layer_calls:
+            for l in layers:
+                pool.compress(l, K[l], V[l])
+        else:  # the whole shared context in one call
+            pool.compress_layers(layers, K, V)
+
+    def attend():  # per layer: layer l + 1's queries come from layer l's output
+        for l in layers:
             pool.attend(l, Q[l], out[l], tail[l] if tail else None)
 
     def decompress():
-        for l in range(L):
-            pool.decompress(l, Kd[l], Vd[l])
+        if args.per_layer_calls:
+            for l in layers:
+                pool.decompress(l, Kd[l], Vd[l])
+        else:
+            pool.decompress_layers(layers, Kd, Vd)
 
     # eager once (state + correctness of the calls), then capture each phase
     compress(); attend(); decompress()
@@ -267,6 +295,7 @@ def run_gpu(args):
     ph_ms = {ph: v / args.steps for ph, v in ph_ms.items()}
     step_ms, ph_ms = max_over_ranks(sum(ph_ms.values()), ph_ms, phases, dev if ws > 1 else None)
 
+    launches = launches_per_step(w, args.k_block, args.per_layer_calls)
     # algorithmic bytes per layer
     nvec = w.kv_heads * w.ctx
     kv_in = 2 * nvec * w.head_dim * 2
@@ -281,7 +310,7 @@ def run_gpu(args):
         gbs = algo[ph] / per_call_s / 1e9
         ph_info[ph] = {"ms_per_step": round(ph_ms[ph], 4), "us_per_layer": round(per_call_s * 1e6, 3),
                        "algo_bytes_per_layer": int(algo[ph]), "GB_per_s": round(gbs, 1),
-                       "hbm_frac": round(gbs / peak, 4)}
+                       "hbm_frac": round(gbs / peak, 4), "launches_per_step": launches[ph]}
     ph_info["attend"]["agent_steps_per_s"] = round(A * ws / (ph_ms["attend"] / 1e3), 1)
     dom = max(phases, key=lambda p: ph_ms[p])
     dom_file = {"compress": "encode.cu", "attend": "attend_tc_impl.cuh", "decompress": "decompress.cu"}[dom]
@@ -297,15 +326,15 @@ def run_gpu(args):
         "data": "synthetic (seeded; bf16 K/V with LogNormal(0,0.5) channel std and 1% x10 outlier "
                 "channels, Q ~ N(0,1))",
         "config": dict(workload_config(w, ws, args.k_block),
+                       calls="one call per layer" if args.per_layer_calls else
+                       "compress and decompress: all layers per call; attend: one call per layer",
                        l2="flushed (512 MiB write) before every phase, outside the timed events"),
         "phases": ph_info,
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": ph_info[dom]["GB_per_s"],
                      "peak": peak, "unit": "GB/s", "frac": ph_info[dom]["hbm_frac"],
                      "traffic": _traffic(dom_file), "peak_source": peak_kind,
                      "algo_bytes_per_launch": int(algo[dom])},
-        # per layer: kmax + encode (compress), attend_tc, decompress; with
-        # --k-block 32: encode, attend_split + attend_combine, decompress
-        "gpu_launches": args.steps * L * 4,
+        "gpu_launches": args.steps * sum(launches.values()),
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
         "e2e": e2e,
@@ -480,6 +509,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--per-layer-calls", action="store_true",
+                    help="compress and decompress one layer per call (default: all layers in one call)")
     ap.add_argument("--k-block", type=int, default=0, choices=[0, 32],
                     help="K scales: 0 = one per layer (default), 32 = one per 32 elements")
     args = ap.parse_args()

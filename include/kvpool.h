@@ -196,6 +196,19 @@ void kvpool_destroy(kvpool_t* pool);
  * as KVPOOL_ERR_NONFINITE. */
 int kvpool_compress(kvpool_t* pool, int layer, const void* K, const void* V, void* stream);
 
+/* Write-once encode of n layers in one call: the same pool bytes as
+ * kvpool_compress(pool, layers[i], K[i], V[i], stream) for every i, with one
+ * max|K| kernel for all of them and one encode kernel per V width among them
+ * (per 32 layers), so that a whole shared context is written with a few
+ * launches (PolyKV summary, section 2.A: the pool is built once for every
+ * layer of the shared context). layers, K, V: host arrays [n]; K[i], V[i]:
+ * device pointers, as for kvpool_compress. KVPOOL_ERR_INVALID_ARG for n < 1,
+ * a null or misaligned pointer, a layer out of range or named twice;
+ * KVPOOL_ERR_STATE if any of the layers is already compressed. On either
+ * error nothing is launched and no layer changes state. */
+int kvpool_compress_layers(kvpool_t* pool, int n, const int* layers, const void* const* K, const void* const* V,
+                           void* stream);
+
 /* Decode attention of `agents` agents over one compressed layer.
  * Q: bf16 [agents][q_heads][head_dim], device; q_heads a multiple of
  * kv_heads; query head h reads KV head h / (q_heads / kv_heads).
@@ -216,6 +229,16 @@ int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_he
  * the PolyKV summary, section 2.A (each agent injects the decompressed KV into
  * its own cache). */
 int kvpool_decompress(kvpool_t* pool, int layer, void* K_out, void* V_out, void* stream);
+
+/* kvpool_decompress of n layers in one launch per V width (per 32 layers):
+ * layer layers[i] into K_out[i], V_out[i] (bf16 [kv_heads][len][head_dim],
+ * device). layers, K_out, V_out: host arrays [n]; K_out or V_out may be NULL
+ * (that half for none of the layers, not both), and then every entry of the
+ * other must be a device pointer. KVPOOL_ERR_INVALID_ARG for n < 1, a layer
+ * out of range, a null or misaligned output; KVPOOL_ERR_STATE if a layer is
+ * not compressed (nothing is launched). */
+int kvpool_decompress_layers(kvpool_t* pool, int n, const int* layers, void* const* K_out, void* const* V_out,
+                             void* stream);
 
 /* Compressed bytes held for the shared context: per layer, int8 K, packed V,
  * float32 norms and the float32 K scale (padding excluded). Independent of

@@ -1,4 +1,4 @@
-// Materialisation of one pool layer as bf16 K and V.
+// Materialisation of pool layers as bf16 K and V.
 //
 // PolyKV summary, section 2.A: each PooledAgent injects the decompressed K/V
 // of every layer into its own cache; section 2.B: V is dequantised by
@@ -6,7 +6,8 @@
 // H / d). This is the per-agent baseline path that direct attention over the
 // pool avoids.
 //
-// One kernel, grid (blocks, kv heads):
+// One kernel per V width for any number of layers (up to 32 per launch),
+// grid (blocks, kv heads, layers):
 //   V blocks: the block's code groups are unpacked into bytes [token]
 //     [coordinate] in shared memory; then D/32 threads per head-vector, 32
 //     coordinates each, look the centroids up in a shared-memory table, FWHT in
@@ -18,6 +19,8 @@
 //     conversion by an integer add and one exact subtraction); s is the
 //     layer's scale or, in block-scaled pools, the element's 32-block scale.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "kvpool_internal.cuh"
 
@@ -40,26 +43,30 @@ __device__ __forceinline__ float2 i8x2_to_f2(uint32_t w, int k) {
                       make_float2(-12582912.0f, -12582912.0f));
 }
 
-// One launch for both halves, grid (blocks, kv heads): the first nbv blocks of
-// each head materialise V (D/32 threads per head-vector), the rest K (16
-// elements per thread).
+// One launch for both halves of every layer of the launch, grid (blocks, kv
+// heads, layers): the first nbv blocks of each head materialise V (D/32
+// threads per head-vector), the next nbk K (16 elements per thread).
 template <int D, int BITS>
 __global__ void __launch_bounds__(kDecThreads, 5)  // five CTAs per SM: both halves in one wave
-decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscale,
-                  const float* __restrict__ kscales,
-                  const uint8_t* __restrict__ vcodes, const float* __restrict__ vnorm, int ctx,
-                  int ctx_pad, int nbv, uint4* __restrict__ Kout, uint4* __restrict__ Vout,
-                  Codebook cb) {
+decompress_kernel(const __grid_constant__ DecBatch b, int ctx_pad, Codebook cb) {
     constexpr int TPV = D / 32;
     constexpr uint32_t MASK = (1u << BITS) - 1;
+    constexpr int VPB = kDecThreads / TPV;  // head-vectors per V block (a multiple of 32)
+    const DecLayer& Ly = b.L[blockIdx.z];
     const int tid = threadIdx.x;
     const long long head = blockIdx.y;
+    const int ctx = Ly.len;
+    const int8_t* __restrict__ kq = Ly.kq;
+    const float* __restrict__ kscales = Ly.kscales;
+    const int nbv = Ly.Vout ? (ctx + VPB - 1) / VPB : 0;
+    const int nbk = Ly.Kout ? (ctx * (D / 16) + kDecThreads * kKGroups - 1) / (kDecThreads * kKGroups) : 0;
+    if ((int)blockIdx.x >= nbv + nbk) return;  // a shorter layer of the launch
     if ((int)blockIdx.x >= nbv) {
         // ---- K = bf16(q * s): the layer's scale, or the scale of the 32-element
         //      block holding a 16-element group. kKGroups groups per thread,
         //      all loads in flight before any conversion.
         const int n16 = ctx * (D / 16);  // 16-element groups in the head
-        const float s0 = kscales ? 1.0f : *kscale;
+        const float s0 = kscales ? 1.0f : *Ly.kscale;
         uint4 q[kKGroups];
         float sc[kKGroups];
 #pragma unroll
@@ -83,7 +90,7 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
                 const float2 v = __fmul2_rn(k, make_float2(sc[u], sc[u]));
                 o[j] = bf16x2_bits(v.x, v.y);
             }
-            uint4* out = Kout + (head * ctx + t) * (D / 8) + 2 * c;
+            uint4* out = Ly.Kout + (head * ctx + t) * (D / 8) + 2 * c;
             out[0] = make_uint4(o[0], o[1], o[2], o[3]);
             out[1] = make_uint4(o[4], o[5], o[6], o[7]);
         }
@@ -92,18 +99,17 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     // ---- V = bf16(fl(fl(z * n) * (1/d))), z = FWHT(c[codes])
     // the block's code groups (pool layout: per 32 tokens, one sequence per
     // coordinate) are unpacked into bytes [token][coordinate] first
-    constexpr int VPB = kDecThreads / TPV;  // head-vectors per block (a multiple of 32)
     __shared__ float cen[16];
     __shared__ __align__(16) uint8_t codes8[VPB * D];
     if (tid < 16) cen[tid] = cb.c[tid];
     const int lt = tid % TPV;
     const int t = blockIdx.x * VPB + tid / TPV;
     const bool live = t < ctx;
-    const float n = live ? __ldg(vnorm + head * ctx_pad + t) : 0.f;  // in flight during the unpacking
+    const float n = live ? __ldg(Ly.vnorm + head * ctx_pad + t) : 0.f;  // in flight during the unpacking
     {
         const int gq = tid / D, c = tid % D;
         const long long grp = (head * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
-        const uint32_t* in = reinterpret_cast<const uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+        const uint32_t* in = reinterpret_cast<const uint32_t*>(Ly.vcodes + (grp * D + c) * (4 * BITS));
         uint32_t w[BITS + 1];
 #pragma unroll
         for (int k = 0; k < BITS; ++k) w[k] = __ldg(in + k);
@@ -156,7 +162,7 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
     if (!live) return;
     const float inv_d = 1.0f / (float)D;  // a power of two: exact
     const float2 n2 = make_float2(n, n), d2 = make_float2(inv_d, inv_d);
-    uint4* out = Vout + (head * ctx + t) * (D / 8) + lt * 4;
+    uint4* out = Ly.Vout + (head * ctx + t) * (D / 8) + lt * 4;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t o[4];
@@ -170,29 +176,59 @@ decompress_kernel(const int8_t* __restrict__ kq, const float* __restrict__ kscal
 }
 
 template <int D, int BITS>
-cudaError_t run(const Shape& s, const LayerBufs& L, void* K_out, void* V_out, cudaStream_t st) {
+cudaError_t run(const Shape& s, const DecBatch& b, cudaStream_t st) {
     constexpr int VPB = kDecThreads / (D / 32);
-    const int nbv = V_out ? (s.ctx + VPB - 1) / VPB : 0;
-    const int nbk = K_out ? (s.ctx * (D / 16) + kDecThreads * kKGroups - 1) / (kDecThreads * kKGroups) : 0;
-    if (nbv + nbk == 0) return cudaSuccess;
-    decompress_kernel<D, BITS><<<dim3(nbv + nbk, s.kv_heads), kDecThreads, 0, st>>>(
-        L.kq, L.kscale, L.kscales, L.vcodes, L.vnorm, s.ctx, s.ctx_pad, nbv, (uint4*)K_out, (uint4*)V_out,
-        codebook(BITS));
+    int gx = 0;
+    for (int i = 0; i < b.n; ++i) {
+        const int len = b.L[i].len;
+        const int nbv = b.L[i].Vout ? (len + VPB - 1) / VPB : 0;
+        const int nbk = b.L[i].Kout ? (len * (D / 16) + kDecThreads * kKGroups - 1) / (kDecThreads * kKGroups) : 0;
+        gx = std::max(gx, nbv + nbk);
+    }
+    if (gx == 0) return cudaSuccess;
+    decompress_kernel<D, BITS><<<dim3(gx, s.kv_heads, b.n), kDecThreads, 0, st>>>(b, s.ctx_pad, codebook(BITS));
     return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t run_bits(int bits, const Shape& s, const DecBatch& b, cudaStream_t st) {
+    if (bits == 2) return run<D, 2>(s, b, st);
+    if (bits == 3) return run<D, 3>(s, b, st);
+    return run<D, 4>(s, b, st);
 }
 
 }  // namespace
 
-cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out,
-                              cudaStream_t st) {
-    if (s.head_dim == 64) {
-        if (L.bits == 2) return run<64, 2>(s, L, K_out, V_out, st);
-        if (L.bits == 3) return run<64, 3>(s, L, K_out, V_out, st);
-        return run<64, 4>(s, L, K_out, V_out, st);
+cudaError_t launch_decompress_layers(const Shape& s, const LayerBufs* L, const int* len, void* const* K_out,
+                                     void* const* V_out, int n, cudaStream_t st) {
+    for (int c0 = 0; c0 < n; c0 += kEncBatch) {
+        const int nc = std::min(kEncBatch, n - c0);
+        for (int bits = 2; bits <= 4; ++bits) {  // one launch per V width
+            DecBatch b = {};
+            for (int i = c0; i < c0 + nc; ++i) {
+                if (L[i].bits != bits) continue;
+                DecLayer& d = b.L[b.n++];
+                d.kq = L[i].kq;
+                d.kscale = L[i].kscale;
+                d.kscales = L[i].kscales;
+                d.vcodes = L[i].vcodes;
+                d.vnorm = L[i].vnorm;
+                d.Kout = K_out ? static_cast<uint4*>(K_out[i]) : nullptr;
+                d.Vout = V_out ? static_cast<uint4*>(V_out[i]) : nullptr;
+                d.len = len[i];
+            }
+            if (b.n == 0) continue;
+            const cudaError_t e = s.head_dim == 64 ? run_bits<64>(bits, s, b, st) : run_bits<128>(bits, s, b, st);
+            if (e != cudaSuccess) return e;
+        }
     }
-    if (L.bits == 2) return run<128, 2>(s, L, K_out, V_out, st);
-    if (L.bits == 3) return run<128, 3>(s, L, K_out, V_out, st);
-    return run<128, 4>(s, L, K_out, V_out, st);
+    return cudaSuccess;
+}
+
+cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out, cudaStream_t st) {
+    void* k[1] = {K_out};
+    void* v[1] = {V_out};
+    return launch_decompress_layers(s, &L, &s.ctx, K_out ? k : nullptr, V_out ? v : nullptr, 1, st);
 }
 
 }  // namespace kvp

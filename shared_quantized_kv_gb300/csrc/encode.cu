@@ -1,4 +1,4 @@
-// Write-once encode of one pool layer.
+// Write-once encode of pool layers.
 //
 // PolyKV summary (gist.science, "PolyKV: A Shared Asymmetrically-Compressed
 // KV Cache Pool for Multi-Agent LLM Inference"), section 2.B:
@@ -31,7 +31,9 @@
 //     integers) the chunk's 8 elements are recomputed with IEEE divisions.
 //     Block-scaled pools (one scale per 32 elements) take each block's scale
 //     from its own maximum and run no max|K| kernel.
-// The next item's copies are requested as soon as a tile is in registers.
+// A CTA's tiles (V of each of its items, then K of each) stream through two
+// shared-memory buffers, two copies in flight: tile t + 2 is requested as
+// soon as every thread has read tile t.
 // Every float operation that decides a code uses an explicit IEEE round-to-
 // nearest intrinsic, in the fixed order of the definition, so the codes are
 // reproducible bit for bit (no contraction into FMA, no approximate division).
@@ -122,17 +124,33 @@ __device__ __forceinline__ uint32_t absmax8(uint4 u) {
     return max(a & 0xFFFFu, a >> 16);
 }
 
-// max|K| of one layer: CTA b reduces the b-th contiguous slice of the K
-// tensor (16-byte chunks) to part[b]. It releases the encode kernel at once.
+// max|K| of each layer of the launch: CTA (b, l) reduces the b-th contiguous
+// slice of layer l's K tensor (16-byte chunks) to a partial maximum; the last
+// CTA of the layer to finish (an arrival counter, re-armed by that CTA)
+// reduces the partials and writes max|K| (bf16 bits), s = max|K| / 127 (1
+// when K is all zero) and 1/s. It releases the encode kernel at once. For
+// block-scaled layers it only sets *kscale = 1 and clears the maxima.
 __global__ void __launch_bounds__(256)
-kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, uint32_t* __restrict__ part,
-            uint32_t* __restrict__ vnmax) {
+kmax_kernel(const __grid_constant__ EncBatch b, long long nchunk, long long per_cta, int kb, int zero_vn,
+            int* __restrict__ status) {
     ptx::grid_dep_launch();
+    const EncLayer& L = b.L[blockIdx.y];
+    const int tid = threadIdx.x, lane = tid % 32, warp = tid / 32;
+    if (blockIdx.x == 0 && tid == 0) {
+        if (zero_vn) L.maxima[1] = 0;  // raised by the encode kernel after its dependency wait
+        if (kb) {
+            L.maxima[0] = 0;
+            *L.kscale = 1.0f;
+        }
+    }
+    if (kb) return;
     __shared__ uint32_t red[8];
+    __shared__ int last;
+    const uint4* K = reinterpret_cast<const uint4*>(L.K);
     const long long c0 = (long long)blockIdx.x * per_cta;
     const long long c1 = min(nchunk, c0 + per_cta);
     uint32_t m = 0;
-    for (long long base = c0 + threadIdx.x; base < c1; base += 8 * 256) {
+    for (long long base = c0 + tid; base < c1; base += 8 * 256) {
         uint4 u[8];  // all of a batch's loads in flight at once
 #pragma unroll
         for (int j = 0; j < 8; ++j) u[j] = (base + j * 256 < c1) ? __ldg(K + base + j * 256) : make_uint4(0, 0, 0, 0);
@@ -140,80 +158,113 @@ kmax_kernel(const uint4* __restrict__ K, long long nchunk, long long per_cta, ui
         for (int j = 0; j < 8; ++j) m = max(m, absmax8(u[j]));
     }
     m = __reduce_max_sync(0xffffffffu, m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x / 32] = m;
+    if (lane == 0) red[warp] = m;
     __syncthreads();
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
 #pragma unroll
         for (int w = 1; w < 8; ++w) m = max(m, red[w]);
-        part[blockIdx.x] = m;
-        if (blockIdx.x == 0) *vnmax = 0;  // raised by the encode kernel after its dependency wait
+        L.kpart[blockIdx.x] = m;
+        __threadfence();  // the partial before the arrival
+        last = atomicAdd(L.kpart + kKmaxCount, 1u) == gridDim.x - 1;
+    }
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    uint32_t mm = 0;
+    for (int i = tid; i < (int)gridDim.x; i += 256) mm = max(mm, *reinterpret_cast<volatile const uint32_t*>(L.kpart + i));
+    mm = __reduce_max_sync(0xffffffffu, mm);
+    __syncthreads();  // red[] is free again
+    if (lane == 0) red[warp] = mm;
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll
+        for (int w = 0; w < 8; ++w) mm = max(mm, red[w]);
+        const float s = (mm == 0) ? 1.0f : __fdiv_rn(__uint_as_float(mm << 16), 127.0f);
+        L.maxima[0] = mm;
+        *L.kscale = s;
+        L.kpart[kKmaxInv] = __float_as_uint(__frcp_rn(s));
+        L.kpart[kKmaxCount] = 0;  // re-armed for the layer's next compress
+        if (mm >= 0x7F80u) atomicOr(status, kStNonfinite);
     }
 }
 
-// KB: block-scaled K (one scale per 32 elements, written to kscales; no
-// max|K| kernel before this one and *kscale = 1)
+// All items of the launch's layers (same V width), layer-major; CTA i takes
+// items i, i + G, ... in two passes: first the V of every item (beside the
+// max|K| kernel), then, after the dependency wait, the K of every item.
+// KB: block-scaled K (one scale per 32 elements, written to kscales).
 template <int D, int BITS, bool KB>
 __global__ void __launch_bounds__(kEncThreads)
-encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, int ctx, int ctx_pad,
-              int t_base, int items_per_head, int items, int8_t* __restrict__ kq, uint8_t* __restrict__ vcodes,
-              float* __restrict__ vnorm, float* __restrict__ kscale, uint32_t* __restrict__ maxima,
-              const uint32_t* __restrict__ kpart, int nparts, float* __restrict__ kscales,
-              int* __restrict__ status, Codebook cb) {
+encode_kernel(const __grid_constant__ EncBatch b, int ctx, int ctx_pad, int t_base, int items_per_head,
+              int items_per_layer, int items, int* __restrict__ status, Codebook cb) {
     constexpr int TPV = D / 32;              // threads per head-vector
     constexpr int VPI = kEncThreads / TPV;   // tokens per item (a multiple of 32)
     constexpr uint32_t kTile = VPI * D * 2;  // bytes of K (and of V) per item: 8 KB
     constexpr int kChunks = (int)(kTile / 16 / kEncThreads);  // 16-byte chunks per thread and tile
     constexpr int L = 1 << BITS;
-    __shared__ __align__(128) unsigned char sK[kTile];
-    __shared__ __align__(128) unsigned char sV[kTile];
+    // the CTA's tiles, V of each of its items and then K of each, stream
+    // through two buffers: tile t + 2 is requested once tile t has been read
+    __shared__ __align__(128) unsigned char tiles[2][kTile];
     __shared__ __align__(16) uint8_t codes8[VPI * D];
     __shared__ uint32_t red[kEncThreads / 32];
-    __shared__ __align__(8) uint64_t bars[2];  // K tile, V tile
+    __shared__ __align__(8) uint64_t bars[2];  // one per buffer
     __shared__ uint32_t sDep[kEncThreads];
+    extern __shared__ uint32_t snm[];  // per item of this CTA: float bits of its largest V norm
     const int tid = threadIdx.x, lane = tid % 32;
     const int lt = tid % TPV;  // this thread's 32-coordinate slice
     const int tl = tid / TPV;  // its token within the item
     const int G = (int)gridDim.x;
     const unsigned gmask = 0xffffffffu;
-    const uint32_t barK = ptx::smem_u32(&bars[0]), barV = ptx::smem_u32(&bars[1]);
+    const int m = (items - (int)blockIdx.x + G - 1) / G;  // items of this CTA (>= 1)
 
-    auto item_h = [&](int it) { return it / items_per_head; };
+    auto item_l = [&](int it) { return it / items_per_layer; };
+    auto item_h = [&](int it) { return (it % items_per_layer) / items_per_head; };
     auto item_t0 = [&](int it) { return (it % items_per_head) * VPI; };
     // K and V are inputs of the launch, written by no kernel that may still
     // run (the max|K| kernel before this one only reads K): the copies start
     // before the dependency wait
     auto item_bytes = [&](int it) { return (uint32_t)min(VPI, ctx - item_t0(it)) * D * 2; };
     auto item_src = [&](int it) { return ((long long)item_h(it) * ctx + item_t0(it)) * D; };
-    auto issueV = [&](int it) {
-        ptx::mbar_expect_tx(barV, item_bytes(it));
-        ptx::bulk_g2s(ptx::smem_u32(sV), V + item_src(it), item_bytes(it), barV);
+    // tile t < m: V of item blockIdx.x + t*G; tile m + k: K of item blockIdx.x + k*G
+    auto issue_tile = [&](int t) {
+        const bool isK = t >= m;
+        const int it = (int)blockIdx.x + (isK ? t - m : t) * G;
+        const uint32_t bar = ptx::smem_u32(&bars[t & 1]);
+        const EncLayer& Ly = b.L[item_l(it)];
+        ptx::mbar_expect_tx(bar, item_bytes(it));
+        ptx::bulk_g2s(ptx::smem_u32(tiles[t & 1]), (isK ? Ly.K : Ly.V) + item_src(it), item_bytes(it), bar);
     };
-    auto issueK = [&](int it) {
-        ptx::mbar_expect_tx(barK, item_bytes(it));
-        ptx::bulk_g2s(ptx::smem_u32(sK), K + item_src(it), item_bytes(it), barK);
+    bool ok = true;
+    auto wait_tile = [&](int t) {
+        if (ok && !ptx::mbar_wait(ptx::smem_u32(&bars[t & 1]), (uint32_t)(t >> 1) & 1, kEncWaitNs)) ok = false;
+    };
+    // after every thread has read tile t (its dependency word stored, then a
+    // barrier): the next tile for the buffer
+    auto next_tile = [&](int t) {
+        if (tid == 0 && ok && t + 2 < 2 * m) {
+            ptx::fence_proxy_async();
+            issue_tile(t + 2);
+        }
     };
     if (tid == 0) {
-        ptx::mbar_init(barK, 1);
-        ptx::mbar_init(barV, 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_u32(&bars[1]), 1);
         ptx::mbar_init_fence();
-        issueV(blockIdx.x);
-        issueK(blockIdx.x);
+        issue_tile(0);
+        issue_tile(1);
     }
     __syncthreads();
 
-    bool ok = true, have_s = false;
-    float s = 1.0f, r = 1.0f;
-    uint32_t nmax = 0;
-    uint32_t phase = 0;
-    for (int it = blockIdx.x; it < items; it += G) {
+    // ---- pass 1: V
+    for (int it = blockIdx.x, k = 0; it < items; it += G, ++k) {
+        const EncLayer& Ly = b.L[item_l(it)];
         const int h = item_h(it), t0 = item_t0(it);
         const int ntok = min(VPI, ctx - t0);
-        if (ok && !ptx::mbar_wait(barV, phase, kEncWaitNs)) ok = false;
+        wait_tile(k);
         const bool live = tl < ntok;
         float2 x[16];  // coordinates (2i, 2i + 1) of this thread's slice
         {
             uint32_t dep = 0;  // depends on every word this thread reads from the V tile
-            const uint4* vs = reinterpret_cast<const uint4*>(sV + tl * (D * 2) + lt * 64);
+            const uint4* vs = reinterpret_cast<const uint4*>(tiles[k & 1] + tl * (D * 2) + lt * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 const uint4 vv = vs[c];
@@ -222,7 +273,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
 #pragma unroll
                 for (int j = 0; j < 4; ++j) x[c * 4 + j] = make_float2(bf_lo(w[j]), bf_hi(w[j]));
             }
-            // The next item's copy overwrites the tile. A barrier does not
+            // The next copy into the buffer overwrites the tile. A barrier does not
             // wait for shared-memory loads still in flight, and the copy
             // writes through the async proxy: every thread first stores a word
             // that depends on all its loads (so they have returned), and the
@@ -230,10 +281,7 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
             sDep[tid] = dep;
         }
         __syncthreads();
-        if (tid == 0 && ok && it + G < items) {
-            ptx::fence_proxy_async();
-            issueV(it + G);
-        }
+        next_tile(k);
 
         // The float steps below run on coordinate pairs (2i, 2i + 1): one
         // instruction, two IEEE round-to-nearest operations in the same order.
@@ -259,7 +307,8 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
             for (int i = 0; i < w / 2; ++i) sq[i] = __fadd2_rn(sq[i], sq[i + w / 2]);
         }
         const float n = __shfl_sync(gmask, __fsqrt_rn(__fadd_rn(sq[0].x, sq[0].y)), lane - lt);  // slice 0 holds the sum
-        if (live) nmax = max(nmax, __float_as_uint(n));
+        const uint32_t nmax = __reduce_max_sync(gmask, live ? __float_as_uint(n) : 0u);
+        if (lane == 0) red[tid / 32] = nmax;
 
         // FWHT, stages h = 1, 2, ..., D/2, lower index first; h = 1 inside
         // each pair, h = 2 ... 16 between pairs i and i + h/2
@@ -306,8 +355,14 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
         uint4* c8 = reinterpret_cast<uint4*>(codes8 + tl * D + lt * 32);
         c8[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
         c8[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        if (live && lt == 0) vnorm[(long long)h * ctx_pad + t_base + t0 + tl] = n;
-        __syncthreads();
+        if (live && lt == 0) Ly.vnorm[(long long)h * ctx_pad + t_base + t0 + tl] = n;
+        __syncthreads();  // codes8 and red[] complete
+        if (tid == 0) {
+            uint32_t nm = red[0];
+#pragma unroll
+            for (int w = 1; w < kEncThreads / 32; ++w) nm = max(nm, red[w]);
+            snm[k] = nm;  // flushed after the dependency wait, once the word is cleared
+        }
 
         // pool layout: one thread per (32-token group of the item, coordinate)
         {
@@ -323,42 +378,34 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                 if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
             }
             const long long grp = ((long long)h * ctx_pad + t_base + t0) / 32 + gq;
-            uint32_t* out = reinterpret_cast<uint32_t*>(vcodes + (grp * D + c) * (4 * BITS));
+            uint32_t* out = reinterpret_cast<uint32_t*>(Ly.vcodes + (grp * D + c) * (4 * BITS));
 #pragma unroll
             for (int w = 0; w < BITS; ++w) out[w] = words[w];
         }
 
-        // K: s = max|K| / 127 (1 when K is all zero) from the partial maxima of
-        // the max|K| kernel, complete once the dependency wait returns (by now
-        // it has long finished: it ran beside the V work above)
-        if (KB && !have_s) {
-            have_s = true;
-            if (blockIdx.x == 0 && tid == 0) {
-                *kscale = 1.0f;
-                maxima[0] = 0;
-            }
+    }
+
+    // ---- pass 2: K. The max|K| kernel is complete: s and 1/s of every layer
+    // are written and the largest-V-norm words cleared.
+    ptx::grid_dep_wait();
+    for (int it = blockIdx.x, k = 0; it < items; it += G, ++k) {
+        const int t = m + k;
+        const unsigned char* sK = tiles[t & 1];
+        const EncLayer& Ly = b.L[item_l(it)];
+        const int h = item_h(it), t0 = item_t0(it);
+        const int ntok = min(VPI, ctx - t0);
+        if (tid == 0) {
+            const uint32_t nm = snm[k];
+            if (nm > *reinterpret_cast<volatile uint32_t*>(&Ly.maxima[1])) atomicMax(&Ly.maxima[1], nm);
+            if (nm >= 0x7F800000u) atomicOr(status, kStNonfinite);
         }
-        if (!have_s) {
-            ptx::grid_dep_wait();
-            uint32_t m = 0;
-            for (int i = tid; i < nparts; i += kEncThreads) m = max(m, kpart[i]);
-            m = __reduce_max_sync(gmask, m);
-            if (lane == 0) red[tid / 32] = m;
-            __syncthreads();
-#pragma unroll
-            for (int w = 0; w < kEncThreads / 32; ++w) m = max(m, red[w]);
-            s = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
-            r = __frcp_rn(s);
-            have_s = true;
-            if (blockIdx.x == 0 && tid == 0) {
-                *kscale = s;
-                maxima[0] = m;
-                if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
-            }
+        float s = 1.0f, r = 1.0f;
+        if constexpr (!KB) {
+            s = *Ly.kscale;
+            r = __uint_as_float(Ly.kpart[kKmaxInv]);
         }
         // q = clamp(rint(k / s), -127, 127), 8 elements per 16-byte chunk
-        if (ok && !ptx::mbar_wait(barK, phase, kEncWaitNs)) ok = false;
-        phase ^= 1;
+        wait_tile(t);
         {
             uint32_t dep = 0;
 #pragma unroll
@@ -377,93 +424,88 @@ encode_kernel(const uint16_t* __restrict__ K, const uint16_t* __restrict__ V, in
                         const uint2 q = quant8(u, sb, __frcp_rn(sb));
                         dep ^= q.x ^ u.x;
                         const long long tok_i = (long long)h * ctx_pad + t_base + t0 + row;
-                        *reinterpret_cast<uint2*>(kq + tok_i * D + (idx % (D / 8)) * 8) = q;
-                        if ((idx & 3) == 0) kscales[tok_i * (D / 32) + (idx % (D / 8)) / 4] = sb;
+                        *reinterpret_cast<uint2*>(Ly.kq + tok_i * D + (idx % (D / 8)) * 8) = q;
+                        if ((idx & 3) == 0) Ly.kscales[tok_i * (D / 32) + (idx % (D / 8)) / 4] = sb;
                         if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
                     }
                 } else if (row < ntok) {
                     const uint4 u = reinterpret_cast<const uint4*>(sK)[idx];
                     const uint2 q = quant8(u, s, r);
                     dep ^= q.x;
-                    *reinterpret_cast<uint2*>(kq + ((long long)h * ctx_pad + t_base + t0 + row) * D + (idx % (D / 8)) * 8) = q;
+                    *reinterpret_cast<uint2*>(Ly.kq + ((long long)h * ctx_pad + t_base + t0 + row) * D +
+                                              (idx % (D / 8)) * 8) = q;
                 }
             }
             sDep[tid] = dep;  // as for the V tile
         }
-        __syncthreads();  // also: red[] and codes8 are free for the next item
-        if (tid == 0 && ok && it + G < items) {
-            ptx::fence_proxy_async();
-            issueK(it + G);
-        }
+        __syncthreads();
+        next_tile(t);
     }
-
-    // the largest V norm of the layer (zeroed by the max|K| kernel, which
-    // completed before the dependency wait above)
-    nmax = __reduce_max_sync(gmask, nmax);
-    __syncthreads();  // red[] is free again
-    if (lane == 0) red[tid / 32] = nmax;
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t nm = 0;
-#pragma unroll
-        for (int w = 0; w < kEncThreads / 32; ++w) nm = max(nm, red[w]);
-        if (nm > *reinterpret_cast<volatile uint32_t*>(&maxima[1])) atomicMax(&maxima[1], nm);
-        if (nm >= 0x7F800000u) atomicOr(status, kStNonfinite);
-        if (!ok) atomicOr(status, kStTimeout);
-    }
+    if (tid == 0 && !ok) atomicOr(status, kStTimeout);
 }
 
-// s.ctx: tokens of this call (the inputs' token axis); t_base: the pool token
-// they start at (0, or a multiple of 32 for appends to block-scaled pools)
 template <int D, int BITS>
-cudaError_t run(const Shape& s, const LayerBufs& L, const void* K, const void* V, int* status,
-                int sm_count, int t_base, cudaStream_t st) {
+cudaError_t run_encode(const Shape& s, const EncBatch& b, int* status, int sm_count, int t_base, bool kb,
+                       cudaStream_t st) {
     constexpr int VPI = kEncThreads / (D / 32);
-    const bool kb = L.kscales != nullptr;
-    static int per_sm[2] = {-1, -1};
-    int& occ = per_sm[kb ? 1 : 0];
-    if (occ < 0) {
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-            &occ, kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>, kEncThreads, 0);
-        if (e != cudaSuccess || occ < 1) {
-            occ = -1;
-            return e != cudaSuccess ? e : cudaErrorInvalidConfiguration;
-        }
-    }
-    // max|K|: about two CTAs per SM, contiguous slices of whole 16-byte chunks
-    const long long nchunk = (long long)s.kv_heads * s.ctx * (D / 8);
-    const int ga = (int)std::min<long long>(
-        kKmaxParts, std::max<long long>(2LL * sm_count, (nchunk + 2047) / 2048));  // one batch per thread
-    const long long per_cta = (nchunk + ga - 1) / ga;
-    cudaError_t e;
-    if (kb) {
-        // block scales need no max|K| kernel; the largest-norm word is raised
-        // with atomics by the encode kernel (over every append of the layer)
-        e = t_base == 0 ? cudaMemsetAsync(L.vnmax, 0, sizeof(uint32_t), st) : cudaSuccess;
-    } else {
-        kmax_kernel<<<ga, 256, 0, st>>>((const uint4*)K, nchunk, per_cta, L.kpart, L.vnmax);
-        e = cudaGetLastError();
-    }
-    if (e != cudaSuccess) return e;
-    // encode: starts while the max|K| kernel runs (programmatic dependent
-    // launch); waits for it only before its first K codes
+    auto kern = kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>;
     const int items_per_head = (s.ctx + VPI - 1) / VPI;
-    const int items = s.kv_heads * items_per_head;
-    const int G = std::min(items, occ * sm_count);
+    const int items_per_layer = s.kv_heads * items_per_head;
+    const long long items_ll = (long long)b.n * items_per_layer;
+    if (items_ll > INT32_MAX) return cudaErrorInvalidValue;
+    const int items = (int)items_ll;
+    // grid: all CTAs resident; each keeps one word per item it takes
+    int occ = 0, G = 0;
+    size_t dyn = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kEncThreads, dyn);
+        if (e != cudaSuccess) return e;
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        G = std::min(items, occ * sm_count);
+        const size_t need = (size_t)((items + G - 1) / G) * sizeof(uint32_t);
+        if (need <= dyn) break;
+        dyn = need;
+    }
+    if ((size_t)((items + G - 1) / G) * sizeof(uint32_t) > dyn) return cudaErrorInvalidConfiguration;
+    if (dyn > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+    }
+    // starts while the max|K| kernel runs (programmatic dependent launch)
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(G, 1, 1);
     cfg.blockDim = dim3(kEncThreads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = dyn;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = kb ? 0 : 1;
-    return cudaLaunchKernelEx(&cfg, kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>,
-                              (const uint16_t*)K, (const uint16_t*)V, s.ctx, s.ctx_pad, t_base, items_per_head, items,
-                              L.kq, L.vcodes, L.vnorm, L.kscale, L.kabsmax, (const uint32_t*)L.kpart, ga,
-                              L.kscales, status, codebook(BITS));
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, b, s.ctx, s.ctx_pad, t_base, items_per_head, items_per_layer, items,
+                              status, codebook(BITS));
+}
+
+template <int D>
+cudaError_t run_bits(int bits, const Shape& s, const EncBatch& b, int* status, int sm_count, int t_base, bool kb,
+                     cudaStream_t st) {
+    if (bits == 2) return run_encode<D, 2>(s, b, status, sm_count, t_base, kb, st);
+    if (bits == 3) return run_encode<D, 3>(s, b, status, sm_count, t_base, kb, st);
+    return run_encode<D, 4>(s, b, status, sm_count, t_base, kb, st);
+}
+
+EncLayer enc_layer(const LayerBufs& L, const void* K, const void* V) {
+    EncLayer e;
+    e.K = static_cast<const uint16_t*>(K);
+    e.V = static_cast<const uint16_t*>(V);
+    e.kq = L.kq;
+    e.vcodes = L.vcodes;
+    e.vnorm = L.vnorm;
+    e.kscale = L.kscale;
+    e.maxima = L.kabsmax;  // {max|K| bits, largest V norm bits}: adjacent words
+    e.kpart = L.kpart;
+    e.kscales = L.kscales;
+    return e;
 }
 
 __global__ void __launch_bounds__(256)
@@ -489,17 +531,41 @@ cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st)
     return cudaGetLastError();
 }
 
+cudaError_t launch_encode_layers(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V,
+                                 int n, int* status, int sm_count, int t_base, cudaStream_t st) {
+    if (n < 1) return cudaErrorInvalidValue;
+    const bool kb = L[0].kscales != nullptr;
+    if (t_base != 0 && (!kb || n != 1 || t_base % 32 != 0)) return cudaErrorInvalidValue;
+    for (int c0 = 0; c0 < n; c0 += kEncBatch) {
+        const int nc = std::min(kEncBatch, n - c0);
+        // max|K| of every layer of the chunk in one launch: about two CTAs per
+        // SM in all, so that they are all running when the encode kernel starts
+        EncBatch all = {};
+        all.n = nc;
+        for (int i = 0; i < nc; ++i) all.L[i] = enc_layer(L[c0 + i], K[c0 + i], V[c0 + i]);
+        const long long nchunk = (long long)s.kv_heads * s.ctx * (s.head_dim / 8);
+        const int gx = kb ? 1 : std::max(1, std::min(kKmaxInv, (2 * sm_count + nc - 1) / nc));
+        const long long per_cta = (nchunk + gx - 1) / gx;
+        kmax_kernel<<<dim3(gx, nc), 256, 0, st>>>(all, nchunk, per_cta, kb ? 1 : 0, t_base == 0 ? 1 : 0, status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        // one encode launch per V width among the chunk's layers
+        for (int bits = 2; bits <= 4; ++bits) {
+            EncBatch sub = {};
+            for (int i = 0; i < nc; ++i)
+                if (L[c0 + i].bits == bits) sub.L[sub.n++] = all.L[i];
+            if (sub.n == 0) continue;
+            e = s.head_dim == 64 ? run_bits<64>(bits, s, sub, status, sm_count, t_base, kb, st)
+                                 : run_bits<128>(bits, s, sub, status, sm_count, t_base, kb, st);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
                           int* status, int sm_count, int t_base, cudaStream_t st) {
-    if (t_base != 0 && (L.kscales == nullptr || t_base % 32 != 0)) return cudaErrorInvalidValue;
-    if (s.head_dim == 64) {
-        if (L.bits == 2) return run<64, 2>(s, L, K, V, status, sm_count, t_base, st);
-        if (L.bits == 3) return run<64, 3>(s, L, K, V, status, sm_count, t_base, st);
-        return run<64, 4>(s, L, K, V, status, sm_count, t_base, st);
-    }
-    if (L.bits == 2) return run<128, 2>(s, L, K, V, status, sm_count, t_base, st);
-    if (L.bits == 3) return run<128, 3>(s, L, K, V, status, sm_count, t_base, st);
-    return run<128, 4>(s, L, K, V, status, sm_count, t_base, st);
+    return launch_encode_layers(s, &L, &K, &V, 1, status, sm_count, t_base, st);
 }
 
 }  // namespace kvp

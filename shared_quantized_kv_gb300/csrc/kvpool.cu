@@ -173,11 +173,13 @@ struct kvpool {
     std::vector<unsigned char> compressed;
     std::vector<int> len;  // tokens the layer holds: ctx once compressed; grows by appends
     // Per stream: the layer that this pool's most recent launch on it wrote,
-    // or -1. An attend may read its layer before the grid-dependency wait
-    // (programmatic dependent launch) unless the launch right before it on
-    // the same stream wrote that layer: only the immediately preceding kernel
-    // can still be running when it starts, and that one cannot have started
-    // before the kernels ahead of it finished.
+    // -1 for none, kWroteMany for several (a multi-layer compress). An attend
+    // may read its layer before the grid-dependency wait (programmatic
+    // dependent launch) unless the launch right before it on the same stream
+    // wrote that layer: only the immediately preceding kernel can still be
+    // running when it starts, and that one cannot have started before the
+    // kernels ahead of it finished.
+    static constexpr int kWroteMany = -2;
     std::unordered_map<void*, int> last_write;
     std::mutex mu;  // last_write: attends may come from several host threads
     void wrote(void* stream, int layer) {
@@ -187,7 +189,7 @@ struct kvpool {
     bool may_read_early(void* stream, int layer) {
         std::lock_guard<std::mutex> g(mu);
         auto it = last_write.find(stream);
-        return it == last_write.end() || it->second != layer;
+        return it == last_write.end() || (it->second != layer && it->second != kWroteMany);
     }
     std::vector<CUtensorMap> kmaps;
     unsigned char* base = nullptr;
@@ -408,6 +410,31 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
     return KVPOOL_OK;
 }
 
+int kvpool_compress_layers(kvpool_t* p, int n, const int* layers, const void* const* K, const void* const* V,
+                           void* stream) {
+    if (!p || n < 1 || !layers || !K || !V) return KVPOOL_ERR_INVALID_ARG;
+    std::vector<char> seen(p->layers, 0);
+    for (int i = 0; i < n; ++i) {
+        const int l = layers[i];
+        if (l < 0 || l >= p->layers || seen[l]) return KVPOOL_ERR_INVALID_ARG;
+        seen[l] = 1;
+        if (!K[i] || !V[i] || !aligned16(K[i]) || !aligned16(V[i])) return KVPOOL_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < n; ++i)
+        if (p->compressed[layers[i]]) return KVPOOL_ERR_STATE;
+    std::vector<kvp::LayerBufs> L(n);
+    for (int i = 0; i < n; ++i) L[i] = p->layer(layers[i]);
+    cudaError_t e = kvp::launch_encode_layers(p->shape(), L.data(), K, V, n, p->status, p->sm_count, 0,
+                                              static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return map_cuda(e);
+    for (int i = 0; i < n; ++i) {
+        p->compressed[layers[i]] = 1;
+        p->len[layers[i]] = p->ctx;
+    }
+    p->wrote(stream, n == 1 ? layers[0] : kvpool::kWroteMany);
+    return KVPOOL_OK;
+}
+
 int kvpool_append(kvpool_t* p, int layer, const void* K, const void* V, int n, void* stream) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
@@ -486,6 +513,29 @@ int kvpool_decompress(kvpool_t* p, int layer, void* K_out, void* V_out, void* st
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
     const cudaError_t e = kvp::launch_decompress(p->shape_of(layer), p->layer(layer), K_out, V_out,
                                                  static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) p->wrote(stream, -1);
+    return map_cuda(e);
+}
+
+int kvpool_decompress_layers(kvpool_t* p, int n, const int* layers, void* const* K_out, void* const* V_out,
+                             void* stream) {
+    if (!p || n < 1 || !layers || (!K_out && !V_out)) return KVPOOL_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) {
+        const int l = layers[i];
+        if (l < 0 || l >= p->layers) return KVPOOL_ERR_INVALID_ARG;
+        if (K_out && (!K_out[i] || !aligned16(K_out[i]))) return KVPOOL_ERR_INVALID_ARG;
+        if (V_out && (!V_out[i] || !aligned16(V_out[i]))) return KVPOOL_ERR_INVALID_ARG;
+    }
+    for (int i = 0; i < n; ++i)
+        if (!p->compressed[layers[i]]) return KVPOOL_ERR_STATE;
+    std::vector<kvp::LayerBufs> L(n);
+    std::vector<int> len(n);
+    for (int i = 0; i < n; ++i) {
+        L[i] = p->layer(layers[i]);
+        len[i] = p->len[layers[i]];
+    }
+    const cudaError_t e = kvp::launch_decompress_layers(p->shape(), L.data(), len.data(), K_out, V_out, n,
+                                                        static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
 }

@@ -31,9 +31,13 @@ struct Codebook {
 // Host: the library's own table for `bits` in {2,3,4} (derived once).
 const Codebook& codebook(int bits);
 
-// Most CTAs of the max|K| kernel that runs ahead of the encode kernel: one
-// partial maximum (bf16 bits of |k|) per CTA, kept per layer.
+// Compress scratch of a layer: kKmaxParts words. Words [0, kKmaxInv) take the
+// max|K| kernel's partial maxima (bf16 bits of |k|, one per CTA); kKmaxInv
+// the float bits of 1/s; kKmaxCount the kernel's arrival counter (0 between
+// launches; the pool is created zeroed).
 constexpr int kKmaxParts = 512;
+constexpr int kKmaxInv = kKmaxParts - 2;
+constexpr int kKmaxCount = kKmaxParts - 1;
 
 // Device buffers of one layer.
 struct LayerBufs {
@@ -53,15 +57,59 @@ struct Shape {
     int kv_heads, head_dim, ctx, ctx_pad;
 };
 
-// ---- encode (write-once compress of one layer)
+// ---- encode (write-once compress)
+// One layer of a multi-layer encode launch (kernel parameter, by value).
+struct EncLayer {
+    const uint16_t* K;  // bf16 [Hk][ctx][D] inputs
+    const uint16_t* V;
+    int8_t* kq;
+    uint8_t* vcodes;
+    float* vnorm;
+    float* kscale;
+    uint32_t* maxima;   // {bf16 bits of max|K|, float bits of the largest V norm}
+    uint32_t* kpart;    // kKmaxParts words of compress scratch
+    float* kscales;     // block-scaled K, else null
+};
+// Most layers per launch of the multi-layer kernels.
+constexpr int kEncBatch = 32;
+struct EncBatch {
+    int n;
+    EncLayer L[kEncBatch];
+};
+
 // s.ctx is the token count of K and V; t_base the pool token they start at
 // (non-zero only for appends to block-scaled layers, a multiple of 32).
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
                           int* status, int sm_count, int t_base, cudaStream_t st);
+// n layers (all of one pool, so one k-scaling mode) in a few launches per
+// kEncBatch of them: one max|K| kernel over all, then one encode kernel per V
+// width. t_base != 0 only with n = 1.
+cudaError_t launch_encode_layers(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V,
+                                 int n, int* status, int sm_count, int t_base, cudaStream_t st);
 
 // ---- decompress
+// One layer of a multi-layer decompress launch (kernel parameter, by value).
+struct DecLayer {
+    const int8_t* kq;
+    const float* kscale;
+    const float* kscales;  // block-scaled K, else null
+    const uint8_t* vcodes;
+    const float* vnorm;
+    uint4* Kout;           // bf16 [Hk][len][D], or null
+    uint4* Vout;
+    int len;               // tokens the layer holds
+};
+struct DecBatch {
+    int n;
+    DecLayer L[kEncBatch];
+};
+
 cudaError_t launch_decompress(const Shape& s, const LayerBufs& L, void* K_out, void* V_out,
                               cudaStream_t st);
+// n layers, one launch per V width and kEncBatch layers; len[i] tokens of
+// layer i; K_out or V_out may be null (that half for none of the layers).
+cudaError_t launch_decompress_layers(const Shape& s, const LayerBufs* L, const int* len, void* const* K_out,
+                                     void* const* V_out, int n, cudaStream_t st);
 
 // ---- attend
 struct AttendArgs {

@@ -65,6 +65,10 @@ _SIGS = {
                                      ctypes.c_float, ctypes.c_void_p]),
     "kvpool_decompress": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
                                          ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_compress_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                              ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
+    "kvpool_decompress_layers": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p,
+                                                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]),
     "kvpool_pool_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
     "kvpool_device_bytes": (ctypes.c_size_t, [ctypes.c_void_p]),
     "kvpool_status": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_void_p]),
@@ -202,6 +206,21 @@ class KVPool:
                                       _dev_ptr(V, torch.bfloat16, "V"), _stream_ptr(stream)),
                "kvpool_compress")
 
+    def compress_layers(self, layers, Ks, Vs, stream=None):
+        """compress() of every layer in ``layers`` (K = Ks[i], V = Vs[i]) in
+        one call: one max|K| kernel for all of them, one encode kernel per V
+        width among them."""
+        import torch
+
+        n = len(layers)
+        if len(Ks) != n or len(Vs) != n:
+            raise ValueError("layers, Ks and Vs must have the same length")
+        lay = (ctypes.c_int * max(n, 1))(*[int(l) for l in layers])
+        kp = (ctypes.c_void_p * max(n, 1))(*[_dev_ptr(K, torch.bfloat16, "K").value for K in Ks])
+        vp = (ctypes.c_void_p * max(n, 1))(*[_dev_ptr(V, torch.bfloat16, "V").value for V in Vs])
+        _check(_lib().kvpool_compress_layers(self._h, n, lay, kp, vp, _stream_ptr(stream)),
+               "kvpool_compress_layers")
+
     def append(self, layer, K, V, stream=None):
         """Append tokens to a block-scaled layer: K, V bf16 [kv_heads, n, d]
         (device) become tokens [len, len + n) of the layer."""
@@ -252,6 +271,31 @@ class KVPool:
                                         _dev_ptr(V_out, torch.bfloat16, "V_out"),
                                         _stream_ptr(stream)), "kvpool_decompress")
         return K_out, V_out
+
+    def decompress_layers(self, layers, K_outs=None, V_outs=None, stream=None):
+        """decompress() of every layer in ``layers`` in one launch per V
+        width. K_outs / V_outs: lists of bf16 [kv_heads, len, d] tensors
+        (allocated when None). Returns (K_outs, V_outs)."""
+        import torch
+
+        n = len(layers)
+        dev = torch.device("cuda", torch.cuda.current_device())
+
+        def outs(given):
+            if given is not None:
+                if len(given) != n:
+                    raise ValueError("one output per layer")
+                return list(given)
+            return [torch.empty((self.kv_heads, self.layer_len(l), self.head_dim), dtype=torch.bfloat16,
+                                device=dev) for l in layers]
+
+        K_outs, V_outs = outs(K_outs), outs(V_outs)
+        lay = (ctypes.c_int * max(n, 1))(*[int(l) for l in layers])
+        kp = (ctypes.c_void_p * max(n, 1))(*[_dev_ptr(K, torch.bfloat16, "K_out").value for K in K_outs])
+        vp = (ctypes.c_void_p * max(n, 1))(*[_dev_ptr(V, torch.bfloat16, "V_out").value for V in V_outs])
+        _check(_lib().kvpool_decompress_layers(self._h, n, lay, kp, vp, _stream_ptr(stream)),
+               "kvpool_decompress_layers")
+        return K_outs, V_outs
 
     def pool_bytes(self) -> int:
         return int(_lib().kvpool_pool_bytes(self._h))

@@ -2,11 +2,14 @@
 times, for profilers (ncu captures one kernel of one repetition).
 
     python -m shared_quantized_kv_gb300.profile_layer --workload llama3_8b_4k --reps 4
+    python -m shared_quantized_kv_gb300.profile_layer --workload llama3_8b_4k --layers 8
 
 Every repetition re-arms the layer (kvpool_reset_layer), compresses it,
 attends all agents and decompresses it; the script exits non-zero if the
 device status word reports an error. Inputs are the seeded synthetic layer of
-the workload (layer 0 unless --layer is given).
+the workload (layer 0 unless --layer is given). With --layers N (N > 1) the
+first N layers of the workload go through the multi-layer calls: one
+compress and one decompress call for all N, attend per layer.
 """
 
 import argparse
@@ -24,8 +27,11 @@ def main() -> int:
     ap.add_argument("--workload", default="llama3_8b_4k")
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--reps", type=int, default=4)
+    ap.add_argument("--layers", type=int, default=1)
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
+    if args.layers > 1:
+        return multi(w, args)
     bits = w.layer_bits(args.layer)
     pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [bits])
     K, V = wl.layer_kv_torch(w, args.layer, "cuda")
@@ -40,6 +46,31 @@ def main() -> int:
     torch.cuda.synchronize()
     st = pool.status()
     print(f"{args.workload} layer {args.layer} ({bits}-bit): {args.reps} repetitions, status {st}")
+    pool.close()
+    return 0 if st == 0 else 1
+
+
+def multi(w, args) -> int:
+    n = min(args.layers, w.layers)
+    bits = [w.layer_bits(l) for l in range(n)]
+    pool = kp.KVPool(n, w.kv_heads, w.head_dim, w.ctx, bits)
+    KV = [wl.layer_kv_torch(w, l, "cuda") for l in range(n)]
+    Ks, Vs = [k for k, _ in KV], [v for _, v in KV]
+    Q = [torch.from_numpy(wl.layer_q(w, l).view(np.int16)).cuda().view(torch.bfloat16) for l in range(n)]
+    out = torch.empty((w.agents, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
+    Kd = [torch.empty_like(k) for k in Ks]
+    Vd = [torch.empty_like(v) for v in Vs]
+    layers = list(range(n))
+    for _ in range(args.reps):
+        for l in layers:
+            pool.reset_layer(l)
+        pool.compress_layers(layers, Ks, Vs)
+        for l in layers:
+            pool.attend(l, Q[l], out)
+        pool.decompress_layers(layers, Kd, Vd)
+    torch.cuda.synchronize()
+    st = pool.status()
+    print(f"{args.workload} layers 0..{n - 1} (multi-layer calls): {args.reps} repetitions, status {st}")
     pool.close()
     return 0 if st == 0 else 1
 
