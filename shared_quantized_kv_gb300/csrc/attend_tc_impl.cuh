@@ -75,6 +75,7 @@ constexpr uint32_t kBarWork = 1;            // named barrier of the worker warps
 constexpr uint64_t kWaitNs = 200ull * 1000 * 1000;
 constexpr uint32_t kCols = 512;             // TMEM: O^T, S^T per chunk tile, K^/V^T per chunk tile
 constexpr int kMaxChunk = 3;
+constexpr int kMaxCluster = 16;             // CTAs per cluster (context splits of one KV head)
 
 struct TcParams {
     const uint8_t* vcodes;
@@ -865,13 +866,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     ptx::fence_proxy_async();
     __syncthreads();
 
-    // 5. send row r to the owner of its agent: slot (this rank, owner's row index)
+    // 5. send the G rows of each agent, consecutive here and at the owner of
+    //    the agent, with one copy: slots (this rank, owner's row index)
+    const int nsend = nrows / p.G;  // row groups hold whole agents
     ptx::cluster_wait();
-    if (tid < nrows) {
-        const uint32_t ow = sOwn[tid], owner = ow >> 16;
+    if (tid < nsend) {
+        const uint32_t ow = sOwn[tid * p.G], owner = ow >> 16;
         const float* dst = slots + (size_t)(crank * p.own + (int)(ow & 0xFFFF)) * ROWF;
-        ptx::bulk_s2cluster(ptx::dsmem_addr(dst, owner), ptx::smem_u32(sO + tid * ROWF), ROWF * 4,
-                            ptx::dsmem_addr(bars + p.nstage + 2, owner));
+        ptx::bulk_s2cluster(ptx::dsmem_addr(dst, owner), ptx::smem_u32(sO + tid * p.G * ROWF),
+                            (uint32_t)(p.G * ROWF * 4), ptx::dsmem_addr(bars + p.nstage + 2, owner));
         ptx::bulk_commit();
     }
 
@@ -885,32 +888,41 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             const int ar = (loc / G) * S + crank, j = loc % G;
             const int rr = ar * G + j;
             const int a = row0 / G + ar;
-            float Ms = -CUDART_INF_F, Ls = 0.f;
-            if (lane < S) {
-                const float2 ml = *reinterpret_cast<const float2*>(slots + (size_t)(lane * p.own + loc) * ROWF + D);
-                Ms = ml.x;
-                Ls = ml.y;
+            // every lane reads the S (m, l) pairs itself (broadcast loads)
+            // and all S partial rows at once: no shuffle chains
+            float ms[kMaxCluster], ls[kMaxCluster];
+#pragma unroll
+            for (int s = 0; s < kMaxCluster; ++s) {
+                ms[s] = -CUDART_INF_F;
+                ls[s] = 0.f;
+                if (s < S) {
+                    const float2 ml = *reinterpret_cast<const float2*>(slots + (size_t)(s * p.own + loc) * ROWF + D);
+                    ms[s] = ml.x;
+                    ls[s] = ml.y;
+                }
             }
-            float M = (Ls > 0.f) ? Ms : -CUDART_INF_F;
+            float M = -CUDART_INF_F;
 #pragma unroll
-            for (int o2 = 16; o2; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
-            const float wl = (Ls > 0.f) ? ptx::ex2(Ms - M) : 0.f;
-            float L = wl * Ls;
-#pragma unroll
-            for (int o2 = 16; o2; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
+            for (int s = 0; s < kMaxCluster; ++s)
+                if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
+            float L = 0.f;
             float acc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float w = __shfl_sync(0xffffffffu, wl, s);
-                const float* src = slots + (size_t)(s * p.own + loc) * ROWF + lane * EPL;
-                if constexpr (EPL == 4) {
-                    const float4 v = *reinterpret_cast<const float4*>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-                    acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-                } else {
-                    const float2 v = *reinterpret_cast<const float2*>(src);
-                    acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+#pragma unroll
+            for (int s = 0; s < kMaxCluster; ++s) {
+                if (s < S) {
+                    const float w = (ls[s] > 0.f) ? ptx::ex2(ms[s] - M) : 0.f;
+                    L = fmaf(w, ls[s], L);
+                    const float* src = slots + (size_t)(s * p.own + loc) * ROWF + lane * EPL;
+                    if constexpr (EPL == 4) {
+                        const float4 v = *reinterpret_cast<const float4*>(src);
+                        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+                        acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
+                    } else {
+                        const float2 v = *reinterpret_cast<const float2*>(src);
+                        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
+                    }
                 }
             }
             // inverse rotation H acc; lane holds EPL consecutive channels
@@ -956,7 +968,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             for (int e = 0; e < EPL; ++e) orow[e] = (acc[e] * oscale * wp + tacc[e] * wt) * inv;
         }
     }
-    if (tid < nrows) ptx::bulk_wait_read();  // the staging row may be released
+    if (tid < nsend) ptx::bulk_wait_read();  // the staging rows may be released
 }
 
 
@@ -1018,7 +1030,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk
     // the staging rows and the merge slots must fit in the stage area
     int bestS = 0;
     long long best = -1;
-    for (int S = 1; S <= 16 && S <= ntiles; ++S) {
+    for (int S = 1; S <= kMaxCluster && S <= ntiles; ++S) {
         const int per = (ntiles + S - 1) / S;
         const int own = (agents_cta + S - 1) / S * prm.G;
         const Layout lay = make_layout(D, BITS, W, std::min(max_ns, per));
