@@ -354,17 +354,34 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
     (attention outputs and the decompressed K/V) copied back, inside the timed
     region. Layers are independent, so the step is pipelined over three
     streams: the inputs of layer l go up while layer l-1 computes and the
-    results of layer l-2 come down. One step (copies included) is captured
-    as a CUDA graph and replayed, as a serving loop would."""
+    results of layer l-2 come down. Each layer's inputs (K, V, Q) sit in one
+    pinned host buffer and one device buffer, and so do its results, so a
+    layer moves with one copy each way. One step (copies included) is
+    captured as a CUDA graph and replayed, as a serving loop would."""
     import torch
 
     L = w.layers
-    hK = [k.cpu().pin_memory() for k in K]
-    hV = [v.cpu().pin_memory() for v in V]
-    hQ = [q.cpu().pin_memory() for q in Q]
-    hout = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in out]
-    hKd = [torch.empty(k.shape, dtype=k.dtype, pin_memory=True) for k in Kd]
-    hVd = [torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for v in Vd]
+    dev = K[0].device
+
+    def packed(parts):
+        # one byte buffer per layer holding `parts` back to back (16-byte aligned
+        # offsets), and a view of each part in it
+        sizes = [t.numel() * t.element_size() for t in parts]
+        buf = torch.empty(sum(sizes), dtype=torch.uint8, device=dev)
+        views, off = [], 0
+        for t, n in zip(parts, sizes):
+            views.append(buf[off:off + n].view(t.dtype).view(t.shape))
+            off += n
+        return buf, views
+
+    dIn, dOut, kv_in, kv_out = [], [], [], []
+    for l in range(L):
+        b_in, (k, v, q) = packed([K[l], V[l], Q[l]])
+        k.copy_(K[l]); v.copy_(V[l]); q.copy_(Q[l])
+        b_out, (o, kd, vd) = packed([out[l], Kd[l], Vd[l]])
+        dIn.append(b_in); dOut.append(b_out); kv_in.append((k, v, q)); kv_out.append((o, kd, vd))
+    hIn = [b.cpu().pin_memory() for b in dIn]
+    hOut = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in dOut]
     s_main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_in = [torch.cuda.Event() for _ in range(L)]
     ev_done = [torch.cuda.Event() for _ in range(L)]
@@ -375,23 +392,21 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
         s_out.wait_stream(s_main)
         with torch.cuda.stream(s_in):
             for l in range(L):
-                K[l].copy_(hK[l], non_blocking=True)
-                V[l].copy_(hV[l], non_blocking=True)
-                Q[l].copy_(hQ[l], non_blocking=True)
+                dIn[l].copy_(hIn[l], non_blocking=True)
                 ev_in[l].record(s_in)
         for l in range(L):
+            k, v, q = kv_in[l]
+            o, kd, vd = kv_out[l]
             s_main.wait_event(ev_in[l])
             pool.reset_layer(l)
-            pool.compress(l, K[l], V[l], stream=s_main)
-            pool.attend(l, Q[l], out[l], tail[l] if tail else None, stream=s_main)
-            pool.decompress(l, Kd[l], Vd[l], stream=s_main)
+            pool.compress(l, k, v, stream=s_main)
+            pool.attend(l, q, o, tail[l] if tail else None, stream=s_main)
+            pool.decompress(l, kd, vd, stream=s_main)
             ev_done[l].record(s_main)
         with torch.cuda.stream(s_out):
             for l in range(L):
                 s_out.wait_event(ev_done[l])
-                hout[l].copy_(out[l], non_blocking=True)
-                hKd[l].copy_(Kd[l], non_blocking=True)
-                hVd[l].copy_(Vd[l], non_blocking=True)
+                hOut[l].copy_(dOut[l], non_blocking=True)
         s_main.wait_stream(s_in)
         s_main.wait_stream(s_out)
 
@@ -413,12 +428,12 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in hK + hV + hQ)
-    d2h = sum(t.numel() * t.element_size() for t in hout + hKd + hVd)
+    h2d = sum(t.numel() * t.element_size() for t in hIn)
+    d2h = sum(t.numel() * t.element_size() for t in hOut)
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": round(w.agents * ws / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "one CUDA graph per step: three streams pipelined over layers (upload, compute, download)"}
+            "how": "one CUDA graph per step: three streams pipelined over layers (upload, compute, download), one copy per layer each way"}
 
 
 # ------------------------------------------------------------------ CPU legs
