@@ -354,9 +354,10 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
     (attention outputs and the decompressed K/V) copied back, inside the timed
     region. Layers are independent, so the step is pipelined over three
     streams: the inputs of layer l go up while layer l-1 computes and the
-    results of layer l-2 come down. Each layer's inputs (K, V, Q) sit in one
-    pinned host buffer and one device buffer, and so do its results, so a
-    layer moves with one copy each way. One step (copies included) is
+    results of layer l-2 come down. The inputs (K, V, Q) of each chunk of
+    --e2e-chunk consecutive layers sit in one pinned host buffer and one
+    device buffer, and so do its results, so a chunk moves with one copy
+    each way. One step (copies included) is
     captured as a CUDA graph and replayed, as a serving loop would."""
     import torch
 
@@ -374,39 +375,47 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
             off += n
         return buf, views
 
-    dIn, dOut, kv_in, kv_out = [], [], [], []
-    for l in range(L):
-        b_in, (k, v, q) = packed([K[l], V[l], Q[l]])
-        k.copy_(K[l]); v.copy_(V[l]); q.copy_(Q[l])
-        b_out, (o, kd, vd) = packed([out[l], Kd[l], Vd[l]])
-        dIn.append(b_in); dOut.append(b_out); kv_in.append((k, v, q)); kv_out.append((o, kd, vd))
+    # copy chunks of `per` consecutive layers
+    per = max(1, args.e2e_chunk)
+    chunks = [list(range(c, min(L, c + per))) for c in range(0, L, per)]
+    dIn, dOut, kv_in, kv_out = [], [], {}, {}
+    for ls in chunks:
+        b_in, vin = packed([t for l in ls for t in (K[l], V[l], Q[l])])
+        b_out, vout = packed([t for l in ls for t in (out[l], Kd[l], Vd[l])])
+        for i, l in enumerate(ls):
+            k, v, q = vin[3 * i:3 * i + 3]
+            k.copy_(K[l]); v.copy_(V[l]); q.copy_(Q[l])
+            kv_in[l] = (k, v, q)
+            kv_out[l] = tuple(vout[3 * i:3 * i + 3])
+        dIn.append(b_in); dOut.append(b_out)
     hIn = [b.cpu().pin_memory() for b in dIn]
     hOut = [torch.empty(b.shape, dtype=b.dtype, pin_memory=True) for b in dOut]
     s_main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
-    ev_in = [torch.cuda.Event() for _ in range(L)]
-    ev_done = [torch.cuda.Event() for _ in range(L)]
+    ev_in = [torch.cuda.Event() for _ in chunks]
+    ev_done = [torch.cuda.Event() for _ in chunks]
 
     def step():
         # runs on s_main (the capturing stream); s_in and s_out fork from it and join it
         s_in.wait_stream(s_main)
         s_out.wait_stream(s_main)
         with torch.cuda.stream(s_in):
-            for l in range(L):
-                dIn[l].copy_(hIn[l], non_blocking=True)
-                ev_in[l].record(s_in)
-        for l in range(L):
-            k, v, q = kv_in[l]
-            o, kd, vd = kv_out[l]
-            s_main.wait_event(ev_in[l])
-            pool.reset_layer(l)
-            pool.compress(l, k, v, stream=s_main)
-            pool.attend(l, q, o, tail[l] if tail else None, stream=s_main)
-            pool.decompress(l, kd, vd, stream=s_main)
-            ev_done[l].record(s_main)
+            for c in range(len(chunks)):
+                dIn[c].copy_(hIn[c], non_blocking=True)
+                ev_in[c].record(s_in)
+        for c, ls in enumerate(chunks):
+            s_main.wait_event(ev_in[c])
+            for l in ls:
+                k, v, q = kv_in[l]
+                o, kd, vd = kv_out[l]
+                pool.reset_layer(l)
+                pool.compress(l, k, v, stream=s_main)
+                pool.attend(l, q, o, tail[l] if tail else None, stream=s_main)
+                pool.decompress(l, kd, vd, stream=s_main)
+            ev_done[c].record(s_main)
         with torch.cuda.stream(s_out):
-            for l in range(L):
-                s_out.wait_event(ev_done[l])
-                hOut[l].copy_(dOut[l], non_blocking=True)
+            for c in range(len(chunks)):
+                s_out.wait_event(ev_done[c])
+                hOut[c].copy_(dOut[c], non_blocking=True)
         s_main.wait_stream(s_in)
         s_main.wait_stream(s_out)
 
@@ -433,7 +442,8 @@ def run_e2e(args, pool, w, K, V, Q, tail, out, Kd, Vd, phases):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     return {"value": round(w.agents * ws / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "one CUDA graph per step: three streams pipelined over layers (upload, compute, download), one copy per layer each way"}
+            "how": "one CUDA graph per step: three streams pipelined over layers (upload, compute, download), "
+                   f"one copy per {per} layer(s) each way"}
 
 
 # ------------------------------------------------------------------ CPU legs
@@ -524,6 +534,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--no-e2e", action="store_true", help="skip the end-to-end leg")
+    ap.add_argument("--e2e-chunk", type=int, default=1,
+                    help="end-to-end leg: layers per host<->device copy (default 1)")
     ap.add_argument("--per-layer-calls", action="store_true",
                     help="compress and decompress one layer per call (default: all layers in one call)")
     ap.add_argument("--k-block", type=int, default=0, choices=[0, 32],
