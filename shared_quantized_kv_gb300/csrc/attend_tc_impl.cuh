@@ -299,6 +299,13 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
     float* tq = reinterpret_cast<float*>(stage);                                // [8][D]
     float* tl = reinterpret_cast<float*>(stage + 8 * D * 4);                   // [8][TCH]
     float* tmx = reinterpret_cast<float*>(stage + 8 * D * 4 + 8 * TCH * 4);    // [8]
+    // P.V: VR tail V rows at a time through shared memory (the next block's
+    // loads in flight while this one is used), VCH 16-byte chunks per block
+    constexpr int VR = 64;
+    constexpr int VCH = VR * D / 8;
+    constexpr int VPT = VCH / kWorkers;  // chunks per worker thread
+    static_assert(VCH % kWorkers == 0, "V block chunks per worker");
+    uint4* tv = reinterpret_cast<uint4*>(stage + 8 * D * 4 + 8 * TCH * 4 + 64);  // [VR][D] bf16
     const int c = tid % D, sub = tid / D;      // P.V phase: rows k with k % RPT == sub, channel c
     const int t = tid % TCH, k0 = tid / TCH;   // logit phase: token t, rows k0 + 2 * kk
     const int G = p.G;
@@ -317,28 +324,35 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
             for (int k = 0; k < 8; ++k) { m_run[k] = -CUDART_INF_F; l_run[k] = 0.f; acc[k] = 0.f; }
             __syncthreads();
             for (int c0 = 0; c0 < tmax; c0 += TCH) {
-                float lg[4];
+                // logits of token t for this thread's rows: each 16-byte chunk of
+                // the K row is loaded once and used for every row (per row, the
+                // products are summed in channel order)
+                float lg[4], dot[4];
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) dot[kk] = 0.f;
+                const bool tok_ok = worker && c0 + t < tmax;
+                if (tok_ok) {
+                    const uint16_t* kr = p.tK + (tbase + c0 + t) * D;
+#pragma unroll 2
+                    for (int cc = 0; cc < D; cc += 8) {
+                        const uint4 u = *reinterpret_cast<const uint4*>(kr + cc);
+                        const float kv[8] = {bf2f(u.x & 0xFFFF), bf2f(u.x >> 16), bf2f(u.y & 0xFFFF), bf2f(u.y >> 16),
+                                             bf2f(u.z & 0xFFFF), bf2f(u.z >> 16), bf2f(u.w & 0xFFFF), bf2f(u.w >> 16)};
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const int k = k0 + 2 * kk;
+                            if (k < cnt) {
+                                const float* qq = tq + k * D + cc;
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) dot[kk] = fmaf(qq[e], kv[e], dot[kk]);
+                            }
+                        }
+                    }
+                }
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
                     const int k = k0 + 2 * kk;
-                    lg[kk] = -CUDART_INF_F;
-                    if (worker && k < cnt && c0 + t < tmax) {
-                        const uint16_t* kr = p.tK + (tbase + c0 + t) * D;
-                        const float* qq = tq + k * D;
-                        float dot = 0.f;
-                        for (int cc = 0; cc < D; cc += 8) {
-                            const uint4 u = *reinterpret_cast<const uint4*>(kr + cc);
-                            dot = fmaf(qq[cc + 0], bf2f(u.x & 0xFFFF), dot);
-                            dot = fmaf(qq[cc + 1], bf2f(u.x >> 16), dot);
-                            dot = fmaf(qq[cc + 2], bf2f(u.y & 0xFFFF), dot);
-                            dot = fmaf(qq[cc + 3], bf2f(u.y >> 16), dot);
-                            dot = fmaf(qq[cc + 4], bf2f(u.z & 0xFFFF), dot);
-                            dot = fmaf(qq[cc + 5], bf2f(u.z >> 16), dot);
-                            dot = fmaf(qq[cc + 6], bf2f(u.w & 0xFFFF), dot);
-                            dot = fmaf(qq[cc + 7], bf2f(u.w >> 16), dot);
-                        }
-                        lg[kk] = __fmul_rn(dot, p.scale_log2);
-                    }
+                    lg[kk] = (tok_ok && k < cnt) ? __fmul_rn(dot[kk], p.scale_log2) : -CUDART_INF_F;
                     if (worker) tl[k * TCH + t] = lg[kk];
                 }
                 __syncthreads();
@@ -369,23 +383,54 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
                     }
                 }
                 __syncthreads();
-                if (worker) {
-                    const uint16_t* vr0 = p.tV + (tbase + c0) * D + c;
+                {
                     const int n2 = min(TCH, tmax - c0);
+                    auto vload = [&](int tb, uint4 (&u)[VPT]) {
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
-                        if (k % RPT != sub || k >= cnt) continue;
-                        float sacc = 0.f, ls = 0.f;
-                        for (int t2 = 0; t2 < n2; ++t2) {
-                            const float pv = tl[k * TCH + t2];
-                            sacc = fmaf(pv, bf2f(vr0[(long long)t2 * D]), sacc);
-                            ls += pv;
+                        for (int i = 0; i < VPT; ++i) {
+                            const int ch = tid + i * kWorkers, row = tb + ch / (D / 8);
+                            u[i] = make_uint4(0, 0, 0, 0);
+                            if (worker && row < n2)
+                                u[i] = *reinterpret_cast<const uint4*>(p.tV + (tbase + c0 + row) * D + (ch % (D / 8)) * 8);
                         }
-                        acc[k] = acc[k] * alpha[k] + sacc;
-                        l_run[k] = l_run[k] * alpha[k] + ls;
+                    };
+                    constexpr int KPT = (8 + RPT - 1) / RPT;  // rows of this thread: k % RPT == sub
+                    float sacc[KPT], ls[KPT];
+#pragma unroll
+                    for (int k = 0; k < KPT; ++k) { sacc[k] = 0.f; ls[k] = 0.f; }
+                    uint4 nxt[VPT];
+                    vload(0, nxt);
+                    for (int tb = 0; tb < n2; tb += VR) {
+                        if (worker) {
+#pragma unroll
+                            for (int i = 0; i < VPT; ++i) tv[tid + i * kWorkers] = nxt[i];
+                        }
+                        __syncthreads();
+                        if (tb + VR < n2) vload(tb + VR, nxt);
+                        if (worker) {
+                            const uint16_t* tv16 = reinterpret_cast<const uint16_t*>(tv) + c;
+                            const int nb = min(VR, n2 - tb);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k) {
+                                if (k % RPT != sub || k >= cnt) continue;
+                                for (int u = 0; u < nb; ++u) {  // token order, as one chain
+                                    const float pv = tl[k * TCH + tb + u];
+                                    sacc[k / RPT] = fmaf(pv, bf2f(tv16[u * D]), sacc[k / RPT]);
+                                    ls[k / RPT] += pv;
+                                }
+                            }
+                        }
+                        __syncthreads();
+                    }
+                    if (worker) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (k % RPT != sub || k >= cnt) continue;
+                            acc[k] = acc[k] * alpha[k] + sacc[k / RPT];
+                            l_run[k] = l_run[k] * alpha[k] + ls[k / RPT];
+                        }
                     }
                 }
-                __syncthreads();
             }
             if (worker) {
 #pragma unroll
@@ -404,7 +449,8 @@ __device__ __noinline__ void tail_attention(const TcParams& p, unsigned char* st
     }
 }
 
-template <int D, int W, int BITS>
+// TAIL: the call has private bf16 tails (instances without them hold no tail code)
+template <int D, int W, int BITS, bool TAIL>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     constexpr int CPT = W / kGroups;         // query rows (TMEM columns) per worker thread: 4..32
@@ -565,7 +611,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 
     // 2. tails of the agents this CTA owns (CUDA cores), overlapping the first
     //    copies; the P' area is free until the first softmax
-    if (p.tK != nullptr) tail_attention<D>(p, sP, tailml, S, crank, g, row0, nrows);
+    if constexpr (TAIL) tail_attention<D>(p, sP, tailml, S, crank, g, row0, nrows);
     ptx::fence_proxy_async();
     ptx::tc_fence_before();
     __syncthreads();
@@ -952,7 +998,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
             float tacc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) tacc[e] = 0.f;
-            if (p.tK != nullptr) {
+            if (TAIL) {
                 mt = tailml[2 * rr];
                 lt = tailml[2 * rr + 1];
                 if (lt > 0.f) {
@@ -972,23 +1018,23 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
 }
 
 
-template <int D, int W, int BITS>
+template <int D, int W, int BITS, bool TAIL>
 void configure() {
     static bool done = false;
     if (done) return;
-    auto kern = attend_tc_kernel<D, W, BITS>;
+    auto kern = attend_tc_kernel<D, W, BITS, TAIL>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     done = true;
 }
 
 // How many clusters of S CTAs with `smem` bytes each can be resident at once.
-template <int D, int W, int BITS>
+template <int D, int W, int BITS, bool TAIL>
 int max_clusters(int S, size_t smem) {
     static int cache[17][2] = {};  // [S] -> (smem key / 1024 + 1, count)
     const int key = (int)(smem / 1024) + 1;
     if (cache[S][0] == key) return cache[S][1];
-    configure<D, W, BITS>();
+    configure<D, W, BITS, TAIL>();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1001,7 +1047,7 @@ int max_clusters(int S, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel<D, W, BITS>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attend_tc_kernel<D, W, BITS, TAIL>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -1010,9 +1056,9 @@ int max_clusters(int S, size_t smem) {
     return n;
 }
 
-template <int D, int W, int BITS>
+template <int D, int W, int BITS, bool TAIL>
 cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
-    configure<D, W, BITS>();
+    configure<D, W, BITS, TAIL>();
     constexpr uint32_t kMaxSmem = 227 * 1024;
     // one CTA per SM (it uses all 512 TMEM columns): the floor on shared
     // memory keeps a second CTA off the SM, where it would wait in
@@ -1036,7 +1082,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk
         const Layout lay = make_layout(D, BITS, W, std::min(max_ns, per));
         if (staging_bytes(D, W) + (size_t)S * own * (D + 4) * 4 > lay.misc) continue;
         const size_t smem = std::max<size_t>(lay.total + 1024, kFloor);
-        const int n = max_clusters<D, W, BITS>(S, smem);
+        const int n = max_clusters<D, W, BITS, TAIL>(S, smem);
         if (n < 1) continue;
         const long long waves = (clusters + n - 1) / n;
         const long long cost = waves * per;
@@ -1070,7 +1116,22 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, TcParams prm, int ntiles, int Hk
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attend_tc_kernel<D, W, BITS>, kmap, prm);
+    return cudaLaunchKernelEx(&cfg, attend_tc_kernel<D, W, BITS, TAIL>, kmap, prm);
+}
+
+template <bool TAIL, int BITS>
+cudaError_t launch_w(const CUtensorMap& km, const TcParams& prm, int D, int W, int ntiles, int Hk, int RGN,
+                     cudaStream_t st) {
+    if (D == 64) {
+        if (W == 16) return launch_cfg<64, 16, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+        if (W == 32) return launch_cfg<64, 32, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+        if (W == 64) return launch_cfg<64, 64, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+        return launch_cfg<64, 128, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+    }
+    if (W == 16) return launch_cfg<128, 16, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+    if (W == 32) return launch_cfg<128, 32, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+    if (W == 64) return launch_cfg<128, 64, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
+    return launch_cfg<128, 128, BITS, TAIL>(km, prm, ntiles, Hk, RGN, st);
 }
 
 }  // namespace
@@ -1116,16 +1177,8 @@ cudaError_t launch_attend_tc_bits(const Shape& s, const LayerBufs& L, const Atte
     }
     prm.inv_lam = 1.0f / cb.lam;
     const CUtensorMap& km = *L.kmap;
-    if (D == 64) {
-        if (W == 16) return launch_cfg<64, 16, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-        if (W == 32) return launch_cfg<64, 32, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-        if (W == 64) return launch_cfg<64, 64, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-        return launch_cfg<64, 128, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-    }
-    if (W == 16) return launch_cfg<128, 16, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-    if (W == 32) return launch_cfg<128, 32, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-    if (W == 64) return launch_cfg<128, 64, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
-    return launch_cfg<128, 128, BITS>(km, prm, ntiles, s.kv_heads, RGN, st);
+    if (prm.tK != nullptr) return launch_w<true, BITS>(km, prm, D, W, ntiles, s.kv_heads, RGN, st);
+    return launch_w<false, BITS>(km, prm, D, W, ntiles, s.kv_heads, RGN, st);
 }
 
 }  // namespace kvp
