@@ -73,4 +73,10 @@ def test_null_pool_calls(kp):
     assert lib.kvpool_compress(None, 0, None, None, None) == -1
     assert lib.kvpool_attend(None, 0, None, 1, 1, None, None, 0.0, None) == -1
     assert lib.kvpool_decompress(None, 0, None, None, None) == -1
+    lay = (ctypes.c_int * 2)(0, 1)
+    ptrs = (ctypes.c_void_p * 2)(16, 32)
+    assert lib.kvpool_compress_layers(None, 2, lay, ptrs, ptrs, None) == -1
+    assert lib.kvpool_decompress_layers(None, 2, lay, ptrs, ptrs, None) == -1
+    assert lib.kvpool_append(None, 0, None, None, 1, None) == -1
+    assert lib.kvpool_layer_len(None, 0) == -1
     lib.kvpool_destroy(None)

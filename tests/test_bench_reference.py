@@ -29,3 +29,17 @@ def test_reference_line():
 
     want = bench.workload_config(wl.WORKLOADS["smollm2_2k"], 1, 0)
     assert {k: d["config"][k] for k in want} == want
+
+
+def test_launch_count_by_call_structure():
+    sys.path.insert(0, ROOT)
+    import bench
+    from shared_quantized_kv_gb300 import workloads as wl
+
+    llama = wl.WORKLOADS["llama3_8b_4k"]  # 32 layers, all 3-bit
+    assert bench.launches_per_step(llama, 0, False) == {"compress": 2, "attend": 32, "decompress": 1}
+    assert bench.launches_per_step(llama, 0, True) == {"compress": 64, "attend": 32, "decompress": 32}
+    assert bench.launches_per_step(llama, 32, False)["attend"] == 64  # split + combine per layer
+    qwen = wl.WORKLOADS["qwen3_32b_32k"]  # 64 layers, 2/3/4 bits: two launch chunks of 32 layers
+    widths = sum(len(set(qwen.bits_list()[c:c + 32])) for c in (0, 32))
+    assert bench.launches_per_step(qwen, 0, False) == {"compress": 2 + widths, "attend": 64, "decompress": widths}
