@@ -125,13 +125,16 @@ __device__ __forceinline__ uint32_t absmax8(uint4 u) {
 }
 
 // max|K| of each layer of the launch: CTA (b, l) reduces the b-th contiguous
-// slice of layer l's K tensor (16-byte chunks) to a partial maximum; the last
-// CTA of the layer to finish (an arrival counter, re-armed by that CTA)
-// reduces the partials and writes max|K| (bf16 bits), s = max|K| / 127 (1
-// when K is all zero) and 1/s. It releases the encode kernel at once. For
-// block-scaled layers it only sets *kscale = 1 and clears the maxima.
+// slice of layer l's K tensor (16-byte chunks) to a partial maximum. With
+// several layers (NB > 1) the last CTA of a layer to finish (an arrival
+// counter, re-armed by that CTA) reduces the partials and writes max|K|
+// (bf16 bits), s = max|K| / 127 (1 when K is all zero) and 1/s; for one layer
+// the encode kernel's CTAs reduce them themselves. It releases the encode
+// kernel at once. For block-scaled layers it only sets *kscale = 1 and clears
+// the maxima.
+template <int NB>
 __global__ void __launch_bounds__(256)
-kmax_kernel(const __grid_constant__ EncBatch b, long long nchunk, long long per_cta, int kb, int zero_vn,
+kmax_kernel(const __grid_constant__ EncBatchT<NB> b, long long nchunk, long long per_cta, int kb, int zero_vn,
             int* __restrict__ status) {
     ptx::grid_dep_launch();
     const EncLayer& L = b.L[blockIdx.y];
@@ -164,9 +167,12 @@ kmax_kernel(const __grid_constant__ EncBatch b, long long nchunk, long long per_
 #pragma unroll
         for (int w = 1; w < 8; ++w) m = max(m, red[w]);
         L.kpart[blockIdx.x] = m;
-        __threadfence();  // the partial before the arrival
-        last = atomicAdd(L.kpart + kKmaxCount, 1u) == gridDim.x - 1;
+        if constexpr (NB > 1) {
+            __threadfence();  // the partial before the arrival
+            last = atomicAdd(L.kpart + kKmaxCount, 1u) == gridDim.x - 1;
+        }
     }
+    if constexpr (NB == 1) return;
     __syncthreads();
     if (!last) return;
     __threadfence();
@@ -192,10 +198,10 @@ kmax_kernel(const __grid_constant__ EncBatch b, long long nchunk, long long per_
 // items i, i + G, ... in two passes: first the V of every item (beside the
 // max|K| kernel), then, after the dependency wait, the K of every item.
 // KB: block-scaled K (one scale per 32 elements, written to kscales).
-template <int D, int BITS, bool KB>
+template <int D, int BITS, bool KB, int NB>
 __global__ void __launch_bounds__(kEncThreads)
-encode_kernel(const __grid_constant__ EncBatch b, int ctx, int ctx_pad, int t_base, int items_per_head,
-              int items_per_layer, int items, int* __restrict__ status, Codebook cb) {
+encode_kernel(const __grid_constant__ EncBatchT<NB> b, int ctx, int ctx_pad, int t_base, int items_per_head,
+              int items_per_layer, int items, int nparts, int* __restrict__ status, Codebook cb) {
     constexpr int TPV = D / 32;              // threads per head-vector
     constexpr int VPI = kEncThreads / TPV;   // tokens per item (a multiple of 32)
     constexpr uint32_t kTile = VPI * D * 2;  // bytes of K (and of V) per item: 8 KB
@@ -388,6 +394,25 @@ encode_kernel(const __grid_constant__ EncBatch b, int ctx, int ctx_pad, int t_ba
     // ---- pass 2: K. The max|K| kernel is complete: s and 1/s of every layer
     // are written and the largest-V-norm words cleared.
     ptx::grid_dep_wait();
+    float s1 = 1.0f, r1 = 1.0f;  // one layer: s and 1/s from the partial maxima
+    if constexpr (NB == 1 && !KB) {
+        const EncLayer& Ly = b.L[0];
+        uint32_t m = 0;
+        for (int i = tid; i < nparts; i += kEncThreads) m = max(m, Ly.kpart[i]);
+        m = __reduce_max_sync(gmask, m);
+        __syncthreads();  // thread 0 may still read red[] of the last V item
+        if (lane == 0) red[tid / 32] = m;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kEncThreads / 32; ++w) m = max(m, red[w]);
+        s1 = (m == 0) ? 1.0f : __fdiv_rn(__uint_as_float(m << 16), 127.0f);
+        r1 = __frcp_rn(s1);
+        if (blockIdx.x == 0 && tid == 0) {
+            *Ly.kscale = s1;
+            Ly.maxima[0] = m;
+            if (m >= 0x7F80u) atomicOr(status, kStNonfinite);
+        }
+    }
     for (int it = blockIdx.x, k = 0; it < items; it += G, ++k) {
         const int t = m + k;
         const unsigned char* sK = tiles[t & 1];
@@ -399,8 +424,8 @@ encode_kernel(const __grid_constant__ EncBatch b, int ctx, int ctx_pad, int t_ba
             if (nm > *reinterpret_cast<volatile uint32_t*>(&Ly.maxima[1])) atomicMax(&Ly.maxima[1], nm);
             if (nm >= 0x7F800000u) atomicOr(status, kStNonfinite);
         }
-        float s = 1.0f, r = 1.0f;
-        if constexpr (!KB) {
+        float s = s1, r = r1;
+        if constexpr (!KB && NB > 1) {
             s = *Ly.kscale;
             r = __uint_as_float(Ly.kpart[kKmaxInv]);
         }
@@ -444,11 +469,11 @@ encode_kernel(const __grid_constant__ EncBatch b, int ctx, int ctx_pad, int t_ba
     if (tid == 0 && !ok) atomicOr(status, kStTimeout);
 }
 
-template <int D, int BITS>
-cudaError_t run_encode(const Shape& s, const EncBatch& b, int* status, int sm_count, int t_base, bool kb,
-                       cudaStream_t st) {
+template <int D, int BITS, int NB>
+cudaError_t run_encode(const Shape& s, const EncBatchT<NB>& b, int* status, int sm_count, int t_base, bool kb,
+                       int nparts, cudaStream_t st) {
     constexpr int VPI = kEncThreads / (D / 32);
-    auto kern = kb ? encode_kernel<D, BITS, true> : encode_kernel<D, BITS, false>;
+    auto kern = kb ? encode_kernel<D, BITS, true, NB> : encode_kernel<D, BITS, false, NB>;
     const int items_per_head = (s.ctx + VPI - 1) / VPI;
     const int items_per_layer = s.kv_heads * items_per_head;
     const long long items_ll = (long long)b.n * items_per_layer;
@@ -483,15 +508,15 @@ cudaError_t run_encode(const Shape& s, const EncBatch& b, int* status, int sm_co
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, b, s.ctx, s.ctx_pad, t_base, items_per_head, items_per_layer, items,
-                              status, codebook(BITS));
+                              nparts, status, codebook(BITS));
 }
 
-template <int D>
-cudaError_t run_bits(int bits, const Shape& s, const EncBatch& b, int* status, int sm_count, int t_base, bool kb,
-                     cudaStream_t st) {
-    if (bits == 2) return run_encode<D, 2>(s, b, status, sm_count, t_base, kb, st);
-    if (bits == 3) return run_encode<D, 3>(s, b, status, sm_count, t_base, kb, st);
-    return run_encode<D, 4>(s, b, status, sm_count, t_base, kb, st);
+template <int D, int NB>
+cudaError_t run_bits(int bits, const Shape& s, const EncBatchT<NB>& b, int* status, int sm_count, int t_base, bool kb,
+                     int nparts, cudaStream_t st) {
+    if (bits == 2) return run_encode<D, 2, NB>(s, b, status, sm_count, t_base, kb, nparts, st);
+    if (bits == 3) return run_encode<D, 3, NB>(s, b, status, sm_count, t_base, kb, nparts, st);
+    return run_encode<D, 4, NB>(s, b, status, sm_count, t_base, kb, nparts, st);
 }
 
 EncLayer enc_layer(const LayerBufs& L, const void* K, const void* V) {
@@ -531,34 +556,49 @@ cudaError_t launch_norm_max(const Shape& s, const LayerBufs& L, cudaStream_t st)
     return cudaGetLastError();
 }
 
+namespace {
+
+// max|K| and encode launches for nc layers of a table of capacity NB
+template <int NB>
+cudaError_t launch_chunk(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V, int nc,
+                         int* status, int sm_count, int t_base, cudaStream_t st) {
+    const bool kb = L[0].kscales != nullptr;
+    // max|K| of every layer in one launch: about two CTAs per SM in all, so
+    // that they are all running when the encode kernel starts
+    EncBatchT<NB> all = {};
+    all.n = nc;
+    for (int i = 0; i < nc; ++i) all.L[i] = enc_layer(L[i], K[i], V[i]);
+    const long long nchunk = (long long)s.kv_heads * s.ctx * (s.head_dim / 8);
+    const int gx = kb ? 1 : std::max(1, std::min(kKmaxInv, (2 * sm_count + nc - 1) / nc));
+    const long long per_cta = (nchunk + gx - 1) / gx;
+    kmax_kernel<NB><<<dim3(gx, nc), 256, 0, st>>>(all, nchunk, per_cta, kb ? 1 : 0, t_base == 0 ? 1 : 0, status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // one encode launch per V width among the layers
+    for (int bits = 2; bits <= 4; ++bits) {
+        EncBatchT<NB> sub = {};
+        for (int i = 0; i < nc; ++i)
+            if (L[i].bits == bits) sub.L[sub.n++] = all.L[i];
+        if (sub.n == 0) continue;
+        e = s.head_dim == 64 ? run_bits<64, NB>(bits, s, sub, status, sm_count, t_base, kb, gx, st)
+                             : run_bits<128, NB>(bits, s, sub, status, sm_count, t_base, kb, gx, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_encode_layers(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V,
                                  int n, int* status, int sm_count, int t_base, cudaStream_t st) {
     if (n < 1) return cudaErrorInvalidValue;
     const bool kb = L[0].kscales != nullptr;
     if (t_base != 0 && (!kb || n != 1 || t_base % 32 != 0)) return cudaErrorInvalidValue;
+    if (n == 1) return launch_chunk<1>(s, L, K, V, 1, status, sm_count, t_base, st);
     for (int c0 = 0; c0 < n; c0 += kEncBatch) {
         const int nc = std::min(kEncBatch, n - c0);
-        // max|K| of every layer of the chunk in one launch: about two CTAs per
-        // SM in all, so that they are all running when the encode kernel starts
-        EncBatch all = {};
-        all.n = nc;
-        for (int i = 0; i < nc; ++i) all.L[i] = enc_layer(L[c0 + i], K[c0 + i], V[c0 + i]);
-        const long long nchunk = (long long)s.kv_heads * s.ctx * (s.head_dim / 8);
-        const int gx = kb ? 1 : std::max(1, std::min(kKmaxInv, (2 * sm_count + nc - 1) / nc));
-        const long long per_cta = (nchunk + gx - 1) / gx;
-        kmax_kernel<<<dim3(gx, nc), 256, 0, st>>>(all, nchunk, per_cta, kb ? 1 : 0, t_base == 0 ? 1 : 0, status);
-        cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_chunk<kEncBatch>(s, L + c0, K + c0, V + c0, nc, status, sm_count, t_base, st);
         if (e != cudaSuccess) return e;
-        // one encode launch per V width among the chunk's layers
-        for (int bits = 2; bits <= 4; ++bits) {
-            EncBatch sub = {};
-            for (int i = 0; i < nc; ++i)
-                if (L[c0 + i].bits == bits) sub.L[sub.n++] = all.L[i];
-            if (sub.n == 0) continue;
-            e = s.head_dim == 64 ? run_bits<64>(bits, s, sub, status, sm_count, t_base, kb, st)
-                                 : run_bits<128>(bits, s, sub, status, sm_count, t_base, kb, st);
-            if (e != cudaSuccess) return e;
-        }
     }
     return cudaSuccess;
 }

@@ -72,10 +72,14 @@ struct EncLayer {
 };
 // Most layers per launch of the multi-layer kernels.
 constexpr int kEncBatch = 32;
-struct EncBatch {
+// A launch's layer table; one-layer calls pass the one-entry form (a smaller
+// parameter block, and the encode kernel reduces the partial maxima itself)
+template <int NB>
+struct EncBatchT {
     int n;
-    EncLayer L[kEncBatch];
+    EncLayer L[NB];
 };
+using EncBatch = EncBatchT<kEncBatch>;
 
 // s.ctx is the token count of K and V; t_base the pool token they start at
 // (non-zero only for appends to block-scaled layers, a multiple of 32).
