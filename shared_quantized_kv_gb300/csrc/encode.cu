@@ -48,7 +48,7 @@ namespace kvp {
 namespace {
 
 constexpr int kEncThreads = 128;
-constexpr uint64_t kEncWaitNs = 200ull * 1000 * 1000;  // bounded waits: copies, grid barrier
+constexpr uint64_t kEncWaitNs = 200ull * 1000 * 1000;  // bounded waits on the tile copies
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -7,8 +7,8 @@
 //                 vcodes uint8 [Hk][ctx_pad/32][D][4*bits_l] (32-token groups)
 //                 vnorm  f32   [Hk][ctx_pad]
 //   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits, largest
-//   V norm float bits}, per layer 512 partial maxima of max|K| (compress
-//   scratch), status int32. Block-scaled pools (kvpool_create_ex, k_block 32)
+//   V norm float bits}, per layer 512 words of compress scratch (partial
+//   maxima of max|K|, 1/s, the max|K| kernel's arrival counter), status int32. Block-scaled pools (kvpool_create_ex, k_block 32)
 //   also hold per layer kscales f32 [Hk][ctx_pad][D/32] and a split-context
 //   attention scratch.
 // Attention needs no scratch: the CTAs of a cluster merge their context
@@ -339,7 +339,7 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
     off = align256(off + 4 * (size_t)layers);
     const size_t off_absmax = off;  // per layer {max|K| bits, largest V norm bits}
     off = align256(off + 8 * (size_t)layers);
-    const size_t off_kpart = off;  // per layer: partial maxima of max|K| (compress scratch)
+    const size_t off_kpart = off;  // per layer: compress scratch (partial maxima, 1/s, arrival counter)
     off = align256(off + 4 * (size_t)kvp::kKmaxParts * layers);
     // block-scaled pools attend on CUDA cores: split scratch for max_rows rows,
     // about two splits per SM over the KV heads

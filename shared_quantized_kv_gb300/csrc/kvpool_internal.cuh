@@ -49,7 +49,7 @@ struct LayerBufs {
     int bits;
     uint32_t* vnmax;   // 1 word right after kabsmax: float bits of the largest V norm
     const CUtensorMap* kmap;  // TMA map of kq as rows of D bytes (128 / 64-byte swizzle), or null
-    uint32_t* kpart;          // [kKmaxParts] partial maxima of max|K| (compress scratch)
+    uint32_t* kpart;          // [kKmaxParts] compress scratch (see kKmaxParts)
     float* kscales;           // block-scaled K: [Hk][ctx_pad][D/32], one scale per 32 elements; else null
 };
 
