@@ -98,7 +98,8 @@ def _dist():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms (the
+    caller keeps the GPU busy with the timed work while it runs)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -271,9 +272,15 @@ def run_gpu(args):
     torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
+    # clocks: sampled every 200 ms while the same step runs untimed for about
+    # 0.6 s and then through the K timed steps (a timed region of a few ms
+    # alone would catch no sample under load)
     sampler = ClockSampler(local)
     sampler.start()
-    time.sleep(0.4)
+    t_load = time.perf_counter()
+    while time.perf_counter() - t_load < 0.6:
+        one_step([])
+        torch.cuda.synchronize()
     rec = []
     torch.cuda.synchronize()
     if ws > 1:
@@ -285,7 +292,7 @@ def run_gpu(args):
     if ws > 1:
         dist.barrier()
     t_wall = time.perf_counter() - t_wall
-    clocks = sampler.stop()
+    clocks = dict(sampler.stop(), window="0.6 s of the same step untimed, then the timed steps")
     assert pool.status() == 0
 
     ph_ms = {ph: 0.0 for ph in phases}
