@@ -43,11 +43,15 @@
 //       carries ~22 bits into the MMA; the tile's P'.V MMAs run while the
 //       next tile's P' is formed.
 //   epilogue: each CTA stages its partial rows (O^T column, m, l) in shared
-//     memory and sends each row with one bulk copy into the shared memory of
-//     the CTA that owns the row's agent, completing on the owner's mbarrier;
-//     each owner merges its rows (log-sum-exp), applies one inverse FWHT per
-//     row (warp shuffles), joins the agent's tail (computed in the prologue
-//     while the first tiles are in flight) and writes the row.
+//     memory and sends the rows of each agent (consecutive at both ends)
+//     with one bulk copy into the shared memory of the CTA that owns the
+//     agent, completing on the owner's mbarrier; each owner merges its rows
+//     (log-sum-exp), applies one inverse FWHT per row (warp shuffles), joins
+//     the agent's tail and writes the row.
+//   tails (instances with TAIL only): the owner CTA computes its agents' tail
+//     attention on CUDA cores in the prologue, while the first tiles are in
+//     flight; tail V rows pass through shared memory in blocks, the next
+//     block's loads in flight while one is used.
 // Every mbarrier wait is bounded; on expiry the kernel records
 // KVPOOL_ERR_TIMEOUT in the status word and carries on to its exit without
 // waiting again, so a fault never hangs the device.
