@@ -897,10 +897,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
     }
     ptx::tc_fence_before();
     __syncthreads();  // every MMA is done: the stage area becomes staging rows
-    if (warp == kIssuer) {
-        ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kCols);
-    }
     if (has_ch) {
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
@@ -1019,6 +1015,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap kmap, const TcParams p) {
         }
     }
     if (tid < nsend) ptx::bulk_wait_read();  // the staging rows may be released
+    // tensor memory is released last (nothing after the O^T loads uses it), so
+    // that its release is off the path to the sends and the merge
+    if (warp == kIssuer) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kCols);
+    }
 }
 
 
