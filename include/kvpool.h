@@ -270,6 +270,9 @@ int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view
  * ctx_padded = ctx rounded up to a multiple of 128): kq int8
  * [kv_heads][ctx_padded][head_dim], vcodes uint8 [kv_heads][ctx_padded/32]
  * [head_dim][4*bits], vnorm float [kv_heads][ctx_padded], kscale one float;
+ * kscales: NULL for a per-tensor layer, or a block-scaled layer's scales
+ * float [kv_heads][ctx_padded][head_dim/32] (kvpool_layer_view_t.kscales;
+ * *kscale, 1 in such a layer's view, multiplies every block scale);
  * Q, tail, out, softmax_scale and stream as in kvpool_attend. The result
  * equals kvpool_attend's on the same layer within float rounding.
  *
@@ -285,7 +288,8 @@ int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view
  * every byte a call reads from the array it has written first. Returns
  * KVPOOL_ERR_UNSUPPORTED on a device other than sm_103. */
 int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, const float* vnorm,
-                          const float* kscale, int kv_heads, int head_dim, int ctx, int bits,
+                          const float* kscale, const float* kscales, int kv_heads, int head_dim,
+                          int ctx, int bits,
                           const void* Q, int agents, int q_heads, const kvpool_tail_t* tail,
                           float* out, float softmax_scale, void* stream);
 

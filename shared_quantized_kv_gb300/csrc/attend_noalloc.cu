@@ -47,13 +47,13 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 }  // namespace
 
 extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, const float* vnorm,
-                                     const float* kscale, int kv_heads, int head_dim, int ctx,
-                                     int bits, const void* Q, int agents, int q_heads,
+                                     const float* kscale, const float* kscales, int kv_heads,
+                                     int head_dim, int ctx, int bits, const void* Q, int agents, int q_heads,
                                      const kvpool_tail_t* tail, float* out, float softmax_scale,
                                      void* stream) {
     if (!kq || !vcodes || !vnorm || !kscale || !Q || !out) return KVPOOL_ERR_INVALID_ARG;
     if (!aligned(kq, 16) || !aligned(vcodes, 16) || !aligned(vnorm, 4) || !aligned(kscale, 4) ||
-        !aligned(Q, 16) || !aligned(out, 16))
+        !aligned(Q, 16) || !aligned(out, 16) || !aligned(kscales, 4))
         return KVPOOL_ERR_INVALID_ARG;
     if ((head_dim != 64 && head_dim != 128) || bits < 2 || bits > 4 || kv_heads < 1 || ctx < 1 ||
         agents < 1 || q_heads < kv_heads || q_heads % kv_heads)
@@ -101,6 +101,7 @@ extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, co
     kvp::LayerBufs layer{const_cast<int8_t*>(kq), const_cast<uint8_t*>(vcodes),
                          const_cast<float*>(vnorm), const_cast<float*>(kscale), nullptr, bits,
                          nullptr};
+    layer.kscales = const_cast<float*>(kscales);  // block-scaled K: one scale per 32 elements
     kvp::AttendArgs a;
     a.Q = Q;
     a.agents = agents;
