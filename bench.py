@@ -331,7 +331,7 @@ def run_gpu(args):
     ph_info["attend"]["agent_steps_per_s"] = round(A * ws / (ph_ms["attend"] / 1e3), 1)
     ph_info["compress"]["note"] = "write-once encode of the shared context (once per pool, not per step)"
     ph_info["decompress"]["note"] = "per-agent materialisation baseline of the pages (not on the decode path)"
-    att_file = "attend_tc_impl.cuh"
+    att_file = "attend_rows.cuh"
 
     e2e = e2e_full = None
     if not args.no_e2e:
