@@ -59,6 +59,8 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
+#include <stdlib.h>
+
 #include <algorithm>
 
 #include "kvpool_internal.cuh"
@@ -114,9 +116,13 @@ struct Layout {
 
 __host__ __device__ inline uint32_t align_up(uint32_t x, uint32_t a) { return (x + a - 1) / a * a; }
 
+// bytes of the staging rows (W rows of D + 4 floats); the merge slots start there
+__host__ __device__ inline uint32_t staging_bytes(int D, int W) { return align_up(W * (D + 4) * 4, 1024); }
+
 // misc area: row factor [128], tile maxima [2][2][128], row-sum halves
-// [2][128], |q| maxima [2][128], tail (m, l) [128][2], owner slot [128]
-constexpr uint32_t kMiscBytes = 128 * 4 * (1 + 4 + 2 + 2 + 2 + 1);
+// [2][128], |q| maxima [2][128], tail (m, l) [128][2], log2 nref (one word,
+// padded)
+constexpr uint32_t kMiscBytes = 128 * 4 * (1 + 4 + 2 + 2 + 2) + 16;
 constexpr int kNumBars(int nraw) { return 2 * nraw + 4 * kNumOp + 7; }
 
 __host__ __device__ inline Layout make_layout(int D, int bits, int nraw) {
@@ -133,9 +139,6 @@ __host__ __device__ inline Layout make_layout(int D, int bits, int nraw) {
     L.total = align_up(L.bars + 8 * kNumBars(nraw) + 8, 1024);
     return L;
 }
-
-// bytes of the staging rows (W rows of D + 4 floats); the merge slots start there
-__host__ __device__ inline uint32_t staging_bytes(int D, int W) { return align_up(W * (D + 4) * 4, 1024); }
 
 __device__ __forceinline__ float bf2f(uint16_t u) { return __uint_as_float((uint32_t)u << 16); }
 
@@ -427,10 +430,9 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     float* psum = pmax + 4 * 128;                                 // [2][128] row-sum halves
     uint32_t* pq = reinterpret_cast<uint32_t*>(psum + 2 * 128);   // [2][128] |q| maxima (bf16 bits)
     float* tailml = reinterpret_cast<float*>(pq + 2 * 128);       // [128][2]
-    uint32_t* sOwn = reinterpret_cast<uint32_t*>(tailml + 2 * 128);  // [128] owner << 16 | slot
+    int* sNref = reinterpret_cast<int*>(tailml + 2 * 128);           // log2 nref, from the expanders
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars(NR));
-    float* sO = reinterpret_cast<float*>(sm);  // epilogue: [W][ROWF]
     const uint32_t b_raw_full = ptx::smem_u32(bars);
     const uint32_t b_raw_empty = b_raw_full + 8 * NR;
     // operand stages: K^ is released once its S MMA is done, V^ and the norms
@@ -445,6 +447,7 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const uint32_t b_o = b_p + 16;                 // a tile's P'.V MMAs are done
     const uint32_t b_fin = b_o + 8;                // every MMA is done
     const uint32_t b_m = b_fin + 8;                // every merge row sent here has landed
+    float* sO = reinterpret_cast<float*>(sm);      // epilogue: staging rows [128][ROWF]
 
     const int g = blockIdx.y;
     const int row0 = blockIdx.z * p.RW;
@@ -493,10 +496,6 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         if (own_cnt > 0) ptx::mbar_expect_tx(b_m, (uint32_t)(S * own_cnt * ROWF * 4));
         ptx::grid_dep_launch();
     }
-    if (tid < kM) {
-        const int ar = tid / p.G;  // agent of row tid, relative to the CTA's first agent
-        sOwn[tid] = ((uint32_t)(ar % S) << 16) | (uint32_t)((ar / S) * p.G + tid % p.G);
-    }
     __syncthreads();
     // Tensor memory: allocated by the issuer warp and published to the
     // softmax warps only (named barrier kBarTmem), so that the loader and the
@@ -523,6 +522,12 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     if (warp == kWarpLoad) {
         // ------------------------------------------------------------ loader
         if (lane == 0) {
+            // warm L2 with this CTA's query rows (the G rows of an agent are
+            // consecutive): the softmax warps read them after the grid-
+            // dependency wait, behind the tile traffic otherwise. A prefetch
+            // reads nothing into the kernel; L2 stays coherent with a writer.
+            for (int ar = 0; ar * p.G < nrows; ++ar)
+                ptx::prefetch_l2(p.Q + ((long long)(row0 / p.G + ar) * p.Hq + g * p.G) * D, p.G * D * 2);
             // the layer's bytes may be read before the grid-dependency wait
             // unless the launch before this one wrote them
             if (!p.early) ptx::grid_dep_wait();
@@ -593,7 +598,9 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     } else if (warp >= kWarpExp) {
         // --------------------------------------------------------- expanders
         const int et = tid - kWarpExp * 32;  // 0..127: token for K^, coordinate for V^
-        const float vr = ldexpf(1.0f, -nref_log2(p.vnmax));
+        const int nl = nref_log2(p.vnmax);  // read once here, kept for the merge
+        if (et == 0) *sNref = nl;
+        const float vr = ldexpf(1.0f, -nl);
         uint32_t tlo[4], thi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
@@ -900,20 +907,22 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     }
     if (bad) atomicOr(p.status, kStTimeout);
 
-    // this CTA is done with its stages: other CTAs may write merge slots here
-    // once every CTA of the cluster has arrived
+    // this CTA is done with its stages (and has read O out of tensor memory):
+    // other CTAs may write merge slots here once every CTA of the cluster has
+    // arrived
     ptx::fence_proxy_async();
+    ptx::tc_fence_before();
     __syncthreads();
     ptx::cluster_arrive();
 
     // send the G rows of each agent, consecutive here and at the owner of the
-    // agent, with one copy: slots (this rank, owner's row index)
+    // agent (agent ar -> CTA ar % S, slots from (ar / S) * G), with one copy
     float* slots = reinterpret_cast<float*>(sm + staging_bytes(D, kM));  // [S][own][ROWF]
     const int nsend = nrows / p.G;  // row groups hold whole agents
     ptx::cluster_wait();
     if (tid < nsend) {
-        const uint32_t ow = sOwn[tid * p.G], owner = ow >> 16;
-        const float* dst = slots + (size_t)(crank * p.own + (int)(ow & 0xFFFF)) * ROWF;
+        const uint32_t owner = (uint32_t)(tid % S);
+        const float* dst = slots + (size_t)(crank * p.own + (tid / S) * p.G) * ROWF;
         ptx::bulk_s2cluster(ptx::dsmem_addr(dst, owner), ptx::smem_u32(sO + tid * p.G * ROWF),
                             (uint32_t)(p.G * ROWF * 4), ptx::dsmem_addr(bars + (b_m - b_raw_full) / 8, owner));
         ptx::bulk_commit();
@@ -925,44 +934,41 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         const bool ok = !__syncthreads_or(late);
         if (late) atomicOr(p.status, kStTimeout);
         const int G = p.G;
-        const float oscale = ldexpf(1.0f, nref_log2(p.vnmax)) / (float)D * p.inv_lam;
+        const float oscale = ldexpf(1.0f, *sNref) / (float)D * p.inv_lam;
         for (int loc = warp; ok && loc < own_cnt; loc += kThreads / 32) {
             const int ar = (loc / G) * S + crank, j = loc % G;
             const int rr = ar * G + j;
             const int a = row0 / G + ar;
-            float ms[kMaxCluster], ls[kMaxCluster];
-#pragma unroll
-            for (int s = 0; s < kMaxCluster; ++s) {
-                ms[s] = -CUDART_INF_F;
-                ls[s] = 0.f;
-                if (s < S) {
-                    const float2 ml = *reinterpret_cast<const float2*>(slots + (size_t)(s * p.own + loc) * ROWF + D);
-                    ms[s] = ml.x;
-                    ls[s] = ml.y;
-                }
+            // lane s < S holds source s's (m, l); the row's maximum, the
+            // weights and the row sum by shuffles; the partial rows are read
+            // without branches (sources past S read source S - 1 at weight 0)
+            float ms = -CUDART_INF_F, ls = 0.f;
+            if (lane < S) {
+                const float2 ml = *reinterpret_cast<const float2*>(slots + (size_t)(lane * p.own + loc) * ROWF + D);
+                ms = ml.x;
+                ls = ml.y;
             }
-            float M = -CUDART_INF_F;
+            float M = ls > 0.f ? ms : -CUDART_INF_F;
 #pragma unroll
-            for (int s = 0; s < kMaxCluster; ++s)
-                if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
-            float L = 0.f;
+            for (int o2 = 16; o2; o2 >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o2));
+            const float w = ls > 0.f ? ptx::ex2(ms - M) : 0.f;
+            float L = w * ls;
+#pragma unroll
+            for (int o2 = 16; o2; o2 >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o2);
             float acc[EPL];
 #pragma unroll
             for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
 #pragma unroll
             for (int s = 0; s < kMaxCluster; ++s) {
-                if (s < S) {
-                    const float w = (ls[s] > 0.f) ? ptx::ex2(ms[s] - M) : 0.f;
-                    L = fmaf(w, ls[s], L);
-                    const float* src = slots + (size_t)(s * p.own + loc) * ROWF + lane * EPL;
-                    if constexpr (EPL == 4) {
-                        const float4 v = *reinterpret_cast<const float4*>(src);
-                        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-                        acc[2] = fmaf(w, v.z, acc[2]); acc[3] = fmaf(w, v.w, acc[3]);
-                    } else {
-                        const float2 v = *reinterpret_cast<const float2*>(src);
-                        acc[0] = fmaf(w, v.x, acc[0]); acc[1] = fmaf(w, v.y, acc[1]);
-                    }
+                const float ws = __shfl_sync(0xffffffffu, w, s);
+                const float* src = slots + (size_t)(min(s, S - 1) * p.own + loc) * ROWF + lane * EPL;
+                if constexpr (EPL == 4) {
+                    const float4 v = *reinterpret_cast<const float4*>(src);
+                    acc[0] = fmaf(ws, v.x, acc[0]); acc[1] = fmaf(ws, v.y, acc[1]);
+                    acc[2] = fmaf(ws, v.z, acc[2]); acc[3] = fmaf(ws, v.w, acc[3]);
+                } else {
+                    const float2 v = *reinterpret_cast<const float2*>(src);
+                    acc[0] = fmaf(ws, v.x, acc[0]); acc[1] = fmaf(ws, v.y, acc[1]);
                 }
             }
             // inverse rotation H acc; lane holds EPL consecutive channels
@@ -1085,6 +1091,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
         }
     }
     if (bestS == 0) return cudaErrorInvalidConfiguration;
+    if (const char* f = getenv("KVPOOL_EXP_S")) bestS = std::min(atoi(f), ntiles);
     const int per = (ntiles + bestS - 1) / bestS;
     const int S = (ntiles + per - 1) / per;  // never more CTAs than needed for `per` tiles each
     prm.tps = per * kTile;
