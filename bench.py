@@ -20,6 +20,11 @@ its attention outputs copied back, inside the timed region. e2e_full_path:
 compress + attend + decompress with the bf16 K, V uploaded and the outputs
 and decompressed K, V downloaded every step.
 
+With N ranks (torchrun) the ranks share one pool: rank r holds KV heads
+[r*Hk/N, (r+1)*Hk/N) of every layer and serves the query heads that read
+them, so attention needs no exchange and the total work is fixed ("strong"
+scaling); value is still every agent's step over the whole pool.
+
 cpu_baseline: the CPU oracle's decode step (dequantise the pool in float64,
 float64 attention for every agent, every layer) on all host cores (one
 process per core, layers spread over them) and on one core, median of 3.
@@ -65,7 +70,8 @@ def workload_config(w, ws, k_block):
             "layers": w.layers, "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim,
             "ctx": w.ctx, "agents": w.agents, "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
             "step": "decode: kvpool_attend of every layer for every agent",
-            "parallelism": f"replicas x{ws} (independent pools, no collective)"}
+            "parallelism": "one GPU" if ws == 1 else
+                           f"one pool, its KV heads split over {ws} ranks (no data-path collective)"}
 
 
 def launches_per_step(w, k_block, per_layer_calls, batch=32):
@@ -87,8 +93,9 @@ def launches_per_step(w, k_block, per_layer_calls, batch=32):
 
 def max_over_ranks(step_ms, ph_ms, phases, device=None):
     """(step time, per-phase times) as the maximum over the ranks of the
-    default process group (unchanged when no group is initialised). Ranks are
-    replicas: the job takes as long as its slowest rank."""
+    default process group (unchanged when no group is initialised). Ranks hold
+    shares of one pool (its KV heads): a step takes as long as its slowest
+    rank."""
     import torch
     import torch.distributed as dist
 
@@ -204,25 +211,33 @@ def run_gpu(args):
 
     w = wl.WORKLOADS[args.workload]
     L, A = w.layers, w.agents
-    pool = kvpool.KVPool(L, w.kv_heads, w.head_dim, w.ctx, w.bits_list(), max_rows=max(w.rows, 1),
+    # N ranks share one pool: rank r holds KV heads [h0, h1) of every layer
+    # and serves the query heads that read them (no exchange in attention)
+    if w.kv_heads % ws:
+        raise SystemExit(f"{w.kv_heads} KV heads do not split over {ws} ranks")
+    hk = w.kv_heads // ws
+    h0, h1 = rank * hk, (rank + 1) * hk
+    G = w.group
+    pool = kvpool.KVPool(L, hk, w.head_dim, w.ctx, w.bits_list(), max_rows=max(w.rows, 1),
                          k_block=args.k_block)
-    seed = rank  # each rank serves its own agents over its own pool
     K, V = [], []
     for l in range(L):
-        k, v = wl.layer_kv_torch(w, l, dev, seed)
-        K.append(k)
-        V.append(v)
-    Q = [torch.from_numpy(wl.layer_q(w, l, 0, seed).view(np.int16)).to(dev).view(torch.bfloat16)
-         for l in range(L)]
+        k, v = wl.layer_kv_torch(w, l, dev)
+        K.append(k[h0:h1].contiguous())
+        V.append(v[h0:h1].contiguous())
+        del k, v
+    Q = [torch.from_numpy(wl.layer_q(w, l, 0).view(np.int16)).to(dev).view(torch.bfloat16)[:, h0 * G:h1 * G]
+         .contiguous() for l in range(L)]
     tail = None
     if w.tail_max:
         tail = []
         for l in range(L):
-            kt, vt = wl.layer_tail(w, l, seed)
+            kt, vt = wl.layer_tail(w, l)
             lens = torch.full((A,), w.tail_len(w.decode_steps - 1), dtype=torch.int32, device=dev)
-            tail.append((torch.from_numpy(kt.view(np.int16)).to(dev).view(torch.bfloat16),
-                         torch.from_numpy(vt.view(np.int16)).to(dev).view(torch.bfloat16), lens))
-    out = [torch.empty((A, w.q_heads, w.head_dim), dtype=torch.float32, device=dev) for _ in range(L)]
+            tail.append((torch.from_numpy(kt.view(np.int16)).to(dev).view(torch.bfloat16)[:, h0:h1].contiguous(),
+                         torch.from_numpy(vt.view(np.int16)).to(dev).view(torch.bfloat16)[:, h0:h1].contiguous(),
+                         lens))
+    out = [torch.empty((A, hk * G, w.head_dim), dtype=torch.float32, device=dev) for _ in range(L)]
     Kd = [torch.empty_like(K[0]) for _ in range(L)]
     Vd = [torch.empty_like(V[0]) for _ in range(L)]
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
@@ -313,11 +328,11 @@ def run_gpu(args):
     step_ms = ph_ms["attend"]  # the decode step: all layers of kvpool_attend
 
     launches = launches_per_step(w, args.k_block, args.per_layer_calls)
-    # algorithmic bytes per layer
-    nvec = w.kv_heads * w.ctx
+    # algorithmic bytes per layer (this rank's share of the heads)
+    nvec = hk * w.ctx
     kv_in = 2 * nvec * w.head_dim * 2
     pool_layer = pool.pool_bytes() / L
-    tail_bytes = 2 * A * w.kv_heads * w.tail_len(w.decode_steps - 1) * w.head_dim * 2 if tail else 0
+    tail_bytes = 2 * A * hk * w.tail_len(w.decode_steps - 1) * w.head_dim * 2 if tail else 0
     algo = {"compress": kv_in + pool_layer, "attend": pool_layer + tail_bytes,
             "decompress": pool_layer + kv_in}
     peak, peak_kind = _peaks()
@@ -328,7 +343,7 @@ def run_gpu(args):
         ph_info[ph] = {"ms_per_step": round(ph_ms[ph], 4), "us_per_layer": round(per_call_s * 1e6, 3),
                        "algo_bytes_per_layer": int(algo[ph]), "GB_per_s": round(gbs, 1),
                        "hbm_frac": round(gbs / peak, 4), "launches_per_step": launches[ph]}
-    ph_info["attend"]["agent_steps_per_s"] = round(A * ws / (ph_ms["attend"] / 1e3), 1)
+    ph_info["attend"]["agent_steps_per_s"] = round(A / (ph_ms["attend"] / 1e3), 1)
     ph_info["compress"]["note"] = "write-once encode of the shared context (once per pool, not per step)"
     ph_info["decompress"]["note"] = "per-agent materialisation baseline of the pages (not on the decode path)"
     att_file = "attend_rows.cuh"
@@ -338,11 +353,11 @@ def run_gpu(args):
         e2e = run_e2e_decode(args, pool, w, Q, tail, out)
         e2e_full = run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd)
 
-    value = A * ws / (step_ms / 1e3)
+    value = A / (step_ms / 1e3)  # every agent's step over the whole (split) pool
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8/u3+f32",
+        "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "int8/u3+f32",
         "data": "synthetic (seeded; bf16 K/V with LogNormal(0,0.5) channel std and 1% x10 outlier "
                 "channels, Q ~ N(0,1))",
         "config": dict(workload_config(w, ws, args.k_block),
@@ -451,8 +466,7 @@ def run_e2e_decode(args, pool, w, Q, tail, out):
     ms = e0.elapsed_time(e1) / args.steps
     # the downloaded outputs are the device's
     assert torch.equal(h_out.view(torch.float32)[:out[0].numel()].view(out[0].shape).to(dev), o_dev[0])
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    return {"value": round(w.agents * ws / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
+    return {"value": round(w.agents / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h_in.numel()), "d2h_bytes_per_step": int(h_out.numel()),
             "how": "decode step through the C-ABI, pool resident: one upload of every layer's queries"
                    + (" and new tail tokens" if tail else "") + ", attend layer by layer, outputs "
@@ -549,8 +563,7 @@ def run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd):
     ms = e0.elapsed_time(e1) / args.steps
     h2d = sum(t.numel() * t.element_size() for t in hIn)
     d2h = sum(t.numel() * t.element_size() for t in hOut)
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    return {"value": round(w.agents * ws / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
+    return {"value": round(w.agents / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "how": "one CUDA graph per step: three streams pipelined over layers (upload, compute, download), "
                    f"one copy per {per} layer(s) each way"}
@@ -659,7 +672,7 @@ def run_reference(args):
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(step_s * 1e3, 2), "higher_is_better": True, "scaling": "strong",
         "vs_baseline": None, "dtype": "f64 attention over the dequantised pool", "data": "synthetic (seeded)",
         "config": dict(workload_config(w, ws, args.k_block),
                        timing=f"full decode step on the host CPU, layers spread over {used} processes"),

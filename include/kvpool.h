@@ -222,6 +222,39 @@ int kvpool_compress_layers(kvpool_t* pool, int n, const int* layers, const void*
 int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_heads,
                   const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream);
 
+/* Context split (one pool's context over several calls, ranks or GPUs):
+ * the attention state of every (agent, query head) row over the pool tokens
+ * [t_begin, t_end) of a compressed layer, instead of the finished output.
+ * For row r = a * G + j of KV head g (G = q_heads / kv_heads, query head
+ * g * G + j of agent a) it writes part_ml[g][r] = (m, l) and part_acc[g][r][:]
+ * = acc with, over the slice's tokens t and logits x_t = softmax_scale *
+ * log2(e) * <q, K_t> (log2 units): l = sum_t 2^(x_t - m) and acc =
+ * sum_t 2^(x_t - m) n_t c[codes_t] in the rotated domain (the slice's
+ * output is H acc / (head_dim * l), H the Sylvester Hadamard matrix); m is
+ * a reference within a few units of the slice's largest logit. part_ml:
+ * float [kv_heads][agents * G][2], 8-byte aligned; part_acc: float
+ * [kv_heads][agents * G][head_dim], 16-byte aligned; device. t_begin a
+ * multiple of 128, 0 <= t_begin < t_end <= kvpool_layer_len. No tail:
+ * the agents' private tails join in kvpool_merge_partials. Per-tensor
+ * pools only (block-scaled: KVPOOL_ERR_UNSUPPORTED). Source: the PolyKV
+ * summary's attention over the shared pool (section 2.A), split over the
+ * context; the merge below is the log-sum-exp combination of softmax
+ * partial sums. */
+int kvpool_attend_partial(kvpool_t* pool, int layer, const void* Q, int agents, int q_heads, int t_begin,
+                          int t_end, float* part_ml, float* part_acc, float softmax_scale, void* stream);
+
+/* Merge `parts` results of kvpool_attend_partial (slices of one context, in
+ * any order), each agent's private bf16 tail (NULL for none) and the final
+ * normalisation into out (float [agents][q_heads][head_dim], device):
+ * o = H (sum_s 2^(m_s - M) acc_s) / head_dim joined with the tail tokens in
+ * one softmax, divided by the total weight. part_ml: float [parts][kv_heads]
+ * [agents * G][2]; part_acc: float [parts][kv_heads][agents * G][head_dim]
+ * (the parts' buffers back to back), device. Q, tail, softmax_scale as in
+ * kvpool_attend. Needs no pool. */
+int kvpool_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads, int head_dim,
+                          const void* Q, int agents, int q_heads, const kvpool_tail_t* tail, float* out,
+                          float softmax_scale, void* stream);
+
 /* Materialise one layer as bf16: K_out = bf16(q*s), V_out_i = bf16(fl(z_i*n)
  * * (1/d)) with z = FWHT(c[codes]) in float32. K_out, V_out: bf16
  * [kv_heads][len][head_dim], device (len = kvpool_layer_len: ctx unless the

@@ -121,3 +121,74 @@ def row_rel_error(out: np.ndarray, ref: np.ndarray) -> float:
     num = np.max(np.abs(o - r), axis=1)
     den = np.maximum(np.max(np.abs(r), axis=1), 1e-30)
     return float(np.max(num / den)) if len(num) else 0.0
+
+
+# ------------------------------------------------------------ context split
+# Softmax attention splits over the context: over each slice S of the tokens
+# a row keeps lse2_S = log2 sum_{t in S} 2^(x_t) (x_t the logit in log2
+# units) and the slice's own normalised output o_S; the output over the
+# union is sum_S 2^(lse2_S - M) o_S / sum_S 2^(lse2_S - M), M = max_S lse2_S.
+# This is the log-sum-exp combination of softmax partial sums; the functions
+# below write it out in float64.
+
+def attend_slice_f64(K_hat, V_hat, Q_bf16, t_begin, t_end, scale=None):
+    """Attention state of every (agent, query head) row over pool tokens
+    [t_begin, t_end): returns (lse2 float64 [agents, q_heads], o float64
+    [agents, q_heads, d]), o the softmax-weighted mean of V_hat over the
+    slice."""
+    A, Hq, d = Q_bf16.shape
+    Hk = K_hat.shape[0]
+    G = Hq // Hk
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(d)
+    Q = codec.bf16_to_f32(Q_bf16).astype(np.float64)
+    lse2 = np.full((A, Hq), -np.inf)
+    out = np.zeros((A, Hq, d))
+    for a in range(A):
+        for g in range(Hk):
+            q = Q[a, g * G:(g + 1) * G]
+            x = scale * (q @ K_hat[g, t_begin:t_end].T) / np.log(2.0)  # log2 units
+            m = x.max(axis=1, keepdims=True)
+            w = np.exp2(x - m)
+            s = w.sum(axis=1, keepdims=True)
+            lse2[a, g * G:(g + 1) * G] = (m + np.log2(s))[:, 0]
+            out[a, g * G:(g + 1) * G] = (w / s) @ V_hat[g, t_begin:t_end]
+    return lse2, out
+
+
+def tail_slice_f64(Q_bf16, tail, kv_heads, scale=None):
+    """The same state over each agent's private bf16 tail tokens (rows of an
+    agent with no tail token: lse2 = -inf, o = 0)."""
+    A, Hq, d = Q_bf16.shape
+    G = Hq // kv_heads
+    if scale is None or scale == 0:
+        scale = 1.0 / np.sqrt(d)
+    Q = codec.bf16_to_f32(Q_bf16).astype(np.float64)
+    Kt = codec.bf16_to_f32(tail[0]).astype(np.float64)
+    Vt = codec.bf16_to_f32(tail[1]).astype(np.float64)
+    lens = np.asarray(tail[2])
+    lse2 = np.full((A, Hq), -np.inf)
+    out = np.zeros((A, Hq, d))
+    for a in range(A):
+        n = int(lens[a])
+        if n <= 0:
+            continue
+        for g in range(kv_heads):
+            q = Q[a, g * G:(g + 1) * G]
+            x = scale * (q @ Kt[a, g, :n].T) / np.log(2.0)
+            m = x.max(axis=1, keepdims=True)
+            w = np.exp2(x - m)
+            s = w.sum(axis=1, keepdims=True)
+            lse2[a, g * G:(g + 1) * G] = (m + np.log2(s))[:, 0]
+            out[a, g * G:(g + 1) * G] = (w / s) @ Vt[a, g, :n]
+    return lse2, out
+
+
+def merge_slices_f64(parts):
+    """Combine slice states [(lse2, o), ...] into the output over their
+    union (parts with lse2 = -inf for a row carry no weight there)."""
+    lse = np.stack([p[0] for p in parts])  # [P, A, Hq]
+    outs = np.stack([p[1] for p in parts])  # [P, A, Hq, d]
+    M = lse.max(axis=0)
+    w = np.where(np.isfinite(lse), np.exp2(lse - M), 0.0)
+    return (w[..., None] * outs).sum(axis=0) / w.sum(axis=0)[..., None]

@@ -19,6 +19,8 @@
 //     row for its split.
 //   attend_combine: one CTA per (row, kv head): log-sum-exp merge of the
 //     splits, inverse FWHT / d, the agent's tail tokens, final normalisation.
+//     The same kernel merges the context slices of kvpool_attend_partial
+//     (kvpool_merge_partials), with the partials laid out by slice.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -163,7 +165,7 @@ attend_split_kernel(const int8_t* __restrict__ kq, const uint8_t* __restrict__ v
 template <int D>
 __global__ void __launch_bounds__(D)
 attend_combine_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml,
-                      int nsplit, int max_rows, int Hk, int Hq, int G,
+                      int nsplit, long long head_stride, long long split_stride, int Hk, int Hq, int G,
                       const uint16_t* __restrict__ Q, const uint16_t* __restrict__ tK,
                       const uint16_t* __restrict__ tV, const int32_t* __restrict__ tlen,
                       int tail_max, float scale_log2, float* __restrict__ out) {
@@ -175,12 +177,12 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
     // merge the splits (log2 domain)
     float M = -CUDART_INF_F;
     for (int s = 0; s < nsplit; ++s) {
-        const long long b = ((long long)g * nsplit + s) * max_rows + r;
+        const long long b = g * head_stride + s * split_stride + r;
         if (part_ml[2 * b + 1] > 0.f) M = fmaxf(M, part_ml[2 * b]);
     }
     float L = 0.f, acc = 0.f;
     for (int s = 0; s < nsplit; ++s) {
-        const long long b = ((long long)g * nsplit + s) * max_rows + r;
+        const long long b = g * head_stride + s * split_stride + r;
         const float ls = part_ml[2 * b + 1];
         if (ls > 0.f) {
             const float w = exp2f(part_ml[2 * b] - M);
@@ -245,13 +247,29 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     attend_combine_kernel<D><<<dim3(a.rows, s.kv_heads), D, 0, st>>>(
-        scr.acc, scr.ml, nsplit, scr.max_rows, s.kv_heads, a.q_heads, a.group,
+        scr.acc, scr.ml, nsplit, (long long)nsplit * scr.max_rows, scr.max_rows, s.kv_heads, a.q_heads, a.group,
         (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len,
         a.tail_max, a.scale_log2, a.out);
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
+                                  int head_dim, const AttendArgs& a, cudaStream_t st) {
+    const long long R = a.rows;
+    if (head_dim == 64)
+        attend_combine_kernel<64><<<dim3(a.rows, kv_heads), 64, 0, st>>>(
+            part_acc, part_ml, parts, R, (long long)kv_heads * R, kv_heads, a.q_heads, a.group,
+            (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len, a.tail_max,
+            a.scale_log2, a.out);
+    else
+        attend_combine_kernel<128><<<dim3(a.rows, kv_heads), 128, 0, st>>>(
+            part_acc, part_ml, parts, R, (long long)kv_heads * R, kv_heads, a.q_heads, a.group,
+            (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len, a.tail_max,
+            a.scale_log2, a.out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const AttendArgs& a,
                                 const AttendScratch& scr, cudaStream_t st) {

@@ -102,7 +102,7 @@ extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, co
                          const_cast<float*>(vnorm), const_cast<float*>(kscale), nullptr, bits,
                          nullptr};
     layer.kscales = const_cast<float*>(kscales);  // block-scaled K: one scale per 32 elements
-    kvp::AttendArgs a;
+    kvp::AttendArgs a{};
     a.Q = Q;
     a.agents = agents;
     a.q_heads = q_heads;
@@ -114,6 +114,8 @@ extern "C" int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, co
     a.tail_len = has_tail ? tail->len : nullptr;
     a.tail_max = has_tail ? tail->T_max : 0;
     a.out = out;
+    a.t0 = 0;
+    a.t1 = ctx;
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
     const cudaError_t e =

@@ -88,7 +88,8 @@ struct Params {
     const float* vnorm;
     const float* kscale;
     const uint32_t* vnmax;
-    int ctx, ctx_pad, Hk;
+    int ctx, ctx_pad, Hk;  // ctx: end of the context slice attended (tokens)
+    int t0;                // start of the slice, a multiple of kTile
     const uint16_t* Q;
     int Hq, G, R, RW;  // RW: rows per row group (whole agents, <= 128)
     const uint16_t* tK;
@@ -104,6 +105,8 @@ struct Params {
     int* status;
     uint32_t tlo[4], thi[4];  // low / high bytes of fp16 lam * c[k], entry k in byte k % 4 of word k / 4
     float inv_lam;
+    float* part_ml;   // partial mode ([Hk][R][2] and [Hk][R][D]), else null
+    float* part_acc;
 };
 
 constexpr int kNumOp = 2;  // operand stages
@@ -395,6 +398,23 @@ __device__ __forceinline__ int nref_log2(const uint32_t* vnmax) {
     return 0;
 }
 
+// Partial mode (kvpool_attend_partial), per merged row: the slice's (M, L)
+// and its accumulator in the rotated domain, in the units where the output is
+// H acc / (D L)
+template <int D>
+__device__ __forceinline__ void write_partial(const Params& p, int g, int row, int lane, float M, float L,
+                                              const float (&acc)[D / 32], float scale) {
+    constexpr int EPL = D / 32;
+    const size_t base = (size_t)g * p.R + row;
+    float* dst = p.part_acc + base * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) dst[e] = acc[e] * scale;
+    if (lane == 0) {
+        p.part_ml[2 * base] = M;
+        p.part_ml[2 * base + 1] = L;
+    }
+}
+
 // Bounded wait shared by a warp: every lane waits, and the warp takes the
 // timeout branch together if any lane gave up.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool& bad) {
@@ -453,7 +473,7 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const int row0 = blockIdx.z * p.RW;
     const int nrows = min(p.RW, p.R - row0);  // a multiple of G
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int t_begin = crank * p.tps;
+    const int t_begin = p.t0 + crank * p.tps;
     const int t_end = min(p.ctx, t_begin + p.tps);
     const int ntile = (t_end - t_begin + kTile - 1) / kTile;  // >= 1
     const long long head_tok = (long long)g * p.ctx_pad;
@@ -971,6 +991,10 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                     acc[0] = fmaf(ws, v.x, acc[0]); acc[1] = fmaf(ws, v.y, acc[1]);
                 }
             }
+            if (p.part_acc != nullptr) {  // partial mode: the slice's state, no rotation, no tail
+                write_partial<D>(p, g, row0 + rr, lane, M, L, acc, oscale * (float)D);
+                continue;
+            }
             // inverse rotation H acc; lane holds EPL consecutive channels
 #pragma unroll
             for (int h = 1; h < EPL; h <<= 1) {
@@ -1130,13 +1154,16 @@ cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const At
     const int RW = ((spread ? 64 : kM) / a.group) * a.group;
     if (RW < 1) return cudaErrorInvalidValue;
     const int RGN = (a.rows + RW - 1) / RW;
-    const int ntiles = (s.ctx + kTile - 1) / kTile;
+    const int ntiles = (a.t1 - a.t0 + kTile - 1) / kTile;
     Params prm = {};
     prm.vcodes = L.vcodes;
     prm.vnorm = L.vnorm;
     prm.kscale = L.kscale;
     prm.vnmax = L.vnmax;
-    prm.ctx = s.ctx;
+    prm.ctx = a.t1;
+    prm.t0 = a.t0;
+    prm.part_ml = a.part_ml;
+    prm.part_acc = a.part_acc;
     prm.ctx_pad = s.ctx_pad;
     prm.Hk = s.kv_heads;
     prm.Q = (const uint16_t*)a.Q;

@@ -475,7 +475,7 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
                                     (reinterpret_cast<uintptr_t>(tail->len) & 3)))
         return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
-    kvp::AttendArgs a;
+    kvp::AttendArgs a{};
     a.Q = Q;
     a.agents = agents;
     a.q_heads = q_heads;
@@ -490,6 +490,8 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
     a.scale_log2 = scale * 1.4426950408889634f;
     a.early = p->may_read_early(stream, layer) ? 1 : 0;
+    a.t0 = 0;
+    a.t1 = p->len[layer];
     cudaError_t e;
     if (p->k_block) {  // block-scaled K: CUDA-core split kernels, the pool's own scratch
         kvp::AttendScratch scr;
@@ -504,6 +506,72 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     }
     if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
+}
+
+int kvpool_attend_partial(kvpool_t* p, int layer, const void* Q, int agents, int q_heads, int t_begin,
+                          int t_end, float* part_ml, float* part_acc, float softmax_scale, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!Q || !part_ml || !part_acc || agents < 1 || q_heads < p->kv_heads || q_heads % p->kv_heads)
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(part_acc) || (reinterpret_cast<uintptr_t>(part_ml) & 7))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!(softmax_scale >= 0.0f) || isinf(softmax_scale)) return KVPOOL_ERR_INVALID_ARG;
+    const int group = q_heads / p->kv_heads;
+    if ((long long)agents * group > p->max_rows) return KVPOOL_ERR_INVALID_ARG;
+    if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
+    if (p->k_block) return KVPOOL_ERR_UNSUPPORTED;
+    if (t_begin < 0 || t_begin % kvp::kTokenPad != 0 || t_end <= t_begin || t_end > p->len[layer])
+        return KVPOOL_ERR_INVALID_ARG;
+    kvp::AttendArgs a{};
+    a.Q = Q;
+    a.agents = agents;
+    a.q_heads = q_heads;
+    a.group = group;
+    a.rows = agents * group;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)p->head_dim);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    a.early = p->may_read_early(stream, layer) ? 1 : 0;
+    a.t0 = t_begin;
+    a.t1 = t_end;
+    a.part_ml = part_ml;
+    a.part_acc = part_acc;
+    const cudaError_t e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
+                                                static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) p->wrote(stream, -1);
+    return map_cuda(e);
+}
+
+int kvpool_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads, int head_dim,
+                          const void* Q, int agents, int q_heads, const kvpool_tail_t* tail, float* out,
+                          float softmax_scale, void* stream) {
+    if (parts < 1 || parts > 4096 || !part_ml || !part_acc || !Q || !out || agents < 1 || kv_heads < 1 ||
+        (head_dim != 64 && head_dim != 128) || q_heads < kv_heads || q_heads % kv_heads)
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!aligned16(Q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(part_ml) & 7) ||
+        (reinterpret_cast<uintptr_t>(part_acc) & 3))
+        return KVPOOL_ERR_INVALID_ARG;
+    if (!(softmax_scale >= 0.0f) || isinf(softmax_scale)) return KVPOOL_ERR_INVALID_ARG;
+    if (tail && (tail->T_max < 0 || (tail->T_max > 0 && (!tail->K || !tail->V || !tail->len))))
+        return KVPOOL_ERR_INVALID_ARG;
+    const long long rows = (long long)agents * (q_heads / kv_heads);
+    if (rows > 65535 || (long long)kv_heads > 65535) return KVPOOL_ERR_INVALID_ARG;
+    kvp::AttendArgs a{};
+    a.Q = Q;
+    a.agents = agents;
+    a.q_heads = q_heads;
+    a.group = q_heads / kv_heads;
+    a.rows = (int)rows;
+    const bool has_tail = tail && tail->T_max > 0;
+    a.tailK = has_tail ? tail->K : nullptr;
+    a.tailV = has_tail ? tail->V : nullptr;
+    a.tail_len = has_tail ? tail->len : nullptr;
+    a.tail_max = has_tail ? tail->T_max : 0;
+    a.out = out;
+    const float scale = softmax_scale > 0.0f ? softmax_scale : 1.0f / sqrtf((float)head_dim);
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return map_cuda(kvp::launch_merge_partials(parts, part_ml, part_acc, kv_heads, head_dim, a,
+                                               static_cast<cudaStream_t>(stream)));
 }
 
 int kvpool_decompress(kvpool_t* p, int layer, void* K_out, void* V_out, void* stream) {

@@ -126,7 +126,19 @@ struct AttendArgs {
     float* out;          // f32 [A][Hq][D]
     float scale_log2;    // softmax scale * log2(e)
     int early;           // 1: the launch right before this one on its stream did not write the layer
+    // context slice [t0, t1) of the layer's tokens (the whole layer: 0, len)
+    int t0, t1;
+    // partial mode: the slice's per-row (m, l) and rotated accumulator instead
+    // of the output (see kvpool_attend_partial); null otherwise
+    float* part_ml;      // [Hk][rows][2]
+    float* part_acc;     // [Hk][rows][D]
 };
+
+// Log-sum-exp merge of `parts` partial results laid out [parts][Hk][rows]
+// (see kvpool_merge_partials), one inverse FWHT per row, the agents' tails,
+// and the final normalisation into a.out.
+cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
+                                  int head_dim, const AttendArgs& a, cudaStream_t st);
 
 struct AttendScratch {
     float* acc;   // [Hk][nsplit][max_rows][D]

@@ -80,6 +80,13 @@ _SIGS = {
     "kvpool_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                               [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]),
+    "kvpool_attend_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                             ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]),
+    "kvpool_merge_partials": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                             ctypes.c_void_p]),
     "kvpool_strerror": (ctypes.c_char_p, [ctypes.c_int]),
 }
 
@@ -153,6 +160,30 @@ def sensitivity(Q, recent, kv_heads, softmax_scale=0.0, stream=None):
                                      softmax_scale, rows.data_ptr(), score.data_ptr(), _stream_ptr(stream)),
            "kvpool_sensitivity")
     return float(score.cpu()[0]), rows
+
+
+def merge_partials(ml, acc, Q, kv_heads, tail=None, out=None, softmax_scale=0.0, stream=None):
+    """kvpool_merge_partials: ml float32 [parts, kv_heads, rows, 2] and acc
+    float32 [parts, kv_heads, rows, d] from attend_partial (device); Q bf16
+    [agents, q_heads, d]; tail None or (K, V, lens) as for attend. Returns out
+    float32 [agents, q_heads, d]."""
+    import torch
+
+    A, Hq, d = Q.shape
+    parts = ml.shape[0]
+    if out is None:
+        out = torch.empty((A, Hq, d), dtype=torch.float32, device=Q.device)
+    tp = None
+    if tail is not None:
+        Kt, Vt, lens = tail
+        t = Tail(_dev_ptr(Kt, torch.bfloat16, "tail K").value, _dev_ptr(Vt, torch.bfloat16, "tail V").value,
+                 _dev_ptr(lens, torch.int32, "tail len").value, Kt.shape[2])
+        tp = ctypes.byref(t)
+    _check(_lib().kvpool_merge_partials(parts, _dev_ptr(ml, torch.float32, "ml"), _dev_ptr(acc, torch.float32, "acc"),
+                                        kv_heads, d, _dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, tp,
+                                        _dev_ptr(out, torch.float32, "out"), softmax_scale, _stream_ptr(stream)),
+           "kvpool_merge_partials")
+    return out
 
 
 def allocate_bits(sens, cost, budget):
@@ -257,6 +288,23 @@ class KVPool:
                                     _dev_ptr(out, torch.float32, "out"), softmax_scale,
                                     _stream_ptr(stream)), "kvpool_attend")
         return out
+
+    def attend_partial(self, layer, Q, t_begin, t_end, ml=None, acc=None, softmax_scale=0.0, stream=None):
+        """kvpool_attend_partial over pool tokens [t_begin, t_end): returns
+        (ml float32 [kv_heads, rows, 2], acc float32 [kv_heads, rows, d]),
+        rows = agents * (q_heads / kv_heads)."""
+        import torch
+
+        A, Hq, d = Q.shape
+        R = A * (Hq // self.kv_heads)
+        if ml is None:
+            ml = torch.empty((self.kv_heads, R, 2), dtype=torch.float32, device=Q.device)
+        if acc is None:
+            acc = torch.empty((self.kv_heads, R, d), dtype=torch.float32, device=Q.device)
+        _check(_lib().kvpool_attend_partial(self._h, layer, _dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, t_begin, t_end,
+                                            _dev_ptr(ml, torch.float32, "ml"), _dev_ptr(acc, torch.float32, "acc"),
+                                            softmax_scale, _stream_ptr(stream)), "kvpool_attend_partial")
+        return ml, acc
 
     def decompress(self, layer, K_out=None, V_out=None, stream=None):
         import torch

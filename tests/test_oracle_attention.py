@@ -153,3 +153,62 @@ def test_row_error_metric():
     ref = np.array([[1.0, -2.0, 0.5], [0.0, 0.0, 4.0]])
     out = ref + np.array([[0.002, 0, 0], [0, 0.004, 0]])
     assert attention.row_rel_error(out, ref) == pytest.approx(1e-3)
+
+
+# ---------------------------------------------------------------- context split
+
+def _small_layer(seed=3, Hk=2, G=2, d=16, T=40, A=3):
+    rng = np.random.default_rng(seed)
+    K = rng.standard_normal((Hk, T, d)) * 1.5
+    V = rng.standard_normal((Hk, T, d))
+    Q = codec.f32_to_bf16(rng.standard_normal((A, Hk * G, d)).astype(np.float32))
+    return K, V, Q
+
+
+@pytest.mark.parametrize("cuts", [[20], [1], [39], [7, 19, 33], list(range(1, 40))])
+def test_merged_slices_equal_full_attention(cuts):
+    # any split of the context, merged by log-sum-exp, is the plain softmax
+    # attention over the whole context
+    K, V, Q = _small_layer()
+    edges = [0] + cuts + [K.shape[1]]
+    parts = [attention.attend_slice_f64(K, V, Q, b, e) for b, e in zip(edges[:-1], edges[1:])]
+    got = attention.merge_slices_f64(parts)
+    want = attention.attend_f64(K, V, Q)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)
+    # the order of the parts does not matter
+    assert np.allclose(attention.merge_slices_f64(parts[::-1]), want, rtol=1e-12, atol=1e-12)
+
+
+def test_one_slice_is_the_slice_attention():
+    K, V, Q = _small_layer(seed=5)
+    lse, o = attention.attend_slice_f64(K, V, Q, 0, K.shape[1])
+    assert np.allclose(attention.merge_slices_f64([(lse, o)]), attention.attend_f64(K, V, Q), atol=1e-12)
+
+
+def test_slice_lse2_brute_force():
+    # lse2 = log2 sum_t 2^(x_t), x_t = scale * <q, k_t> / ln 2, by a Python loop
+    K, V, Q = _small_layer(seed=7, Hk=1, G=2, d=8, T=9, A=2)
+    lse, _ = attention.attend_slice_f64(K, V, Q, 2, 7)
+    q = codec.bf16_to_f32(Q).astype(np.float64)
+    scale = 1.0 / math.sqrt(8)
+    for a in range(2):
+        for h in range(2):
+            tot = 0.0
+            for t in range(2, 7):
+                x = scale * sum(q[a, h, i] * K[0, t, i] for i in range(8)) / math.log(2.0)
+                tot += 2.0 ** x
+            assert abs(lse[a, h] - math.log2(tot)) < 1e-12
+
+
+def test_slices_with_tail_equal_attention_with_tail():
+    K, V, Q = _small_layer(seed=9, Hk=2, G=2, d=16, T=30, A=3)
+    rng = np.random.default_rng(11)
+    Kt = codec.f32_to_bf16(rng.standard_normal((3, 2, 5, 16)).astype(np.float32))
+    Vt = codec.f32_to_bf16(rng.standard_normal((3, 2, 5, 16)).astype(np.float32))
+    lens = np.array([0, 5, 2])
+    tail = (Kt, Vt, lens)
+    parts = [attention.attend_slice_f64(K, V, Q, 0, 13), attention.attend_slice_f64(K, V, Q, 13, 30),
+             attention.tail_slice_f64(Q, tail, 2)]
+    got = attention.merge_slices_f64(parts)
+    want = attention.attend_f64(K, V, Q, tail)
+    assert np.allclose(got, want, rtol=1e-12, atol=1e-12)

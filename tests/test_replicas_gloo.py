@@ -1,6 +1,6 @@
 """The multi-process path of the benchmark on CPU: two ranks over gloo
-(127.0.0.1). Ranks are replicas (independent pools, no data-path
-collective); the only exchange is the maximum of the per-rank step times,
+(127.0.0.1). Ranks hold shares (KV heads) of one pool, with no data-path
+collective; the only exchange is the maximum of the per-rank step times,
 so the job's rate is set by its slowest rank."""
 
 import os
@@ -39,7 +39,7 @@ def _rank_main(rank, world, port, out):
     dist.destroy_process_group()
 
 
-def test_two_rank_replicas_take_the_slowest_rank():
+def test_two_ranks_take_the_slowest_rank():
     port = _free_port()
     with mp.Manager() as m:
         out = m.dict()
