@@ -59,8 +59,6 @@
 #include <cuda_fp16.h>
 #include <math_constants.h>
 
-#include <stdlib.h>
-
 #include <algorithm>
 
 #include "kvpool_internal.cuh"
@@ -1115,7 +1113,6 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
         }
     }
     if (bestS == 0) return cudaErrorInvalidConfiguration;
-    if (const char* f = getenv("KVPOOL_EXP_S")) bestS = std::min(atoi(f), ntiles);
     const int per = (ntiles + bestS - 1) / bestS;
     const int S = (ntiles + per - 1) / per;  // never more CTAs than needed for `per` tiles each
     prm.tps = per * kTile;
