@@ -78,9 +78,8 @@ def launches_per_step(w, k_block, per_layer_calls, batch=32):
     """The library's kernel launches in one step, by phase. Compress: a max|K|
     kernel and an encode kernel per layer, or, for all layers in one call, one
     max|K| kernel and one encode kernel per V width per 32 layers. Attend: the
-    tensor-core kernel per layer, or the split and combine kernels (block-
-    scaled K). Decompress: one kernel per layer, or one per V width per 32
-    layers."""
+    tensor-core kernel per layer (per-tensor and block-scaled K alike).
+    Decompress: one kernel per layer, or one per V width per 32 layers."""
     bits = w.bits_list()
     chunks = [bits[i:i + batch] for i in range(0, len(bits), batch)]
     widths = sum(len(set(c)) for c in chunks)
@@ -88,7 +87,7 @@ def launches_per_step(w, k_block, per_layer_calls, batch=32):
         comp, dec = 2 * len(bits), len(bits)
     else:
         comp, dec = len(chunks) + widths, widths
-    return {"compress": comp, "attend": len(bits) * (2 if k_block else 1), "decompress": dec}
+    return {"compress": comp, "attend": len(bits), "decompress": dec}
 
 
 def max_over_ranks(step_ms, ph_ms, phases, device=None):

@@ -101,7 +101,7 @@ typedef struct {
  * `kv_heads` KV heads of size `head_dim` (64 or 128). bits_per_layer: host
  * array [layers] of V bit widths, each 2, 3 or 4 (NULL: 3 for every layer).
  * max_rows: the most query rows that may share one KV head in kvpool_attend
- * (agents x GQA group), 1..1024 (0: 512); it sizes the attention scratch.
+ * (agents x GQA group), 1..1024 (0: 512).
  * Allocates all device memory on the current device. Source: PolyKV summary,
  * section 2.A (one shared object, O(1) in the number of agents). */
 int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
@@ -116,9 +116,10 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
  * 2.B (which names both a per-tensor scale and q8_0); the scales are float32,
  * not q8_0's fp16, because a bf16 K can exceed the fp16 range. The pool then
  * holds head_dim/32 scales per token and head (kvpool_layer_view_t.kscales).
- * Attention over such a pool runs on CUDA cores (the split-context kernels)
- * with a split scratch sized here for max_rows; attend calls on one such
- * pool share that scratch and must be ordered on one stream by the caller.
+ * Attention over such a pool runs on the tensor cores like that of a
+ * per-tensor pool and needs no scratch: K^ is formed from each block's
+ * quantised values and scale as a pair of fp16 operands (about 22 significant
+ * bits), the token's power-of-two range factor applied to its logit exactly.
  * kvpool_export_layer exports such a layer with *kscale = 1 and
  * kvpool_export_kscales copies its block scales; kvpool_import_layer returns
  * KVPOOL_ERR_UNSUPPORTED for these pools. Other k_block values:
@@ -235,8 +236,8 @@ int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_he
  * float [kv_heads][agents * G][2], 8-byte aligned; part_acc: float
  * [kv_heads][agents * G][head_dim], 16-byte aligned; device. t_begin a
  * multiple of 128, 0 <= t_begin < t_end <= kvpool_layer_len. No tail:
- * the agents' private tails join in kvpool_merge_partials. Per-tensor
- * pools only (block-scaled: KVPOOL_ERR_UNSUPPORTED). Source: the PolyKV
+ * the agents' private tails join in kvpool_merge_partials. Per-tensor and
+ * block-scaled pools. Source: the PolyKV
  * summary's attention over the shared pool (section 2.A), split over the
  * context; the merge below is the log-sum-exp combination of softmax
  * partial sums. */

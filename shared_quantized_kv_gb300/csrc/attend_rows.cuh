@@ -105,12 +105,14 @@ struct Params {
     float inv_lam;
     float* part_ml;   // partial mode ([Hk][R][2] and [Hk][R][D]), else null
     float* part_acc;
+    const float* kscales;  // block-scaled K: [Hk][ctx_pad][D/32] (instances with KB), else unused
 };
 
-constexpr int kNumOp = 2;  // operand stages
+// operand stages (block-scaled K^ takes twice the room, leaving one raw stage)
+__host__ __device__ constexpr int num_op(bool kb) { return kb ? 2 : 2; }
 
 struct Layout {
-    uint32_t op, op_v, op_n;    // operand stage: K^ at 0, V^ at op_v, norms at op_n
+    uint32_t op, op_v, op_n;    // operand stage: K^ at 0 (block-scaled: hi, then lo), V^ at op_v, norms at op_n
     uint32_t raw, raw_v, raw_n; // raw stage: int8 K at 0, V codes at raw_v, norms at raw_n
     uint32_t raw0, misc, bars, total;
 };
@@ -123,21 +125,23 @@ __host__ __device__ inline uint32_t staging_bytes(int D, int W) { return align_u
 // misc area: row factor [128], tile maxima [2][2][128], row-sum halves
 // [2][128], |q| maxima [2][128], tail (m, l) [128][2], log2 nref (one word,
 // padded)
+// (block-scaled K: then the column factors sigma_t, [2][128])
 constexpr uint32_t kMiscBytes = 128 * 4 * (1 + 4 + 2 + 2 + 2) + 16;
-constexpr int kNumBars(int nraw) { return 2 * nraw + 4 * kNumOp + 7; }
+constexpr uint32_t kSigBytes = 2 * 128 * 4;
+__host__ __device__ constexpr int kNumBars(int nraw, bool kb) { return 2 * nraw + 4 * num_op(kb) + 7 + (kb ? 4 : 0); }
 
-__host__ __device__ inline Layout make_layout(int D, int bits, int nraw) {
+__host__ __device__ inline Layout make_layout(int D, int bits, int nraw, bool kb) {
     Layout L;
-    L.op_v = kTile * D * 2;
+    L.op_v = kTile * D * 2 * (kb ? 2 : 1);
     L.op_n = L.op_v + D * kTile * 2;
     L.op = align_up(L.op_n + kTile * 4, 1024);
     L.raw_v = kTile * D;
     L.raw_n = L.raw_v + kTile * D * bits / 8;
     L.raw = align_up(L.raw_n + kTile * 4, 1024);
-    L.raw0 = kNumOp * L.op;
+    L.raw0 = num_op(kb) * L.op;
     L.misc = L.raw0 + nraw * L.raw;
-    L.bars = align_up(L.misc + kMiscBytes, 8);
-    L.total = align_up(L.bars + 8 * kNumBars(nraw) + 8, 1024);
+    L.bars = align_up(L.misc + kMiscBytes + (kb ? kSigBytes : 0), 8);
+    L.total = align_up(L.bars + 8 * kNumBars(nraw, kb) + 8, 1024);
     return L;
 }
 
@@ -159,6 +163,20 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& lo, uint32_t&
     __half2 hb = __hsub2(*reinterpret_cast<const __half2*>(&b), bias);
     lo = *reinterpret_cast<uint32_t*>(&ha);
     hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+
+// an fp16x2 pair of int8 values q times r = rh + rl (rh = fp16(r), rl =
+// fp16(r - rh)), as fp16x2 hi + lo: hi = fl(q rh); q rh - hi is exact in
+// fp16 (a short remainder), so one fused step adds q rl to it; hi + lo
+// carries ~21 significant bits of q r (ratios below 2^-14 lose bits to the
+// fp16 range: blocks that much smaller than the token's largest)
+__device__ __forceinline__ void split_scaled(uint32_t qh2, __half2 rh, __half2 rl, uint32_t& hi, uint32_t& lo) {
+    const __half2 q = *reinterpret_cast<const __half2*>(&qh2);
+    const __half2 h = __hmul2(q, rh);
+    const __half2 e = __hfma2(q, rh, __hneg2(h));  // q rh - hi, exact
+    const __half2 l = __hfma2(q, rl, e);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
 // 8 codes of BITS bits (the low 8*BITS bits of x) -> 8 nibbles
@@ -423,8 +441,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool& b
 }
 
 // SPREAD: row groups of at most 64 rows, each row on two lanes (four
-// softmax threads per row, all four lane quarters busy)
-template <int D, int BITS, bool TAIL, bool SPREAD>
+// softmax threads per row, all four lane quarters busy).
+// KB: block-scaled K (one scale s_b per 32 channels of a token). The
+// expanders write K^ = q * s_b / sigma_t with sigma_t the power of two just
+// above the token's largest s_b, as fp16 hi + lo (~21 significant bits), and
+// sigma_t into a two-slot ring; S takes both halves (16 MMAs) and the softmax
+// scales S column t by sigma_t (exact).
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     constexpr int HC = D / 2;                // O columns per softmax half
@@ -441,7 +464,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int S = (int)ptx::cluster_size();
     const int crank = (int)ptx::cluster_rank();
-    const Layout lay = make_layout(D, BITS, p.nraw);
+    constexpr int kNumOp = num_op(KB);
+    const Layout lay = make_layout(D, BITS, p.nraw, KB);
     const int NR = p.nraw;
     float* crow = reinterpret_cast<float*>(sm + lay.misc);       // [128] logit factor per row
     float* pmax = crow + 128;                                     // [2][2][128] tile maxima (parity, half)
@@ -449,8 +473,9 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     uint32_t* pq = reinterpret_cast<uint32_t*>(psum + 2 * 128);   // [2][128] |q| maxima (bf16 bits)
     float* tailml = reinterpret_cast<float*>(pq + 2 * 128);       // [128][2]
     int* sNref = reinterpret_cast<int*>(tailml + 2 * 128);           // log2 nref, from the expanders
+    float* sig = reinterpret_cast<float*>(sm + lay.misc + kMiscBytes);  // KB: [2][128] sigma_t per ring slot
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + lay.bars);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars(NR));
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + kNumBars(NR, KB));
     const uint32_t b_raw_full = ptx::smem_u32(bars);
     const uint32_t b_raw_empty = b_raw_full + 8 * NR;
     // operand stages: K^ is released once its S MMA is done, V^ and the norms
@@ -465,6 +490,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const uint32_t b_o = b_p + 16;                 // a tile's P'.V MMAs are done
     const uint32_t b_fin = b_o + 8;                // every MMA is done
     const uint32_t b_m = b_fin + 8;                // every merge row sent here has landed
+    const uint32_t b_sig_full = b_m + 8;           // KB: [2] sigma_t of a tile is written
+    const uint32_t b_sig_empty = b_sig_full + 16;  // KB: [2] the softmax is done with the slot
     float* sO = reinterpret_cast<float*>(sm);      // epilogue: staging rows [128][ROWF]
 
     const int g = blockIdx.y;
@@ -510,6 +537,12 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         ptx::mbar_init(b_o, 1);
         ptx::mbar_init(b_fin, 1);
         ptx::mbar_init(b_m, 1);
+        if constexpr (KB) {
+            for (int b = 0; b < 2; ++b) {
+                ptx::mbar_init(b_sig_full + 8 * b, kExpThreads / 32);
+                ptx::mbar_init(b_sig_empty + 8 * b, 8);
+            }
+        }
         ptx::mbar_init_fence();
         if (own_cnt > 0) ptx::mbar_expect_tx(b_m, (uint32_t)(S * own_cnt * ROWF * 4));
         ptx::grid_dep_launch();
@@ -526,13 +559,13 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     };
 
     // tails of the agents this CTA owns (CUDA cores, every warp), while the
-    // first tiles are in flight; the second operand stage is free until then
+    // first tiles are in flight; the (last) operand stage is free until then
     int first = 0;  // loader: tiles requested before the role loops
     if constexpr (TAIL) {
         ptx::grid_dep_wait();
         if (tid == 0)
             for (; first < min(ntile, NR); ++first) issue_tile(first);
-        tail_attention<D>(p, sm + lay.op, tailml, S, crank, g, row0, nrows);
+        tail_attention<D>(p, sm + (kNumOp == 2 ? lay.op : 0), tailml, S, crank, g, row0, nrows);
     }
 
     bool bad = false;
@@ -602,6 +635,15 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                     const uint64_t bk = ptx::sdesc(aK + (ks / 4) * KBLK + (ks % 4) * 32, 16, 1024);
                     ptx::mma_f16_ta(tS, tQ + ks * 8, bk, idS, ks > 0 ? 1u : 0u);
                 }
+                if constexpr (KB) {
+                    // + Q (K^ lo)^T
+                    const uint32_t aL = aK + kTile * D * 2;
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        const uint64_t bk = ptx::sdesc(aL + (ks / 4) * KBLK + (ks % 4) * 32, 16, 1024);
+                        ptx::mma_f16_ta(tS, tQ + ks * 8, bk, idS, 1u);
+                    }
+                }
                 ptx::mma_commit(b_k_empty + 8 * e);
                 ptx::mma_commit(b_s + 8 * b);
                 if (i > 0) pv(i - 1);
@@ -622,6 +664,20 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         uint32_t tlo[4], thi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) { tlo[k] = p.tlo[k]; thi[k] = p.thi[k]; }
+        // KB: this token's block scales, one tile ahead (the padding's are 0)
+        constexpr int NB = D / 32;
+        float scn[NB] = {};
+        auto load_scales = [&](int i) {
+            const float* src = p.kscales + (head_tok + t_begin + (long long)i * kTile + et) * NB;
+            if constexpr (NB == 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(src));
+                scn[0] = v.x, scn[1] = v.y, scn[2] = v.z, scn[3] = v.w;
+            } else {
+                const float2 v = __ldg(reinterpret_cast<const float2*>(src));
+                scn[0] = v.x, scn[1] = v.y;
+            }
+        };
+        if constexpr (KB) load_scales(0);
         for (int i = 0; i < ntile; ++i) {
             const int s = i % NR, e = i % kNumOp;
             warp_wait(b_raw_full + 8 * s, (i / NR) & 1, bad);
@@ -630,8 +686,36 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             unsigned char* opk = sm + e * lay.op;
             unsigned char* opv = opk + lay.op_v;
             float* opn = reinterpret_cast<float*>(opk + lay.op_n);
+            // KB: sigma_t = 2^(E + 1) for the largest scale m 2^E (1 if all are 0),
+            // r_b = s_b / sigma_t (exact) into the ring slot of the tile
+            float rb[NB];
+            __half2 rbh[NB], rbl[NB];
+            if constexpr (KB) {
+                float sc[NB];
+                float mx = 0.0f;
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+                    sc[k] = scn[k];
+                    mx = fmaxf(mx, sc[k]);
+                }
+                if (i + 1 < ntile) load_scales(i + 1);
+                int ex = mx > 0.0f ? (int)((__float_as_uint(mx) >> 23) & 0xFF) - 126 : 0;  // E + 1
+                ex = max(-125, min(127, ex));
+                const float inv = __uint_as_float((uint32_t)(127 - ex) << 23);
+#pragma unroll
+                for (int k = 0; k < NB; ++k) {
+                    rb[k] = __fmul_rn(sc[k], inv);
+                    const __half h = __float2half_rn(rb[k]);
+                    rbh[k] = __half2half2(h);
+                    rbl[k] = __half2half2(__float2half_rn(rb[k] - __half2float(h)));
+                }
+                if (i >= 2) warp_wait(b_sig_empty + 8 * (i & 1), ((i >> 1) - 1) & 1, bad);
+                sig[(i & 1) * 128 + et] = __uint_as_float((uint32_t)(127 + ex) << 23);
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(b_sig_full + 8 * (i & 1));
+            }
             // K^: token et, D int8 -> D fp16 (TMA swizzle of the raw row: 128 B
-            // for D = 128, 64 B for D = 64)
+            // for D = 128, 64 B for D = 64); block-scaled: hi and lo of q r_b
             {
                 const int t = et;
                 const int sw = D == 128 ? (t & 7) : ((t >> 1) & 3);
@@ -643,8 +727,25 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                     i8x4_to_h2x2(u.y, a.z, a.w);
                     i8x4_to_h2x2(u.z, b.x, b.y);
                     i8x4_to_h2x2(u.w, b.z, b.w);
-                    *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c, KBLK)) = a;
-                    *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c + 1, KBLK)) = b;
+                    if constexpr (KB) {
+                        const __half2 rh = rbh[c / 2], rl = rbl[c / 2];  // block c / 2 of 32 channels
+                        uint4 ah, al, bh, bl;
+                        split_scaled(a.x, rh, rl, ah.x, al.x);
+                        split_scaled(a.y, rh, rl, ah.y, al.y);
+                        split_scaled(a.z, rh, rl, ah.z, al.z);
+                        split_scaled(a.w, rh, rl, ah.w, al.w);
+                        split_scaled(b.x, rh, rl, bh.x, bl.x);
+                        split_scaled(b.y, rh, rl, bh.y, bl.y);
+                        split_scaled(b.z, rh, rl, bh.z, bl.z);
+                        split_scaled(b.w, rh, rl, bh.w, bl.w);
+                        *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c, KBLK)) = ah;
+                        *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c + 1, KBLK)) = bh;
+                        *reinterpret_cast<uint4*>(opk + kTile * D * 2 + kmajor_off(t, 2 * c, KBLK)) = al;
+                        *reinterpret_cast<uint4*>(opk + kTile * D * 2 + kmajor_off(t, 2 * c + 1, KBLK)) = bl;
+                    } else {
+                        *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c, KBLK)) = a;
+                        *reinterpret_cast<uint4*>(opk + kmajor_off(t, 2 * c + 1, KBLK)) = b;
+                    }
                 }
             }
             ptx::fence_proxy_async();  // the MMAs read the operands through the async proxy
@@ -705,6 +806,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             for (int i = 0; i < ntile; ++i) {
                 warp_wait(b_s + 8 * (i & 1), (i >> 1) & 1, bad);
                 if (lane == 0) ptx::mbar_arrive(b_p + 8 * (i & 1));
+                if constexpr (KB)
+                    if (lane == 0) ptx::mbar_arrive(b_sig_empty + 8 * (i & 1));
             }
         } else {
             // Q row r -> fp16 in tensor memory (the A operand of S), scaled by the
@@ -762,10 +865,23 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 ptx::tc_fence_after();
                 const uint32_t tS = tmem + kColS + 128 * b + lane_off;
                 const int nval = t_end - (t_begin + i * kTile);  // valid tokens of the tile
-                // chunk ch (32 tokens) of S for this lane, tokens past the split at -inf
+                if constexpr (KB) warp_wait(b_sig_full + 8 * (i & 1), (i >> 1) & 1, bad);
+                // chunk ch (32 tokens) of S for this lane (block-scaled: column t
+                // times sigma_t), tokens past the split at -inf
                 auto load_s = [&](int ch, uint32_t (&u)[32]) {
                     ptx::tmem_ld32(tS + 32 * ch, u);
                     ptx::tmem_wait_ld();
+                    if constexpr (KB) {
+                        const float4* s4 = reinterpret_cast<const float4*>(sig + (i & 1) * 128 + 32 * ch);
+#pragma unroll
+                        for (int k4 = 0; k4 < 8; ++k4) {
+                            const float4 f = s4[k4];
+                            u[4 * k4 + 0] = __float_as_uint(__uint_as_float(u[4 * k4 + 0]) * f.x);
+                            u[4 * k4 + 1] = __float_as_uint(__uint_as_float(u[4 * k4 + 1]) * f.y);
+                            u[4 * k4 + 2] = __float_as_uint(__uint_as_float(u[4 * k4 + 2]) * f.z);
+                            u[4 * k4 + 3] = __float_as_uint(__uint_as_float(u[4 * k4 + 3]) * f.w);
+                        }
+                    }
                     if (nval < 32 * ch + 32) {  // the same in every thread
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
@@ -887,6 +1003,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(b_p + 8 * b);
+                if constexpr (KB)
+                    if (lane == 0) ptx::mbar_arrive(b_sig_empty + 8 * b);
             }
             // every MMA is done, so no stage is read any more: this half of the
             // row's O goes straight into the staging rows (SPREAD: the sum of
@@ -1045,23 +1163,23 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
 // ------------------------------------------------------------------ launch
 
-template <int D, int BITS, bool TAIL, bool SPREAD>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
 void configure() {
     static bool done = false;
     if (done) return;
-    auto kern = attend_rows_kernel<D, BITS, TAIL, SPREAD>;
+    auto kern = attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     done = true;
 }
 
 // How many clusters of S CTAs with `smem` bytes each can be resident at once.
-template <int D, int BITS, bool TAIL, bool SPREAD>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
 int max_clusters(int S, size_t smem) {
     static int cache[kMaxCluster + 1][2] = {};  // [S] -> (smem key / 1024 + 1, count)
     const int key = (int)(smem / 1024) + 1;
     if (cache[S][0] == key) return cache[S][1];
-    configure<D, BITS, TAIL, SPREAD>();
+    configure<D, BITS, TAIL, SPREAD, KB>();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1074,7 +1192,7 @@ int max_clusters(int S, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_rows_kernel<D, BITS, TAIL, SPREAD>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -1083,16 +1201,17 @@ int max_clusters(int S, size_t smem) {
     return n;
 }
 
-template <int D, int BITS, bool TAIL, bool SPREAD>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
 cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
-    configure<D, BITS, TAIL, SPREAD>();
+    configure<D, BITS, TAIL, SPREAD, KB>();
     constexpr uint32_t kMaxSmem = 227 * 1024;
     const int rows_cta = std::min(prm.RW, prm.R);
     const int agents_cta = rows_cta / prm.G;
     const int clusters = Hk * RGN;
     // raw stages: as many as fit (up to 3)
     int max_nr = 3;
-    while (max_nr > 1 && make_layout(D, BITS, max_nr).total + 1024 > kMaxSmem) --max_nr;
+    while (max_nr > 1 && make_layout(D, BITS, max_nr, KB).total + 1024 > kMaxSmem) --max_nr;
+    if (make_layout(D, BITS, max_nr, KB).total + 1024 > kMaxSmem) return cudaErrorInvalidConfiguration;
     // cluster size: fewest (waves x tiles per CTA), then the larger cluster;
     // the staging rows and the merge slots must fit in the stage area
     int bestS = 0;
@@ -1100,10 +1219,10 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
     for (int S = 1; S <= kMaxCluster && S <= ntiles; ++S) {
         const int per = (ntiles + S - 1) / S;
         const int own = (agents_cta + S - 1) / S * prm.G;
-        const Layout lay = make_layout(D, BITS, std::min(max_nr, per));
+        const Layout lay = make_layout(D, BITS, std::min(max_nr, per), KB);
         if (staging_bytes(D, kM) + (size_t)S * own * (D + 4) * 4 > lay.misc) continue;
         const size_t smem = lay.total + 1024;
-        const int n = max_clusters<D, BITS, TAIL, SPREAD>(S, smem);
+        const int n = max_clusters<D, BITS, TAIL, SPREAD, KB>(S, smem);
         if (n < 1) continue;
         const long long waves = (clusters + n - 1) / n;
         const long long cost = waves * per;
@@ -1118,7 +1237,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
     prm.tps = per * kTile;
     prm.own = (agents_cta + S - 1) / S * prm.G;
     prm.nraw = std::min(max_nr, per);
-    const Layout lay = make_layout(D, BITS, prm.nraw);
+    const Layout lay = make_layout(D, BITS, prm.nraw, KB);
     if (staging_bytes(D, kM) + (size_t)S * prm.own * (D + 4) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, Hk, RGN);
@@ -1134,7 +1253,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attend_rows_kernel<D, BITS, TAIL, SPREAD>, kmap, prm);
+    return cudaLaunchKernelEx(&cfg, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>, kmap, prm);
 }
 
 }  // namespace rows
@@ -1182,15 +1301,19 @@ cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const At
         prm.thi[k / 4] |= (uint32_t)(cb.c16[k] >> 8) << (8 * (k % 4));
     }
     prm.inv_lam = 1.0f / cb.lam;
+    prm.kscales = L.kscales;
     const CUtensorMap& km = *L.kmap;
     const bool tail = prm.tK != nullptr;
-#define KVP_ROWS_LAUNCH(DD, TT, SS) launch_cfg<DD, BITS, TT, SS>(km, prm, ntiles, s.kv_heads, RGN, st)
+    const bool kb = L.kscales != nullptr;
+#define KVP_ROWS_LAUNCH(DD, TT, SS, KK) launch_cfg<DD, BITS, TT, SS, KK>(km, prm, ntiles, s.kv_heads, RGN, st)
+#define KVP_ROWS_KB(DD, TT, SS) (kb ? KVP_ROWS_LAUNCH(DD, TT, SS, true) : KVP_ROWS_LAUNCH(DD, TT, SS, false))
     if (D == 64) {
-        if (spread) return tail ? KVP_ROWS_LAUNCH(64, true, true) : KVP_ROWS_LAUNCH(64, false, true);
-        return tail ? KVP_ROWS_LAUNCH(64, true, false) : KVP_ROWS_LAUNCH(64, false, false);
+        if (spread) return tail ? KVP_ROWS_KB(64, true, true) : KVP_ROWS_KB(64, false, true);
+        return tail ? KVP_ROWS_KB(64, true, false) : KVP_ROWS_KB(64, false, false);
     }
-    if (spread) return tail ? KVP_ROWS_LAUNCH(128, true, true) : KVP_ROWS_LAUNCH(128, false, true);
-    return tail ? KVP_ROWS_LAUNCH(128, true, false) : KVP_ROWS_LAUNCH(128, false, false);
+    if (spread) return tail ? KVP_ROWS_KB(128, true, true) : KVP_ROWS_KB(128, false, true);
+    return tail ? KVP_ROWS_KB(128, true, false) : KVP_ROWS_KB(128, false, false);
+#undef KVP_ROWS_KB
 #undef KVP_ROWS_LAUNCH
 }
 

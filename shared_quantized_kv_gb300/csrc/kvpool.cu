@@ -9,8 +9,7 @@
 //   kscale f32 [layers], per layer two u32 words {max|K| bf16 bits, largest
 //   V norm float bits}, per layer 512 words of compress scratch (partial
 //   maxima of max|K|, 1/s, the max|K| kernel's arrival counter), status int32. Block-scaled pools (kvpool_create_ex, k_block 32)
-//   also hold per layer kscales f32 [Hk][ctx_pad][D/32] and a split-context
-//   attention scratch.
+//   also hold per layer kscales f32 [Hk][ctx_pad][D/32].
 // Attention needs no scratch: the CTAs of a cluster merge their context
 // splits through distributed shared memory. Each layer also has a TMA tensor
 // map of its kq (rows of head_dim bytes) for the attention kernel.
@@ -197,9 +196,6 @@ struct kvpool {
     float* kscale = nullptr;
     uint32_t* kabsmax = nullptr;
     uint32_t* kpart = nullptr;
-    float* split_acc = nullptr;  // block-scaled pools: split-context attention scratch
-    float* split_ml = nullptr;
-    int split_n = 0;
     int* status = nullptr;
 
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
@@ -341,18 +337,6 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
     off = align256(off + 8 * (size_t)layers);
     const size_t off_kpart = off;  // per layer: compress scratch (partial maxima, 1/s, arrival counter)
     off = align256(off + 4 * (size_t)kvp::kKmaxParts * layers);
-    // block-scaled pools attend on CUDA cores: split scratch for max_rows rows,
-    // about two splits per SM over the KV heads
-    size_t off_sacc = off, off_sml = off;
-    if (k_block) {
-        const int ntile = (p->ctx + 31) / 32;
-        p->split_n = std::max(1, std::min(ntile, (2 * p->sm_count + kv_heads - 1) / kv_heads));
-        const size_t rows = (size_t)kv_heads * p->split_n * max_rows;
-        off_sacc = off;
-        off = align256(off + rows * head_dim * 4);
-        off_sml = off;
-        off = align256(off + rows * 2 * 4);
-    }
     const size_t off_status = off;
     off = align256(off + 4);
     p->bytes = off;
@@ -371,10 +355,6 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
     p->kscale = reinterpret_cast<float*>(p->base + off_scale);
     p->kabsmax = reinterpret_cast<uint32_t*>(p->base + off_absmax);
     p->kpart = reinterpret_cast<uint32_t*>(p->base + off_kpart);
-    if (k_block) {
-        p->split_acc = reinterpret_cast<float*>(p->base + off_sacc);
-        p->split_ml = reinterpret_cast<float*>(p->base + off_sml);
-    }
     p->status = reinterpret_cast<int*>(p->base + off_status);
     p->kmaps.resize(layers);
     for (int l = 0; l < layers; ++l) {
@@ -492,18 +472,8 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     a.early = p->may_read_early(stream, layer) ? 1 : 0;
     a.t0 = 0;
     a.t1 = p->len[layer];
-    cudaError_t e;
-    if (p->k_block) {  // block-scaled K: CUDA-core split kernels, the pool's own scratch
-        kvp::AttendScratch scr;
-        scr.acc = p->split_acc;
-        scr.ml = p->split_ml;
-        scr.nsplit = p->split_n;
-        scr.max_rows = p->max_rows;
-        e = kvp::launch_attend_split(p->shape_of(layer), p->layer(layer), a, scr, static_cast<cudaStream_t>(stream));
-    } else {
-        e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
-                                  static_cast<cudaStream_t>(stream));
-    }
+    const cudaError_t e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
+                                                static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
 }
@@ -520,7 +490,6 @@ int kvpool_attend_partial(kvpool_t* p, int layer, const void* Q, int agents, int
     const int group = q_heads / p->kv_heads;
     if ((long long)agents * group > p->max_rows) return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
-    if (p->k_block) return KVPOOL_ERR_UNSUPPORTED;
     if (t_begin < 0 || t_begin % kvp::kTokenPad != 0 || t_end <= t_begin || t_end > p->len[layer])
         return KVPOOL_ERR_INVALID_ARG;
     kvp::AttendArgs a{};

@@ -8,7 +8,8 @@ state of that slice: the slice's output H acc / (D l) within 2e-3 (the
 attention metric) and its log-sum-exp m + log2 l within 1e-3 (log2 units).
 The merged parts, with and without the agents' bf16 tails, must give the
 oracle's attention over the whole context within 2e-3 and agree with
-kvpool_attend. Argument errors are refused."""
+kvpool_attend. Argument errors are refused. Block-scaled pools take the same
+calls."""
 
 import numpy as np
 import pytest
@@ -20,7 +21,7 @@ from parity_util import TOL, to_dev
 
 pytestmark = pytest.mark.gpu
 
-INVALID_ARG, UNSUPPORTED = -1, -7
+INVALID_ARG = -1
 
 
 @pytest.fixture(scope="module")
@@ -131,10 +132,29 @@ def test_refusals(kp):
             pool.attend_partial(0, Q, b, e)
         assert err.value.code == INVALID_ARG, (b, e)
     pool.close()
-    kb = kp.KVPool(1, 2, 64, 300, [3], k_block=32)
+
+
+def test_block_scaled_slices(kp):
+    # block-scaled K: slice states and their merge against the oracle
+    import torch
+
+    w = wl.custom("cp_kb", 1, 4, 16, 128, 1100, 5, "lognormal", 0, 1, (3,))
+    pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [3], k_block=32)
     K, V = wl.layer_kv(w, 0)
-    kb.compress(0, to_dev(K), to_dev(V))
-    with pytest.raises(kp.KVPoolError) as err:
-        kb.attend_partial(0, Q, 0, 300)
-    assert err.value.code == UNSUPPORTED
-    kb.close()
+    pool.compress(0, to_dev(K), to_dev(V))
+    Kh, Vh = attention.dequantise_f64(codec.encode_layer(K, V, 3, k_block=32))
+    Qh = wl.layer_q(w, 0)
+    Q = to_dev(Qh)
+    MLs, ACCs = [], []
+    for b, e in [(0, 384), (384, 1100)]:
+        ml, acc = pool.attend_partial(0, Q, b, e)
+        lse_g, o_g = _slice_state(ml, acc, 128, 4)
+        lse_r, o_r = attention.attend_slice_f64(Kh, Vh, Qh, b, e)
+        assert _row_err(o_g, o_r) <= TOL
+        assert np.abs(lse_g - lse_r).max() <= 1e-3
+        MLs.append(ml)
+        ACCs.append(acc)
+    out = kp.merge_partials(torch.stack(MLs), torch.stack(ACCs), Q, w.kv_heads)
+    assert _row_err(out.cpu().numpy(), attention.attend_f64(Kh, Vh, Qh)) <= TOL
+    assert pool.status() == 0
+    pool.close()

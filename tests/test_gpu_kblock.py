@@ -1,8 +1,9 @@
 """GPU parity of block-scaled K pools (kvpool_create_ex with k_block = 32, the
 "q8_0" reading): int8 K codes, their float32 block scales, V codes and norms
-bit-exact; decompress bit-exact; attention (CUDA-core split kernels over the
-pool) within 2e-3 of the oracle's float64 attention over the same
-dequantised cache."""
+bit-exact; decompress bit-exact; attention (the tensor-core kernel, K^ as fp16
+hi + lo of each block's codes times its scale) within 2e-3 of the oracle's
+float64 attention over the same dequantised cache: row groups of at most 64
+rows (spread layout) and of 128, with and without tails."""
 
 import numpy as np
 import pytest
@@ -56,6 +57,8 @@ SMALL = [
     ("kb_d64_3bit_tail", 2, 4, 64, 700, 6, 3, 20),
     ("kb_4bit_tail", 2, 16, 128, 1000, 2, 4, 7),
     ("kb_ctx1", 1, 2, 128, 1, 4, 3, 3),
+    ("kb_128rows_3bit", 2, 16, 128, 600, 16, 3, 0),
+    ("kb_200rows_d64_4bit_tail", 2, 16, 64, 900, 25, 4, 9),
 ]
 
 
