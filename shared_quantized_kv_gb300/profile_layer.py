@@ -3,13 +3,15 @@ times, for profilers (ncu captures one kernel of one repetition).
 
     python -m shared_quantized_kv_gb300.profile_layer --workload llama3_8b_4k --reps 4
     python -m shared_quantized_kv_gb300.profile_layer --workload llama3_8b_4k --layers 8
+    python -m shared_quantized_kv_gb300.profile_layer --workload llama3_8b_4k --k-block 32
 
 Every repetition re-arms the layer (kvpool_reset_layer), compresses it,
 attends all agents and decompresses it; the script exits non-zero if the
 device status word reports an error. Inputs are the seeded synthetic layer of
 the workload (layer 0 unless --layer is given). With --layers N (N > 1) the
 first N layers of the workload go through the multi-layer calls: one
-compress and one decompress call for all N, attend per layer.
+compress and one decompress call for all N, attend per layer. --k-block 32
+builds the pool with block-scaled K.
 """
 
 import argparse
@@ -28,12 +30,13 @@ def main() -> int:
     ap.add_argument("--layer", type=int, default=0)
     ap.add_argument("--reps", type=int, default=4)
     ap.add_argument("--layers", type=int, default=1)
+    ap.add_argument("--k-block", type=int, default=0, choices=[0, 32])
     args = ap.parse_args()
     w = wl.WORKLOADS[args.workload]
     if args.layers > 1:
         return multi(w, args)
     bits = w.layer_bits(args.layer)
-    pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [bits])
+    pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [bits], k_block=args.k_block)
     K, V = wl.layer_kv_torch(w, args.layer, "cuda")
     Q = torch.from_numpy(wl.layer_q(w, args.layer).view(np.int16)).cuda().view(torch.bfloat16)
     out = torch.empty((w.agents, w.q_heads, w.head_dim), dtype=torch.float32, device="cuda")
@@ -53,7 +56,7 @@ def main() -> int:
 def multi(w, args) -> int:
     n = min(args.layers, w.layers)
     bits = [w.layer_bits(l) for l in range(n)]
-    pool = kp.KVPool(n, w.kv_heads, w.head_dim, w.ctx, bits)
+    pool = kp.KVPool(n, w.kv_heads, w.head_dim, w.ctx, bits, k_block=args.k_block)
     KV = [wl.layer_kv_torch(w, l, "cuda") for l in range(n)]
     Ks, Vs = [k for k, _ in KV], [v for _, v in KV]
     Q = [torch.from_numpy(wl.layer_q(w, l).view(np.int16)).cuda().view(torch.bfloat16) for l in range(n)]
