@@ -947,9 +947,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 #pragma unroll
                         for (int w2 = 0; w2 < 2; ++w2) {
                             const int k = k4 * 2 + w2;  // token pair (2k, 2k + 1) of the chunk
-                            const float2 d = __fmul2_rn(make_float2(__fadd_rn(__uint_as_float(u[2 * k]), ns.x),
-                                                                    __fadd_rn(__uint_as_float(u[2 * k + 1]), ns.y)),
-                                                        c2);
+                            const float2 d = __fmul2_rn(
+                                __fadd2_rn(make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1])), ns), c2);
                             const float2 pv = make_float2(ptx::ex2(d.x), ptx::ex2(d.y));  // -inf -> 0
                             l2 = __fadd2_rn(l2, pv);
                             const float2 pp = __fmul2_rn(pv, w2 ? make_float2(nn.z, nn.w) : make_float2(nn.x, nn.y));
