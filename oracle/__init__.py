@@ -14,7 +14,8 @@ What it computes (a plain restatement of the pages, slow and in plain numpy):
 * ``codec``      -- the write-once encode of one layer: per-tensor symmetric int8
   K, and V rotated per head-vector by the fast Walsh-Hadamard transform, scaled
   to N(0, 1) by the vector norm and mapped to the nearest centroid, bit-packed;
-  and the decompress (centroid lookup + inverse FWHT) to bf16.
+  and the decompress (centroid lookup + inverse FWHT) to bf16; layers built
+  from 32-token groups of their own V widths (``encode_layer_groups``).
 * ``attention``  -- float64 decode attention of every agent's query rows over
   the dequantised pool plus the agent's private bf16 tail (plain softmax
   definition).
@@ -27,8 +28,9 @@ Sources, cited by page title and section:
   N(0,1) centroids, 3-bit; dequantisation by centroid lookup + inverse FWHT;
   ratio 16/((8+3)/2)).
 * "CoMixKV ... Qwen3显存降低32.08%" (zicq.com article), sections on the
-  incremental quantisation strategy (recent states stay at native precision)
-  and on 2-4 bit per-layer precision.
+  incremental quantisation strategy (recent states stay at native precision;
+  a new width applies only to blocks quantised afterwards) and on 2-4 bit
+  per-layer precision.
 
 Where the pages are silent the readings are fixed in each function's docstring.
 

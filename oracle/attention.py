@@ -40,16 +40,22 @@ def hadamard(d: int) -> np.ndarray:
 
 def dequantise_f64(enc: dict):
     """(K_hat, V_hat) in float64, [kv_heads, ctx, d], from the stored codes."""
-    cen, _ = lloyd_max.tables_f32(enc["bits"])
     codes = enc["codes"]
     d = codes.shape[-1]
+    # centroid of every code (per-group widths: each token's own table)
+    widths = codec.token_widths(enc, codes.shape[1])
+    cval = np.zeros(codes.shape, dtype=np.float64)
+    for b in np.unique(widths):
+        cen, _ = lloyd_max.tables_f32(int(b))
+        sel = widths == b
+        cval[:, sel] = cen.astype(np.float64)[codes[:, sel]]
     if enc.get("k_block"):
         kb = enc["k_block"]
         q = enc["kq"].astype(np.float64)
         K = (q.reshape(q.shape[:-1] + (d // kb, kb)) * enc["kscales"].astype(np.float64)[..., None]).reshape(q.shape)
     else:
         K = enc["kq"].astype(np.float64) * float(enc["scale"])
-    rot = cen.astype(np.float64)[codes] * enc["norms"].astype(np.float64)[..., None]
+    rot = cval * enc["norms"].astype(np.float64)[..., None]
     V = rot @ hadamard(d) / d
     return K, V
 

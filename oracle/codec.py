@@ -274,7 +274,14 @@ def decompress_layer(enc: dict):
         K = k_dequantize_block_bf16(enc["kq"], enc["kscales"])
     else:
         K = k_dequantize_bf16(enc["kq"], enc["scale"])
-    return K, v_decompress_bf16(enc["codes"], enc["norms"], enc["bits"])
+    if enc.get("widths") is None:
+        return K, v_decompress_bf16(enc["codes"], enc["norms"], enc["bits"])
+    # per-group widths: each group decodes with its own table
+    V = np.zeros(enc["codes"].shape, dtype=np.uint16)
+    for g, b in enumerate(enc["widths"]):
+        sl = slice(g * GROUP, (g + 1) * GROUP)
+        V[:, sl] = v_decompress_bf16(enc["codes"][:, sl], enc["norms"][:, sl], b)
+    return K, V
 
 
 def layer_bytes(kv_heads: int, ctx: int, head_dim: int, bits: int) -> int:
@@ -282,3 +289,84 @@ def layer_bytes(kv_heads: int, ctx: int, head_dim: int, bits: int) -> int:
     scale (no padding)."""
     n = kv_heads * ctx
     return n * head_dim + n * head_dim * bits // 8 + 4 * n + 4
+
+
+# ------------------------------------------------- per-group V widths (appends)
+#
+# CoMixKV article, section "增量量化策略" (incremental quantisation strategy):
+# a width newly chosen by the allocator applies only to cache blocks quantised
+# afterwards; blocks already quantised keep their width and bytes. With the
+# pool's 32-token groups as the blocks, a layer is then a sequence of groups,
+# group g coded at its own width b_g with the same per-vector pipeline as
+# above (norm, FWHT, midpoint count against b_g's table). Readings (the
+# article fixes no layout):
+#   * a group's bytes are the uniform layout's bytes for those 32 tokens at
+#     b_g (d sequences of 4*b_g bytes, coordinate order);
+#   * per KV head the groups follow each other in token order with no gap, so
+#     group g starts at byte sum_{g' < g} d * 4 * b_{g'} of the head's codes.
+# A layer whose groups all have width b is exactly pack_pool_v(codes, b).
+
+
+def pack_pool_v_groups(codes: np.ndarray, widths) -> np.ndarray:
+    """Per-group-width layout of one layer's V codes [kv_heads, ctx, d] with
+    widths[g] the width of tokens [32 g, 32 g + 32): uint8 [kv_heads,
+    sum_g d * 4 * widths[g]]."""
+    c = np.asarray(codes, dtype=np.uint8)
+    H, T, d = c.shape
+    ng = -(-T // GROUP)
+    if len(widths) != ng:
+        raise ValueError("one width per 32-token group")
+    parts = []
+    for g in range(ng):
+        tok = c[:, g * GROUP:(g + 1) * GROUP]
+        parts.append(pack_pool_v(tok, int(widths[g])).reshape(H, -1))
+    return np.concatenate(parts, axis=1)
+
+
+def unpack_pool_v_groups(packed: np.ndarray, widths, ctx: int, d: int) -> np.ndarray:
+    """Inverse of pack_pool_v_groups: codes [kv_heads, ctx, d]."""
+    p = np.asarray(packed, dtype=np.uint8)
+    H = p.shape[0]
+    out, off = [], 0
+    for b in widths:
+        n = d * 4 * int(b)
+        out.append(unpack_pool_v(p[:, off:off + n].reshape(H, 1, d, 4 * int(b)), int(b), GROUP))
+        off += n
+    if off != p.shape[1]:
+        raise ValueError("byte count does not match the widths")
+    return np.concatenate(out, axis=1)[:, :ctx]
+
+
+def encode_layer_groups(K_bf16, V_bf16, widths, k_block: int = 32) -> dict:
+    """Everything the pool stores for a layer built from 32-token groups of
+    per-group V widths (widths[g] in {2, 3, 4} for tokens [32 g, 32 g + 32)).
+    K as in encode_layer (block-scaled by default: the pools that take
+    appends); every group's codes and norms are those of its own tokens."""
+    V = np.asarray(V_bf16)
+    H, T, d = V.shape
+    widths = [int(b) for b in widths]
+    if len(widths) != -(-T // GROUP):
+        raise ValueError("one width per 32-token group")
+    codes = np.zeros((H, T, d), dtype=np.uint8)
+    norms = np.zeros((H, T), dtype=np.float32)
+    for g, b in enumerate(widths):
+        sl = slice(g * GROUP, min(T, (g + 1) * GROUP))
+        codes[:, sl], norms[:, sl] = v_codes(V[:, sl], b)
+    enc = dict(bits=None, widths=widths, codes=codes, norms=norms, packed=pack_pool_v_groups(codes, widths),
+               k_block=k_block)
+    if k_block:
+        if k_block != K_BLOCK:
+            raise ValueError("k_block must be 0 or 32")
+        sc = k_scales_block(K_bf16)
+        enc.update(absmax=F32(0), scale=F32(1), kscales=sc, kq=k_quantize_block(K_bf16, sc))
+    else:
+        absmax, scale = k_scale(K_bf16)
+        enc.update(absmax=absmax, scale=scale, kq=k_quantize(K_bf16, scale))
+    return enc
+
+
+def token_widths(enc: dict, T: int) -> np.ndarray:
+    """Width of every token of an encoded layer (int [T])."""
+    if enc.get("widths") is None:
+        return np.full(T, enc["bits"], dtype=np.int64)
+    return np.repeat(np.asarray(enc["widths"], dtype=np.int64), GROUP)[:T]
