@@ -95,6 +95,16 @@ typedef struct {
     int k_block;           /* 0 (per-tensor scale) or 32                       */
     int len;               /* tokens the layer holds: ctx once compressed or
                               imported; appends (kvpool_append) grow it         */
+    const uint8_t* group_bits; /* block-scaled pools: uint8 [ctx_padded/32],
+                              device, the V width of each 32-token group
+                              (entries from ceil(len/32) on are not
+                              meaningful); NULL for per-tensor pools         */
+    const uint32_t* group_off; /* block-scaled pools: uint32 [ctx_padded/32],
+                              device, the byte offset of each written group
+                              within its KV head's codes; NULL otherwise      */
+    int mixed;             /* 1 if the written groups do not all have width
+                              `bits` (kvpool_append_bits); the layout is then
+                              the per-group one of kvpool_append_bits         */
 } kvpool_layer_view_t;
 
 /* Create a pool for `layers` layers of a shared context of `ctx` tokens with
@@ -149,6 +159,30 @@ int kvpool_export_kscales(const kvpool_t* pool, int layer, float* kscales, void*
  * scale cannot take new tokens without re-encoding the old ones). */
 int kvpool_append(kvpool_t* pool, int layer, const void* K, const void* V, int n, void* stream);
 
+/* kvpool_append with the V codes of the n new tokens at width `bits` (2, 3
+ * or 4, at most the layer's width fixed at create, which sets the layer's
+ * reserved size). CoMixKV article, incremental quantisation strategy: a
+ * width newly chosen by the allocator (kvpool_allocate_bits) applies only to
+ * blocks quantised afterwards; earlier blocks keep their width and bytes.
+ * The unit is the 32-token group: every group has one width, and per KV head
+ * the groups' codes follow each other in token order with no gap (group g at
+ * byte sum_{g' < g} head_dim * 4 * b_{g'} of the head's codes, which start at
+ * h * ctx_padded * head_dim * bits_create / 8), each group in the uniform
+ * layout of kvpool_layer_view_t at its own width. Attend, partial attend and
+ * decompress read every group at its width; kvpool_export_layer writes each
+ * head's groups back to back (kv_heads * sum_g head_dim * 4 * b_g bytes; see
+ * kvpool_layer_widths). Errors as kvpool_append, and KVPOOL_ERR_INVALID_ARG
+ * for a width outside [2, create width]. */
+int kvpool_append_bits(kvpool_t* pool, int layer, const void* K, const void* V, int n, int bits,
+                       void* stream);
+
+/* Widths of the 32-token groups layer `layer` holds: writes the width of
+ * group g (tokens [32 g, 32 g + 32)) to widths[g] for g < max_groups (host
+ * array; may be NULL when max_groups is 0) and returns the number of groups,
+ * ceil(kvpool_layer_len / 32), or a negative error code. Per-tensor pools and
+ * layers filled by kvpool_compress report the layer's width for every group. */
+int kvpool_layer_widths(const kvpool_t* pool, int layer, uint8_t* widths, int max_groups);
+
 /* Tokens layer `layer` holds (see kvpool_append), or a negative error code. */
 int kvpool_layer_len(const kvpool_t* pool, int layer);
 
@@ -178,8 +212,9 @@ int kvpool_sensitivity(const void* Q, int agents, int q_heads, const kvpool_tail
  * cost[l] >= 1: the layer's V bytes per bit of width (kv_heads * tokens *
  * head_dim / 8 for a pool layer). KVPOOL_ERR_INVALID_ARG when even 2 bits
  * everywhere exceed the budget, KVPOOL_ERR_UNSUPPORTED when the table would
- * exceed 2^26 entries. The widths apply to layers created or appended later
- * (a pool's layer widths are fixed at kvpool_create). */
+ * exceed 2^26 entries. The widths apply to layers created later
+ * (kvpool_create) or, in block-scaled pools, to the blocks appended later
+ * (kvpool_append_bits, up to each layer's create width). */
 int kvpool_allocate_bits(int layers, const double* sens, const int64_t* cost, int64_t budget, uint8_t* bits);
 
 /* Free all device memory of the pool. Waits for the device first. NULL is a
@@ -300,7 +335,10 @@ int kvpool_layer_view(const kvpool_t* pool, int layer, kvpool_layer_view_t* view
  * convenience only.
  *
  * Inputs and outputs are the caller's: one compressed layer in the pool's
- * layout (as kvpool_layer_view describes it, token axis padded to
+ * uniform layout (every group at width `bits`; layers of per-group widths,
+ * kvpool_layer_view_t.mixed = 1, are not supported here and give wrong
+ * results; the library cannot tell from these pointers), as
+ * kvpool_layer_view describes it (token axis padded to
  * ctx_padded = ctx rounded up to a multiple of 128): kq int8
  * [kv_heads][ctx_padded][head_dim], vcodes uint8 [kv_heads][ctx_padded/32]
  * [head_dim][4*bits], vnorm float [kv_heads][ctx_padded], kscale one float;
@@ -330,8 +368,10 @@ int kvpool_attend_noalloc(const int8_t* kq, const uint8_t* vcodes, const float* 
 /* Copy the stored bytes of one compressed layer, token padding removed, to
  * caller buffers in host or device memory (any of the four may be NULL):
  * kq int8 [kv_heads][ctx][head_dim], vcodes uint8 [kv_heads][ceil(ctx/32)]
- * [head_dim][4*bits] (whole 32-token groups, see kvpool_layer_view_t), vnorm
- * float [kv_heads][ctx], kscale one float. Asynchronous on
+ * [head_dim][4*bits] (whole 32-token groups, see kvpool_layer_view_t; a layer
+ * of per-group widths: uint8 [kv_heads][sum_g head_dim * 4 * b_g], see
+ * kvpool_append_bits), vnorm float [kv_heads][ctx], kscale one float.
+ * Asynchronous on
  * `stream` (host buffers should be pinned). This is the quantised-cache handoff
  * of the QKVShare blog (mhpn.cn, section 3.1: the sender packs the quantised
  * cache with its scales; the receiver loads it instead of recomputing). */

@@ -106,6 +106,13 @@ struct Params {
     float* part_ml;   // partial mode ([Hk][R][2] and [Hk][R][D]), else null
     float* part_acc;
     const float* kscales;  // block-scaled K: [Hk][ctx_pad][D/32] (instances with KB), else unused
+    // per-group V widths (instances with MIX): the width of each 32-token
+    // group, its byte offset within a KV head's codes, the bytes per KV head,
+    // and the operand tables of widths 2, 3, 4 under one lam (as tlo / thi)
+    const uint8_t* gbits;
+    const uint32_t* goff;
+    long long vhead;
+    uint32_t mlo[3][4], mhi[3][4];
 };
 
 // operand stages (block-scaled K^ takes twice the room, leaving one raw stage)
@@ -447,7 +454,32 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, bool& b
 // above the token's largest s_b, as fp16 hi + lo (~21 significant bits), and
 // sigma_t into a two-slot ring; S takes both halves (16 MMAs) and the softmax
 // scales S column t by sigma_t (exact).
-template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
+// the 32 codes of a group of width w (one coordinate's sequence at `seq`)
+// with the tables of Params::mlo / mhi; w = 0 (a group not written): zeros
+__device__ __forceinline__ void decode32_mixed(const unsigned char* seq, int w, const Params& p, uint32_t* h) {
+    uint32_t tl[4], th[4];
+    if (w == 2) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { tl[k] = p.mlo[0][k]; th[k] = p.mhi[0][k]; }
+        decode32<2>(seq, tl, th, h);
+    } else if (w == 3) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { tl[k] = p.mlo[1][k]; th[k] = p.mhi[1][k]; }
+        decode32<3>(seq, tl, th, h);
+    } else if (w == 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) { tl[k] = p.mlo[2][k]; th[k] = p.mhi[2][k]; }
+        decode32<4>(seq, tl, th, h);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 16; ++k) h[k] = 0u;
+    }
+}
+
+// MIX: a block-scaled layer whose 32-token groups have their own V widths
+// (at most BITS, which sizes the raw stages); a tile's code bytes are its four
+// groups back to back
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB, bool MIX = false>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     constexpr int HC = D / 2;                // O columns per softmax half
@@ -506,14 +538,30 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const int nag = nrows / p.G;
     const int own_cnt = crank < nag ? ((nag - crank + S - 1) / S) * p.G : 0;
 
+    // MIX: the widths of the four groups of tile i, one per byte (the tile
+    // starts at a multiple of 128 tokens, so they are one aligned word)
+    auto tile_widths = [&](int i) {
+        return __ldg(reinterpret_cast<const uint32_t*>(p.gbits) + (t_begin + i * kTile) / 128);
+    };
     auto issue_tile = [&](int i) {
         const int s = i % NR;
         const long long t0 = head_tok + t_begin + (long long)i * kTile;
         const uint32_t dst = ptx::smem_u32(sm + lay.raw0 + s * lay.raw);
         const uint32_t bar = b_raw_full + 8 * s;
-        ptx::mbar_expect_tx(bar, raw_bytes);
-        ptx::tma_load_2d(dst, &kmap, 0, (int)t0, bar);
-        ptx::bulk_g2s(dst + lay.raw_v, p.vcodes + t0 * VB, kTile * VB, bar);
+        if constexpr (MIX) {
+            const uint32_t wd = tile_widths(i);
+            const uint32_t nb =
+                (uint32_t)D * 4 * ((wd & 0xFFu) + ((wd >> 8) & 0xFFu) + ((wd >> 16) & 0xFFu) + (wd >> 24));
+            ptx::mbar_expect_tx(bar, (uint32_t)(kTile * D + kTile * 4) + nb);
+            ptx::tma_load_2d(dst, &kmap, 0, (int)t0, bar);
+            if (nb)
+                ptx::bulk_g2s(dst + lay.raw_v, p.vcodes + g * p.vhead + __ldg(p.goff + (t_begin + i * kTile) / 32),
+                              nb, bar);
+        } else {
+            ptx::mbar_expect_tx(bar, raw_bytes);
+            ptx::tma_load_2d(dst, &kmap, 0, (int)t0, bar);
+            ptx::bulk_g2s(dst + lay.raw_v, p.vcodes + t0 * VB, kTile * VB, bar);
+        }
         ptx::bulk_g2s(dst + lay.raw_n, p.vnorm + t0, kTile * 4, bar);
     };
 
@@ -757,11 +805,20 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             {
                 constexpr int GPT = 4 * D / kExpThreads;  // groups per thread
                 const int c = et % D, g0 = (et / D) * GPT;
+                const uint32_t wd = MIX ? tile_widths(i) : 0u;
 #pragma unroll
                 for (int gg = 0; gg < GPT; ++gg) {
                     const int gi = g0 + gg;
                     uint32_t h[16];
-                    decode32<BITS>(raw + lay.raw_v + gi * GB + c * (4 * BITS), tlo, thi, h);
+                    if constexpr (MIX) {
+                        // group gi's width (warp-uniform) and the bytes of the groups before it
+                        const int w = (int)((wd >> (8 * gi)) & 0xFFu);
+                        const uint32_t below = gi == 0 ? 0u : (wd & (0xFFFFFFFFu >> (32 - 8 * gi)));
+                        const uint32_t nbelow = (below & 0xFFu) + ((below >> 8) & 0xFFu) + ((below >> 16) & 0xFFu);
+                        decode32_mixed(raw + lay.raw_v + nbelow * (D * 4) + c * (4 * w), w, p, h);
+                    } else {
+                        decode32<BITS>(raw + lay.raw_v + gi * GB + c * (4 * BITS), tlo, thi, h);
+                    }
 #pragma unroll
                     for (int m = 0; m < 4; ++m)
                         *reinterpret_cast<uint4*>(opv + kmajor_off(c, gi * 4 + m, VBLK)) =
@@ -1162,23 +1219,23 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 
 // ------------------------------------------------------------------ launch
 
-template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB, bool MIX>
 void configure() {
     static bool done = false;
     if (done) return;
-    auto kern = attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>;
+    auto kern = attend_rows_kernel<D, BITS, TAIL, SPREAD, KB, MIX>;
     cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     done = true;
 }
 
 // How many clusters of S CTAs with `smem` bytes each can be resident at once.
-template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB, bool MIX>
 int max_clusters(int S, size_t smem) {
     static int cache[kMaxCluster + 1][2] = {};  // [S] -> (smem key / 1024 + 1, count)
     const int key = (int)(smem / 1024) + 1;
     if (cache[S][0] == key) return cache[S][1];
-    configure<D, BITS, TAIL, SPREAD, KB>();
+    configure<D, BITS, TAIL, SPREAD, KB, MIX>();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -1191,7 +1248,7 @@ int max_clusters(int S, size_t smem) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB, MIX>, &cfg) != cudaSuccess) {
         cudaGetLastError();
         n = 0;
     }
@@ -1200,9 +1257,9 @@ int max_clusters(int S, size_t smem) {
     return n;
 }
 
-template <int D, int BITS, bool TAIL, bool SPREAD, bool KB>
+template <int D, int BITS, bool TAIL, bool SPREAD, bool KB, bool MIX>
 cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
-    configure<D, BITS, TAIL, SPREAD, KB>();
+    configure<D, BITS, TAIL, SPREAD, KB, MIX>();
     constexpr uint32_t kMaxSmem = 227 * 1024;
     const int rows_cta = std::min(prm.RW, prm.R);
     const int agents_cta = rows_cta / prm.G;
@@ -1221,7 +1278,7 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
         const Layout lay = make_layout(D, BITS, std::min(max_nr, per), KB);
         if (staging_bytes(D, kM) + (size_t)S * own * (D + 4) * 4 > lay.misc) continue;
         const size_t smem = lay.total + 1024;
-        const int n = max_clusters<D, BITS, TAIL, SPREAD, KB>(S, smem);
+        const int n = max_clusters<D, BITS, TAIL, SPREAD, KB, MIX>(S, smem);
         if (n < 1) continue;
         const long long waves = (clusters + n - 1) / n;
         const long long cost = waves * per;
@@ -1252,13 +1309,14 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB>, kmap, prm);
+    return cudaLaunchKernelEx(&cfg, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB, MIX>, kmap, prm);
 }
 
 }  // namespace rows
 
-// Launch for layers whose V codes have BITS bits.
-template <int BITS>
+// Launch for layers whose V codes have BITS bits (MIX: block-scaled layers
+// whose groups have their own widths, BITS the largest).
+template <int BITS, bool MIX>
 cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const AttendArgs& a, int* status,
                                     cudaStream_t st) {
     using namespace rows;
@@ -1294,18 +1352,34 @@ cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const At
     prm.scale_log2 = a.scale_log2;
     prm.early = a.early;
     prm.status = status;
-    const Codebook& cb = codebook(BITS);
-    for (int k = 0; k < 16; ++k) {
-        prm.tlo[k / 4] |= (uint32_t)(cb.c16[k] & 0xFF) << (8 * (k % 4));
-        prm.thi[k / 4] |= (uint32_t)(cb.c16[k] >> 8) << (8 * (k % 4));
+    if constexpr (MIX) {
+        if (!L.kscales || !L.gbits || !L.goff) return cudaErrorInvalidValue;
+        const MixBook& mb = mixbook();
+        for (int w = 0; w < 3; ++w)
+            for (int k = 0; k < 16; ++k) {
+                prm.mlo[w][k / 4] |= (uint32_t)(mb.c16[w][k] & 0xFF) << (8 * (k % 4));
+                prm.mhi[w][k / 4] |= (uint32_t)(mb.c16[w][k] >> 8) << (8 * (k % 4));
+            }
+        prm.inv_lam = 1.0f / mb.lam;
+        prm.gbits = L.gbits;
+        prm.goff = L.goff;
+        prm.vhead = L.vhead;
+    } else {
+        const Codebook& cb = codebook(BITS);
+        for (int k = 0; k < 16; ++k) {
+            prm.tlo[k / 4] |= (uint32_t)(cb.c16[k] & 0xFF) << (8 * (k % 4));
+            prm.thi[k / 4] |= (uint32_t)(cb.c16[k] >> 8) << (8 * (k % 4));
+        }
+        prm.inv_lam = 1.0f / cb.lam;
     }
-    prm.inv_lam = 1.0f / cb.lam;
     prm.kscales = L.kscales;
     const CUtensorMap& km = *L.kmap;
     const bool tail = prm.tK != nullptr;
     const bool kb = L.kscales != nullptr;
-#define KVP_ROWS_LAUNCH(DD, TT, SS, KK) launch_cfg<DD, BITS, TT, SS, KK>(km, prm, ntiles, s.kv_heads, RGN, st)
-#define KVP_ROWS_KB(DD, TT, SS) (kb ? KVP_ROWS_LAUNCH(DD, TT, SS, true) : KVP_ROWS_LAUNCH(DD, TT, SS, false))
+#define KVP_ROWS_LAUNCH(DD, TT, SS, KK) \
+    launch_cfg<DD, BITS, TT, SS, KK, MIX>(km, prm, ntiles, s.kv_heads, RGN, st)
+// (MIX instances are block-scaled only: their second branch is the first)
+#define KVP_ROWS_KB(DD, TT, SS) (kb ? KVP_ROWS_LAUNCH(DD, TT, SS, true) : KVP_ROWS_LAUNCH(DD, TT, SS, MIX))
     if (D == 64) {
         if (spread) return tail ? KVP_ROWS_KB(64, true, true) : KVP_ROWS_KB(64, false, true);
         return tail ? KVP_ROWS_KB(64, true, false) : KVP_ROWS_KB(64, false, false);

@@ -3,6 +3,6 @@
 #include "attend_rows.cuh"
 
 namespace kvp {
-template cudaError_t launch_attend_rows_bits<3>(const Shape&, const LayerBufs&, const AttendArgs&, int*,
-                                                  cudaStream_t);
+template cudaError_t launch_attend_rows_bits<3, false>(const Shape&, const LayerBufs&, const AttendArgs&, int*,
+                                                         cudaStream_t);
 }  // namespace kvp

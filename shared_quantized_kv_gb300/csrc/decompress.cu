@@ -43,14 +43,37 @@ __device__ __forceinline__ float2 i8x2_to_f2(uint32_t w, int k) {
                       make_float2(-12582912.0f, -12582912.0f));
 }
 
+// Centroids of the launch: c_BITS in entries [0, 2^BITS), or (layers of
+// per-group widths) the tables of widths 2, 3, 4 at entries 0, 4, 12.
+struct CenTable {
+    float c[28];
+};
+__host__ __device__ constexpr int mix_base(int w) { return w == 2 ? 0 : (w == 3 ? 4 : 12); }
+
+// one packed sequence of 32 codes of width B (4 * B bytes at `in`) into the
+// bytes dst[0], dst[D], ..., dst[31 D], each plus `base`
+template <int D, int B>
+__device__ __forceinline__ void unpack_seq(const uint32_t* __restrict__ in, uint8_t* dst, uint32_t base) {
+    constexpr uint32_t MASK = (1u << B) - 1;
+    uint32_t w[B + 1];
+#pragma unroll
+    for (int k = 0; k < B; ++k) w[k] = __ldg(in + k);
+    w[B] = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const int bit = j * B;
+        dst[j * D] = (uint8_t)(base + (__funnelshift_r(w[bit / 32], w[bit / 32 + 1], bit % 32) & MASK));
+    }
+}
+
 // One launch for both halves of every layer of the launch, grid (blocks, kv
 // heads, layers): the first nbv blocks of each head materialise V (D/32
-// threads per head-vector), the next nbk K (16 elements per thread).
-template <int D, int BITS>
+// threads per head-vector), the next nbk K (16 elements per thread). MIX:
+// layers of per-group V widths (each 32-token group read at its own width).
+template <int D, int BITS, bool MIX>
 __global__ void __launch_bounds__(kDecThreads, 5)  // five CTAs per SM: both halves in one wave
-decompress_kernel(const __grid_constant__ DecBatch b, int ctx_pad, Codebook cb) {
+decompress_kernel(const __grid_constant__ DecBatch b, int ctx_pad, const __grid_constant__ CenTable ct) {
     constexpr int TPV = D / 32;
-    constexpr uint32_t MASK = (1u << BITS) - 1;
     constexpr int VPB = kDecThreads / TPV;  // head-vectors per V block (a multiple of 32)
     const DecLayer& Ly = b.L[blockIdx.z];
     const int tid = threadIdx.x;
@@ -99,25 +122,31 @@ decompress_kernel(const __grid_constant__ DecBatch b, int ctx_pad, Codebook cb) 
     // ---- V = bf16(fl(fl(z * n) * (1/d))), z = FWHT(c[codes])
     // the block's code groups (pool layout: per 32 tokens, one sequence per
     // coordinate) are unpacked into bytes [token][coordinate] first
-    __shared__ float cen[16];
+    __shared__ float cen[28];
     __shared__ __align__(16) uint8_t codes8[VPB * D];
-    if (tid < 16) cen[tid] = cb.c[tid];
+    if (tid < 28) cen[tid] = ct.c[tid];
     const int lt = tid % TPV;
     const int t = blockIdx.x * VPB + tid / TPV;
     const bool live = t < ctx;
     const float n = live ? __ldg(Ly.vnorm + head * ctx_pad + t) : 0.f;  // in flight during the unpacking
     {
         const int gq = tid / D, c = tid % D;
-        const long long grp = (head * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
-        const uint32_t* in = reinterpret_cast<const uint32_t*>(Ly.vcodes + (grp * D + c) * (4 * BITS));
-        uint32_t w[BITS + 1];
+        uint8_t* dst = codes8 + gq * 32 * D + c;
+        if constexpr (MIX) {
+            // the group's width (warp-uniform: a warp serves one group); a
+            // group not written holds no live token
+            const int gi = blockIdx.x * (VPB / 32) + gq;
+            const int w = __ldg(Ly.gbits + gi);
+            const unsigned char* grp = Ly.vcodes + head * Ly.vhead + (w ? __ldg(Ly.goff + gi) : 0u);
+            if (w == 2) unpack_seq<D, 2>(reinterpret_cast<const uint32_t*>(grp + c * 8), dst, mix_base(2));
+            else if (w == 3) unpack_seq<D, 3>(reinterpret_cast<const uint32_t*>(grp + c * 12), dst, mix_base(3));
+            else if (w == 4) unpack_seq<D, 4>(reinterpret_cast<const uint32_t*>(grp + c * 16), dst, mix_base(4));
+            else
 #pragma unroll
-        for (int k = 0; k < BITS; ++k) w[k] = __ldg(in + k);
-        w[BITS] = 0;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const int bit = j * BITS;
-            codes8[(gq * 32 + j) * D + c] = (uint8_t)(__funnelshift_r(w[bit / 32], w[bit / 32 + 1], bit % 32) & MASK);
+                for (int j = 0; j < 32; ++j) dst[j * D] = 0;
+        } else {
+            const long long grp = (head * ctx_pad + (long long)blockIdx.x * VPB) / 32 + gq;
+            unpack_seq<D, BITS>(reinterpret_cast<const uint32_t*>(Ly.vcodes + (grp * D + c) * (4 * BITS)), dst, 0);
         }
     }
     __syncthreads();
@@ -175,7 +204,7 @@ decompress_kernel(const __grid_constant__ DecBatch b, int ctx_pad, Codebook cb) 
     }
 }
 
-template <int D, int BITS>
+template <int D, int BITS, bool MIX>
 cudaError_t run(const Shape& s, const DecBatch& b, cudaStream_t st) {
     constexpr int VPB = kDecThreads / (D / 32);
     int gx = 0;
@@ -186,15 +215,24 @@ cudaError_t run(const Shape& s, const DecBatch& b, cudaStream_t st) {
         gx = std::max(gx, nbv + nbk);
     }
     if (gx == 0) return cudaSuccess;
-    decompress_kernel<D, BITS><<<dim3(gx, s.kv_heads, b.n), kDecThreads, 0, st>>>(b, s.ctx_pad, codebook(BITS));
+    CenTable ct = {};
+    if (MIX) {
+        for (int w = 2; w <= 4; ++w)
+            for (int k = 0; k < (1 << w); ++k) ct.c[mix_base(w) + k] = codebook(w).c[k];
+    } else {
+        for (int k = 0; k < (1 << BITS); ++k) ct.c[k] = codebook(BITS).c[k];
+    }
+    decompress_kernel<D, BITS, MIX><<<dim3(gx, s.kv_heads, b.n), kDecThreads, 0, st>>>(b, s.ctx_pad, ct);
     return cudaGetLastError();
 }
 
+// bits 0: layers of per-group widths
 template <int D>
 cudaError_t run_bits(int bits, const Shape& s, const DecBatch& b, cudaStream_t st) {
-    if (bits == 2) return run<D, 2>(s, b, st);
-    if (bits == 3) return run<D, 3>(s, b, st);
-    return run<D, 4>(s, b, st);
+    if (bits == 0) return run<D, 4, true>(s, b, st);
+    if (bits == 2) return run<D, 2, false>(s, b, st);
+    if (bits == 3) return run<D, 3, false>(s, b, st);
+    return run<D, 4, false>(s, b, st);
 }
 
 }  // namespace
@@ -203,16 +241,20 @@ cudaError_t launch_decompress_layers(const Shape& s, const LayerBufs* L, const i
                                      void* const* V_out, int n, cudaStream_t st) {
     for (int c0 = 0; c0 < n; c0 += kEncBatch) {
         const int nc = std::min(kEncBatch, n - c0);
-        for (int bits = 2; bits <= 4; ++bits) {  // one launch per V width
+        for (int bits = 0; bits <= 4; ++bits) {  // one launch per V width (0: per-group widths)
+            if (bits == 1) continue;
             DecBatch b = {};
             for (int i = c0; i < c0 + nc; ++i) {
-                if (L[i].bits != bits) continue;
+                if ((L[i].mixed ? 0 : L[i].bits) != bits) continue;
                 DecLayer& d = b.L[b.n++];
                 d.kq = L[i].kq;
                 d.kscale = L[i].kscale;
                 d.kscales = L[i].kscales;
                 d.vcodes = L[i].vcodes;
                 d.vnorm = L[i].vnorm;
+                d.gbits = L[i].gbits;
+                d.goff = L[i].goff;
+                d.vhead = L[i].vhead;
                 d.Kout = K_out ? static_cast<uint4*>(K_out[i]) : nullptr;
                 d.Vout = V_out ? static_cast<uint4*>(V_out[i]) : nullptr;
                 d.len = len[i];

@@ -383,10 +383,20 @@ encode_kernel(const __grid_constant__ EncBatchT<NB> b, int ctx, int ctx_pad, int
                 words[w] |= code << off;
                 if (off + BITS > 32) words[w + 1] |= code >> (32 - off);
             }
-            const long long grp = ((long long)h * ctx_pad + t_base + t0) / 32 + gq;
-            uint32_t* out = reinterpret_cast<uint32_t*>(Ly.vcodes + (grp * D + c) * (4 * BITS));
+            // only groups holding tokens of this encode: a group past its end
+            // belongs to a later append (or lies past the head's codes)
+            const int gl = t0 / 32 + gq;  // group within the encode
+            if (gl * 32 < ctx) {
+                uint32_t* out = reinterpret_cast<uint32_t*>(Ly.vcodes + h * Ly.vhead + Ly.voff +
+                                                            ((long long)gl * D + c) * (4 * BITS));
 #pragma unroll
-            for (int w = 0; w < BITS; ++w) out[w] = words[w];
+                for (int w = 0; w < BITS; ++w) out[w] = words[w];
+                if (Ly.gbits && h == 0 && c == 0) {  // the group's width and offset, once per layer
+                    const int g = t_base / 32 + gl;
+                    Ly.gbits[g] = (uint8_t)BITS;
+                    Ly.goff[g] = (uint32_t)(Ly.voff + (long long)gl * D * 4 * BITS);
+                }
+            }
         }
 
     }
@@ -519,8 +529,12 @@ cudaError_t run_bits(int bits, const Shape& s, const EncBatchT<NB>& b, int* stat
     return run_encode<D, 4, NB>(s, b, status, sm_count, t_base, kb, nparts, st);
 }
 
-EncLayer enc_layer(const LayerBufs& L, const void* K, const void* V) {
+EncLayer enc_layer(const LayerBufs& L, const void* K, const void* V, long long voff) {
     EncLayer e;
+    e.vhead = L.vhead;
+    e.voff = voff;
+    e.gbits = L.gbits;
+    e.goff = L.goff;
     e.K = static_cast<const uint16_t*>(K);
     e.V = static_cast<const uint16_t*>(V);
     e.kq = L.kq;
@@ -561,13 +575,13 @@ namespace {
 // max|K| and encode launches for nc layers of a table of capacity NB
 template <int NB>
 cudaError_t launch_chunk(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V, int nc,
-                         int* status, int sm_count, int t_base, cudaStream_t st) {
+                         int* status, int sm_count, int t_base, long long voff, cudaStream_t st) {
     const bool kb = L[0].kscales != nullptr;
     // max|K| of every layer in one launch: about two CTAs per SM in all, so
     // that they are all running when the encode kernel starts
     EncBatchT<NB> all = {};
     all.n = nc;
-    for (int i = 0; i < nc; ++i) all.L[i] = enc_layer(L[i], K[i], V[i]);
+    for (int i = 0; i < nc; ++i) all.L[i] = enc_layer(L[i], K[i], V[i], voff);
     const long long nchunk = (long long)s.kv_heads * s.ctx * (s.head_dim / 8);
     const int gx = kb ? 1 : std::max(1, std::min(kKmaxInv, (2 * sm_count + nc - 1) / nc));
     const long long per_cta = (nchunk + gx - 1) / gx;
@@ -590,22 +604,26 @@ cudaError_t launch_chunk(const Shape& s, const LayerBufs* L, const void* const* 
 }  // namespace
 
 cudaError_t launch_encode_layers(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V,
-                                 int n, int* status, int sm_count, int t_base, cudaStream_t st) {
+                                 int n, int* status, int sm_count, int t_base, long long voff,
+                                 cudaStream_t st) {
     if (n < 1) return cudaErrorInvalidValue;
     const bool kb = L[0].kscales != nullptr;
-    if (t_base != 0 && (!kb || n != 1 || t_base % 32 != 0)) return cudaErrorInvalidValue;
-    if (n == 1) return launch_chunk<1>(s, L, K, V, 1, status, sm_count, t_base, st);
+    if ((t_base != 0 || voff != 0) && (!kb || n != 1 || t_base % 32 != 0)) return cudaErrorInvalidValue;
+    for (int i = 0; i < n; ++i)
+        if (L[i].vhead <= 0) return cudaErrorInvalidValue;
+    if (n == 1) return launch_chunk<1>(s, L, K, V, 1, status, sm_count, t_base, voff, st);
     for (int c0 = 0; c0 < n; c0 += kEncBatch) {
         const int nc = std::min(kEncBatch, n - c0);
-        const cudaError_t e = launch_chunk<kEncBatch>(s, L + c0, K + c0, V + c0, nc, status, sm_count, t_base, st);
+        const cudaError_t e =
+            launch_chunk<kEncBatch>(s, L + c0, K + c0, V + c0, nc, status, sm_count, t_base, voff, st);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
 
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, int sm_count, int t_base, cudaStream_t st) {
-    return launch_encode_layers(s, &L, &K, &V, 1, status, sm_count, t_base, st);
+                          int* status, int sm_count, int t_base, long long voff, cudaStream_t st) {
+    return launch_encode_layers(s, &L, &K, &V, 1, status, sm_count, t_base, voff, st);
 }
 
 }  // namespace kvp

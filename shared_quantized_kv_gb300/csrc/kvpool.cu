@@ -88,16 +88,16 @@ double half_value(uint16_t h) {
 }
 
 // Scale lam in [1, 2) minimising the largest relative fp16 rounding error of
-// lam * c over the positive centroids (the table is antisymmetric).
-float pick_lambda(const double* c, int L) {
+// lam * c over the n positive centroids pos (the tables are antisymmetric).
+float pick_lambda(const double* pos, int n) {
     double best = 1e30;
     float best_lam = 1.0f;
     for (int i = 0; i < (1 << 20); ++i) {
         const float lam = 1.0f + (float)i / (float)(1 << 20);
         double worst = 0.0;
-        for (int k = L / 2; k < L; ++k) {
-            const double v = (double)(float)((double)lam * c[k]);
-            const double e = fabs(half_value(half_bits((float)v)) - (double)lam * c[k]) / ((double)lam * c[k]);
+        for (int k = 0; k < n; ++k) {
+            const double v = (double)(float)((double)lam * pos[k]);
+            const double e = fabs(half_value(half_bits((float)v)) - (double)lam * pos[k]) / ((double)lam * pos[k]);
             if (e > worst) worst = e;
             if (worst >= best) break;
         }
@@ -110,9 +110,13 @@ float pick_lambda(const double* c, int L) {
 }
 
 Codebook g_books[5];
+MixBook g_mix;
 std::once_flag g_books_once;
 
 void build_books() {
+    double allpos[14];  // positive centroids of the three widths
+    int npos = 0;
+    double cen[5][16];
     for (int bits = 2; bits <= 4; ++bits) {
         Codebook& b = g_books[bits];
         const int L = 1 << bits, K = L / 2;
@@ -127,10 +131,17 @@ void build_books() {
         for (int k = 0; k < 16; ++k) b.m[k] = (k < L - 1) ? (float)(0.5 * (c[k] + c[k + 1])) : 0.0f;
         b.levels = L;
         b.bits = bits;
-        b.lam = pick_lambda(c, L);
+        b.lam = pick_lambda(c + K, K);
         for (int k = 0; k < 16; ++k)
             b.c16[k] = (k < L) ? half_bits((float)((double)b.lam * c[k])) : (uint16_t)0;
+        for (int k = 0; k < 16; ++k) cen[bits][k] = k < L ? c[k] : 0.0;
+        for (int k = 0; k < K; ++k) allpos[npos++] = c[K + k];
     }
+    g_mix.lam = pick_lambda(allpos, npos);
+    for (int bits = 2; bits <= 4; ++bits)
+        for (int k = 0; k < 16; ++k)
+            g_mix.c16[bits - 2][k] =
+                k < (1 << bits) ? half_bits((float)((double)g_mix.lam * cen[bits][k])) : (uint16_t)0;
 }
 
 }  // namespace
@@ -138,6 +149,11 @@ void build_books() {
 const Codebook& codebook(int bits) {
     std::call_once(g_books_once, build_books);
     return g_books[bits];
+}
+
+const MixBook& mixbook() {
+    std::call_once(g_books_once, build_books);
+    return g_mix;
 }
 
 // Mean squared error of the Lloyd-Max quantiser for N(0,1) at `bits` bits,
@@ -167,8 +183,12 @@ struct kvpool {
     int layers = 0, kv_heads = 0, head_dim = 0, ctx = 0, ctx_pad = 0, max_rows = 0;
     int device = 0, sm_count = 0;
     int k_block = 0;  // 0: one K scale per layer; 32: one per 32 elements
-    std::vector<int> bits;
-    std::vector<size_t> off_kq, off_vc, off_vn, off_ks;
+    std::vector<int> bits;  // per layer: the width fixed at create (the largest a group may take)
+    std::vector<size_t> off_kq, off_vc, off_vn, off_ks, off_gt;
+    // block-scaled pools: the width of every written 32-token group of a layer
+    // (its device copy, with the groups' byte offsets, is written by the
+    // encode kernel)
+    std::vector<std::vector<uint8_t>> gw;
     std::vector<unsigned char> compressed;
     std::vector<int> len;  // tokens the layer holds: ctx once compressed; grows by appends
     // Per stream: the layer that this pool's most recent launch on it wrote,
@@ -201,12 +221,35 @@ struct kvpool {
     kvp::Shape shape() const { return {kv_heads, head_dim, ctx, ctx_pad}; }
     // the layer's current tokens (attend, decompress, export read [0, len))
     kvp::Shape shape_of(int l) const { return {kv_heads, head_dim, len[l], ctx_pad}; }
-    kvp::LayerBufs layer(int l) const {
-        return {reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
-                reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
-                kabsmax + 2 * l + 1, &kmaps[l], kpart + (size_t)l * kvp::kKmaxParts,
-                k_block ? reinterpret_cast<float*>(base + off_ks[l]) : nullptr};
+    int groups() const { return ctx_pad / 32; }
+    // 1 when the layer's written groups do not all have its create width
+    int mixed(int l) const {
+        for (uint8_t b : gw[l])
+            if (b != bits[l]) return 1;
+        return 0;
     }
+    // byte offset within a KV head's codes of the layer's group g (g <= groups written)
+    long long group_offset(int l, int g) const {
+        long long o = 0;
+        for (int i = 0; i < g; ++i) o += (long long)head_dim * 4 * gw[l][i];
+        return o;
+    }
+    kvp::LayerBufs layer(int l) const {
+        kvp::LayerBufs L{reinterpret_cast<int8_t*>(base + off_kq[l]), base + off_vc[l],
+                         reinterpret_cast<float*>(base + off_vn[l]), kscale + l, kabsmax + 2 * l, bits[l],
+                         kabsmax + 2 * l + 1, &kmaps[l], kpart + (size_t)l * kvp::kKmaxParts,
+                         k_block ? reinterpret_cast<float*>(base + off_ks[l]) : nullptr};
+        L.vhead = (long long)ctx_pad * head_dim * bits[l] / 8;
+        if (k_block) {
+            L.gbits = base + off_gt[l];
+            L.goff = reinterpret_cast<uint32_t*>(base + off_gt[l] + align_groups());
+            L.mixed = mixed(l);
+        }
+        return L;
+    }
+    // group table of a layer: widths [groups] (u8), then offsets [groups] (u32)
+    size_t align_groups() const { return ((size_t)groups() + 255) & ~size_t(255); }
+    size_t group_table_bytes() const { return align_groups() + (size_t)groups() * 4; }
 };
 
 namespace {
@@ -318,6 +361,7 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
     p->bits.resize(layers);
     p->compressed.assign(layers, 0);
     p->len.assign(layers, 0);
+    p->gw.resize(layers);
     size_t off = 0;
     const size_t nvec = (size_t)kv_heads * p->ctx_pad;
     for (int l = 0; l < layers; ++l) {
@@ -330,6 +374,8 @@ int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int
         off = align256(off + nvec * 4);
         p->off_ks.push_back(off);
         if (k_block) off = align256(off + nvec * (head_dim / k_block) * 4);
+        p->off_gt.push_back(off);
+        if (k_block) off = align256(off + p->group_table_bytes());
     }
     const size_t off_scale = off;
     off = align256(off + 4 * (size_t)layers);
@@ -381,11 +427,12 @@ int kvpool_compress(kvpool_t* p, int layer, const void* K, const void* V, void* 
     if (rc) return rc;
     if (!K || !V || !aligned16(K) || !aligned16(V)) return KVPOOL_ERR_INVALID_ARG;
     if (p->compressed[layer]) return KVPOOL_ERR_STATE;
-    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status, p->sm_count, 0,
+    cudaError_t e = kvp::launch_encode(p->shape(), p->layer(layer), K, V, p->status, p->sm_count, 0, 0,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     p->compressed[layer] = 1;
     p->len[layer] = p->ctx;
+    if (p->k_block) p->gw[layer].assign((p->ctx + 31) / 32, (uint8_t)p->bits[layer]);
     p->wrote(stream, layer);
     return KVPOOL_OK;
 }
@@ -404,12 +451,13 @@ int kvpool_compress_layers(kvpool_t* p, int n, const int* layers, const void* co
         if (p->compressed[layers[i]]) return KVPOOL_ERR_STATE;
     std::vector<kvp::LayerBufs> L(n);
     for (int i = 0; i < n; ++i) L[i] = p->layer(layers[i]);
-    cudaError_t e = kvp::launch_encode_layers(p->shape(), L.data(), K, V, n, p->status, p->sm_count, 0,
+    cudaError_t e = kvp::launch_encode_layers(p->shape(), L.data(), K, V, n, p->status, p->sm_count, 0, 0,
                                               static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     for (int i = 0; i < n; ++i) {
         p->compressed[layers[i]] = 1;
         p->len[layers[i]] = p->ctx;
+        if (p->k_block) p->gw[layers[i]].assign((p->ctx + 31) / 32, (uint8_t)p->bits[layers[i]]);
     }
     p->wrote(stream, n == 1 ? layers[0] : kvpool::kWroteMany);
     return KVPOOL_OK;
@@ -418,19 +466,40 @@ int kvpool_compress_layers(kvpool_t* p, int n, const int* layers, const void* co
 int kvpool_append(kvpool_t* p, int layer, const void* K, const void* V, int n, void* stream) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
+    return kvpool_append_bits(p, layer, K, V, n, p->bits[layer], stream);
+}
+
+int kvpool_append_bits(kvpool_t* p, int layer, const void* K, const void* V, int n, int bits, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
     if (!K || !V || !aligned16(K) || !aligned16(V) || n < 1) return KVPOOL_ERR_INVALID_ARG;
     if (!p->k_block) return KVPOOL_ERR_UNSUPPORTED;
+    if (bits < 2 || bits > p->bits[layer]) return KVPOOL_ERR_INVALID_ARG;
     const int len = p->len[layer];
     if (len % 32 != 0) return KVPOOL_ERR_STATE;  // a ragged append closed the layer
     if ((long long)len + n > p->ctx) return KVPOOL_ERR_INVALID_ARG;
     const kvp::Shape s{p->kv_heads, p->head_dim, n, p->ctx_pad};
-    cudaError_t e = kvp::launch_encode(s, p->layer(layer), K, V, p->status, p->sm_count, len,
+    kvp::LayerBufs L = p->layer(layer);
+    L.bits = bits;  // the width these tokens are coded at
+    const long long voff = p->group_offset(layer, len / 32);
+    cudaError_t e = kvp::launch_encode(s, L, K, V, p->status, p->sm_count, len, voff,
                                        static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return map_cuda(e);
     p->len[layer] = len + n;
     p->compressed[layer] = 1;
+    p->gw[layer].resize((len + n + 31) / 32, (uint8_t)bits);
     p->wrote(stream, layer);
     return KVPOOL_OK;
+}
+
+int kvpool_layer_widths(const kvpool_t* p, int layer, uint8_t* widths, int max_groups) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (max_groups < 0 || (max_groups > 0 && !widths)) return KVPOOL_ERR_INVALID_ARG;
+    const int ng = (p->len[layer] + 31) / 32;
+    for (int g = 0; g < ng && g < max_groups; ++g)
+        widths[g] = p->k_block ? p->gw[layer][g] : (uint8_t)p->bits[layer];
+    return ng;
 }
 
 int kvpool_layer_len(const kvpool_t* p, int layer) {
@@ -611,6 +680,7 @@ int kvpool_reset_layer(kvpool_t* p, int layer) {
     if (rc) return rc;
     p->compressed[layer] = 0;
     p->len[layer] = 0;
+    p->gw[layer].clear();
     return KVPOOL_OK;
 }
 
@@ -630,6 +700,9 @@ int kvpool_layer_view(const kvpool_t* p, int layer, kvpool_layer_view_t* v) {
     v->kscales = L.kscales;
     v->k_block = p->k_block;
     v->len = p->len[layer];
+    v->group_bits = L.gbits;
+    v->group_off = L.goff;
+    v->mixed = L.mixed;
     return KVPOOL_OK;
 }
 
@@ -643,8 +716,11 @@ int copy_layer(const kvpool* p, int layer, bool to_pool, void* kq, void* vc, voi
     const int T = to_pool ? p->ctx : p->len[layer];  // tokens moved
     const size_t kw = (size_t)T * p->head_dim, kp = (size_t)p->ctx_pad * p->head_dim;
     const size_t vb = (size_t)p->head_dim * L.bits / 8;
-    // V codes travel in whole 32-token groups (the pool layout)
-    const size_t vw = (size_t)((T + 31) / 32 * 32) * vb, vp = (size_t)p->ctx_pad * vb;
+    // V codes travel in whole 32-token groups (the pool layout); a layer of
+    // per-group widths moves each head's written groups back to back
+    const size_t vw = (p->k_block && !to_pool) ? (size_t)p->group_offset(layer, (T + 31) / 32)
+                                               : (size_t)((T + 31) / 32 * 32) * vb;
+    const size_t vp = (size_t)L.vhead;
     const size_t nw = (size_t)T * 4, np_ = (size_t)p->ctx_pad * 4;
     cudaError_t e = cudaSuccess;
     if (kq && e == cudaSuccess)

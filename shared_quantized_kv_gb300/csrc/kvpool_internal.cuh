@@ -31,6 +31,15 @@ struct Codebook {
 // Host: the library's own table for `bits` in {2,3,4} (derived once).
 const Codebook& codebook(int bits);
 
+// Tensor-core operand tables of the three widths under one scale lam (layers
+// whose groups have different widths: the attention kernel divides its output
+// by one lam), c16[b - 2][k] = fp16 bits of lam * c_b[k].
+struct MixBook {
+    uint16_t c16[3][16];
+    float lam;
+};
+const MixBook& mixbook();
+
 // Compress scratch of a layer: kKmaxParts words. Words [0, kKmaxInv) take the
 // max|K| kernel's partial maxima (bf16 bits of |k|, one per CTA); kKmaxInv
 // the float bits of 1/s; kKmaxCount the kernel's arrival counter (0 between
@@ -51,6 +60,17 @@ struct LayerBufs {
     const CUtensorMap* kmap;  // TMA map of kq as rows of D bytes (128 / 64-byte swizzle), or null
     uint32_t* kpart;          // [kKmaxParts] compress scratch (see kKmaxParts)
     float* kscales;           // block-scaled K: [Hk][ctx_pad][D/32], one scale per 32 elements; else null
+    // Per-group V widths (block-scaled pools, whose layers grow by appends):
+    // gbits[g] the width of 32-token group g (0: not written), goff[g] the
+    // byte offset of its codes within a KV head (null for per-tensor pools);
+    // KV head h's codes start at h * vhead (ctx_pad * D * bits / 8, bits the
+    // width fixed at create, the largest a group may take). mixed = 1 when the
+    // written groups do not all have width `bits`: attend and decompress then
+    // take the per-group path.
+    uint8_t* gbits;
+    uint32_t* goff;
+    long long vhead;
+    int mixed;
 };
 
 struct Shape {
@@ -69,6 +89,12 @@ struct EncLayer {
     uint32_t* maxima;   // {bf16 bits of max|K|, float bits of the largest V norm}
     uint32_t* kpart;    // kKmaxParts words of compress scratch
     float* kscales;     // block-scaled K, else null
+    // V codes of token group g of the encode (g = 0 at its first token) start
+    // at vcodes + h * vhead + voff + g * D * 4 * bits; block-scaled pools also
+    // record each group's width and offset in gbits / goff (else null)
+    long long vhead, voff;
+    uint8_t* gbits;
+    uint32_t* goff;
 };
 // Most layers per launch of the multi-layer kernels.
 constexpr int kEncBatch = 32;
@@ -82,14 +108,17 @@ struct EncBatchT {
 using EncBatch = EncBatchT<kEncBatch>;
 
 // s.ctx is the token count of K and V; t_base the pool token they start at
-// (non-zero only for appends to block-scaled layers, a multiple of 32).
+// (non-zero only for appends to block-scaled layers, a multiple of 32) and
+// voff the byte offset of its group within a KV head's codes; L.bits is the
+// width the tokens are coded at.
 cudaError_t launch_encode(const Shape& s, const LayerBufs& L, const void* K, const void* V,
-                          int* status, int sm_count, int t_base, cudaStream_t st);
+                          int* status, int sm_count, int t_base, long long voff, cudaStream_t st);
 // n layers (all of one pool, so one k-scaling mode) in a few launches per
 // kEncBatch of them: one max|K| kernel over all, then one encode kernel per V
-// width. t_base != 0 only with n = 1.
+// width. t_base != 0 or voff != 0 only with n = 1.
 cudaError_t launch_encode_layers(const Shape& s, const LayerBufs* L, const void* const* K, const void* const* V,
-                                 int n, int* status, int sm_count, int t_base, cudaStream_t st);
+                                 int n, int* status, int sm_count, int t_base, long long voff,
+                                 cudaStream_t st);
 
 // ---- decompress
 // One layer of a multi-layer decompress launch (kernel parameter, by value).
@@ -99,6 +128,9 @@ struct DecLayer {
     const float* kscales;  // block-scaled K, else null
     const uint8_t* vcodes;
     const float* vnorm;
+    const uint8_t* gbits;  // per-group widths (kernels of mixed layers), else unused
+    const uint32_t* goff;
+    long long vhead;       // bytes per KV head of the codes
     uint4* Kout;           // bf16 [Hk][len][D], or null
     uint4* Vout;
     int len;               // tokens the layer holds

@@ -36,7 +36,8 @@ class LayerView(ctypes.Structure):
     _fields_ = [("kq", ctypes.c_void_p), ("vcodes", ctypes.c_void_p), ("vnorm", ctypes.c_void_p),
                 ("kscale", ctypes.c_void_p), ("ctx", ctypes.c_int), ("ctx_padded", ctypes.c_int),
                 ("bits", ctypes.c_int), ("compressed", ctypes.c_int),
-                ("kscales", ctypes.c_void_p), ("k_block", ctypes.c_int), ("len", ctypes.c_int)]
+                ("kscales", ctypes.c_void_p), ("k_block", ctypes.c_int), ("len", ctypes.c_int),
+                ("group_bits", ctypes.c_void_p), ("group_off", ctypes.c_void_p), ("mixed", ctypes.c_int)]
 
 
 _LIB = None
@@ -51,6 +52,9 @@ _SIGS = {
     "kvpool_export_kscales": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "kvpool_append": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
                                      ctypes.c_int, ctypes.c_void_p]),
+    "kvpool_append_bits": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_int, ctypes.c_int, ctypes.c_void_p]),
+    "kvpool_layer_widths": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int]),
     "kvpool_layer_len": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int]),
     "kvpool_sensitivity": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                           ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_void_p,
@@ -252,14 +256,28 @@ class KVPool:
         _check(_lib().kvpool_compress_layers(self._h, n, lay, kp, vp, _stream_ptr(stream)),
                "kvpool_compress_layers")
 
-    def append(self, layer, K, V, stream=None):
+    def append(self, layer, K, V, bits=None, stream=None):
         """Append tokens to a block-scaled layer: K, V bf16 [kv_heads, n, d]
-        (device) become tokens [len, len + n) of the layer."""
+        (device) become tokens [len, len + n) of the layer, their V codes at
+        `bits` (None: the layer's width; else 2..that width)."""
         import torch
 
-        _check(_lib().kvpool_append(self._h, layer, _dev_ptr(K, torch.bfloat16, "K"),
-                                    _dev_ptr(V, torch.bfloat16, "V"), int(K.shape[1]),
-                                    _stream_ptr(stream)), "kvpool_append")
+        kp, vp = _dev_ptr(K, torch.bfloat16, "K"), _dev_ptr(V, torch.bfloat16, "V")
+        if bits is None:
+            _check(_lib().kvpool_append(self._h, layer, kp, vp, int(K.shape[1]), _stream_ptr(stream)),
+                   "kvpool_append")
+        else:
+            _check(_lib().kvpool_append_bits(self._h, layer, kp, vp, int(K.shape[1]), int(bits),
+                                             _stream_ptr(stream)), "kvpool_append_bits")
+
+    def layer_widths(self, layer):
+        """V width of every 32-token group the layer holds (list of int)."""
+        n = int(_lib().kvpool_layer_widths(self._h, layer, None, 0))
+        if n < 0:
+            raise KVPoolError(n, "kvpool_layer_widths")
+        buf = (ctypes.c_uint8 * max(n, 1))()
+        _check(min(0, _lib().kvpool_layer_widths(self._h, layer, buf, n)), "kvpool_layer_widths")
+        return [int(b) for b in buf[:n]]
 
     def layer_len(self, layer) -> int:
         """Tokens the layer holds (ctx once compressed)."""
@@ -366,15 +384,19 @@ class KVPool:
     def export_layer(self, layer, stream=None):
         """The layer's stored bytes as device tensors (token padding removed):
         kq int8 [Hk, ctx, d], vcodes uint8 [Hk, ceil(ctx/32), d, 4*bits] (per
-        32-token group, one packed code sequence per coordinate), vnorm float32
-        [Hk, ctx], kscale float32 [1]."""
+        32-token group, one packed code sequence per coordinate; a layer of
+        per-group widths: [Hk, sum_g d*4*b_g], its groups back to back),
+        vnorm float32 [Hk, ctx], kscale float32 [1]."""
         import torch
 
         bits = self.bits[layer]
         dev = torch.device("cuda", torch.cuda.current_device())
         Hk, T, d = self.kv_heads, self.layer_len(layer), self.head_dim
         kq = torch.empty((Hk, T, d), dtype=torch.int8, device=dev)
-        vc = torch.empty((Hk, (T + 31) // 32, d, 4 * bits), dtype=torch.uint8, device=dev)
+        if self.layer_view(layer).mixed:
+            vc = torch.empty((Hk, d * 4 * sum(self.layer_widths(layer))), dtype=torch.uint8, device=dev)
+        else:
+            vc = torch.empty((Hk, (T + 31) // 32, d, 4 * bits), dtype=torch.uint8, device=dev)
         vn = torch.empty((Hk, T), dtype=torch.float32, device=dev)
         ks = torch.empty(1, dtype=torch.float32, device=dev)
         _check(_lib().kvpool_export_layer(self._h, layer, kq.data_ptr(), vc.data_ptr(),

@@ -78,5 +78,7 @@ def test_null_pool_calls(kp):
     assert lib.kvpool_compress_layers(None, 2, lay, ptrs, ptrs, None) == -1
     assert lib.kvpool_decompress_layers(None, 2, lay, ptrs, ptrs, None) == -1
     assert lib.kvpool_append(None, 0, None, None, 1, None) == -1
+    assert lib.kvpool_append_bits(None, 0, None, None, 1, 3, None) == -1
+    assert lib.kvpool_layer_widths(None, 0, None, 0) == -1
     assert lib.kvpool_layer_len(None, 0) == -1
     lib.kvpool_destroy(None)

@@ -42,6 +42,10 @@ def _check_prefix(pool, K, V, Q, T, bits):
     (128, (256, 640, 690), 3),       # 32-token items; a ragged last append
     (64, (32, 128, 160, 333), 2),    # 64-token items starting at odd group offsets
     (128, (96, 1000), 4),
+    # d 64 encodes 64 tokens per item: an append in the last 32-token group of
+    # the padded token axis (96 of 128) must not write the item's second group,
+    # which lies past the KV head's codes
+    (64, (96, 100), 3),
 ])
 def test_appends_equal_one_encode(kp, d, cuts, bits):
     ctx = cuts[-1] + 24  # capacity above the last length
