@@ -258,6 +258,28 @@ int kvpool_compress_layers(kvpool_t* pool, int n, const int* layers, const void*
 int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_heads,
                   const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream);
 
+/* kvpool_attend through a caller-provided workspace (device memory of at
+ * least kvpool_attend_ws_bytes(pool, agents, q_heads) bytes, 16-byte
+ * aligned; its contents need no initialisation and are scratch afterwards):
+ * the context is cut into more slices than kvpool_attend's clusters can hold
+ * (one CTA each, enough to fill every SM once), their partial states (the
+ * kvpool_attend_partial quantities) go to the workspace, and a second kernel
+ * merges them with the agents' tails exactly as kvpool_merge_partials. Same
+ * arguments, result and errors as kvpool_attend, plus
+ * KVPOOL_ERR_INVALID_ARG for a missing, misaligned or short workspace and
+ * KVPOOL_ERR_UNSUPPORTED when the (KV head, row group) pairs alone exceed
+ * one wave of CTAs. Calls that overlap on the GPU must not share a
+ * workspace. Source: the PolyKV summary's attention over the shared pool
+ * (section 2.A), split over the context with the log-sum-exp merge of
+ * softmax partial sums. */
+int kvpool_attend_ws(kvpool_t* pool, int layer, const void* Q, int agents, int q_heads,
+                     const kvpool_tail_t* tail, float* out, float softmax_scale, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace kvpool_attend_ws needs for `agents` agents with q_heads
+ * query heads over any layer of the pool (0 for invalid arguments). */
+size_t kvpool_attend_ws_bytes(const kvpool_t* pool, int agents, int q_heads);
+
 /* Context split (one pool's context over several calls, ranks or GPUs):
  * the attention state of every (agent, query head) row over the pool tokens
  * [t_begin, t_end) of a compressed layer, instead of the finished output.

@@ -19,8 +19,9 @@
 //     row for its split.
 //   attend_combine: one CTA per (row, kv head): log-sum-exp merge of the
 //     splits, inverse FWHT / d, the agent's tail tokens, final normalisation.
-//     The same kernel merges the context slices of kvpool_attend_partial
-//     (kvpool_merge_partials), with the partials laid out by slice.
+//   merge_rows: the same merge with one warp per (row, kv head), for the
+//     context slices of kvpool_attend_partial (kvpool_merge_partials) and of
+//     kvpool_attend_ws, the partials laid out by slice.
 #include <cuda_bf16.h>
 #include <math_constants.h>
 
@@ -232,6 +233,128 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
     out[((long long)a * Hq + h) * D + i] = (Opool * wp + Ot * wt) / (L * wp + lt * wt);
 }
 
+// kvpool_merge_partials and the merge of kvpool_attend_ws: one warp per
+// (row, KV head), lane = D/32 consecutive channels. The slices' (m, l) are
+// read by the lanes at once, their accumulators four slices at a time; one
+// inverse FWHT per row in registers and shuffles; then the agent's tail
+// tokens (online softmax) and the final normalisation. Launched as a
+// programmatic dependent of the kernel that wrote the partials.
+template <int D>
+__global__ void __launch_bounds__(256)
+merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml, int nsplit, int R,
+                  int Hk, int Hq, int G, const uint16_t* __restrict__ Q, const uint16_t* __restrict__ tK,
+                  const uint16_t* __restrict__ tV, const int32_t* __restrict__ tlen, int tail_max,
+                  float scale_log2, float* __restrict__ out) {
+    constexpr int EPL = D / 32;
+    const unsigned full = 0xffffffffu;
+    const int lane = threadIdx.x % 32;
+    const int r = blockIdx.x * 8 + threadIdx.x / 32, g = blockIdx.y;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (r >= R) return;
+    const long long stride = (long long)Hk * R;  // between slices
+    const long long b0 = (long long)g * R + r;
+    float M = -CUDART_INF_F;
+    for (int s = lane; s < nsplit; s += 32) {
+        const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + s * stride));
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+    }
+    M = warp_max(M);
+    float L = 0.f;
+    float acc[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
+    for (int s0 = 0; s0 < nsplit; s0 += 32) {
+        float w = 0.f;
+        if (s0 + lane < nsplit) {
+            const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + (s0 + lane) * stride));
+            if (ml.y > 0.f) {
+                w = exp2f(ml.x - M);
+                L += w * ml.y;
+            }
+        }
+        const int n = min(32, nsplit - s0);
+        for (int k = 0; k < n; k += 4) {
+            float ww[4], v[4][EPL];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                ww[u] = __shfl_sync(full, w, (k + u) & 31);
+                if (k + u >= n) ww[u] = 0.f;
+                const float* src = part_acc + (b0 + (long long)(s0 + k + u) * stride) * D + lane * EPL;
+                if (ww[u] != 0.f) {  // the same for every lane
+                    if constexpr (EPL == 4) {
+                        const float4 x = *reinterpret_cast<const float4*>(src);
+                        v[u][0] = x.x, v[u][1] = x.y, v[u][2] = x.z, v[u][3] = x.w;
+                    } else {
+                        const float2 x = *reinterpret_cast<const float2*>(src);
+                        v[u][0] = x.x, v[u][1] = x.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ww[u], v[u][e], acc[e]);
+        }
+    }
+    L = warp_sum(L);
+    // inverse rotation H acc / D: channel lane * EPL + e
+#pragma unroll
+    for (int h = 1; h < EPL; h <<= 1) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            if (!(e & h)) {
+                const float u = acc[e], v = acc[e + h];
+                acc[e] = u + v;
+                acc[e + h] = u - v;
+            }
+        }
+    }
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const bool upper = (lane & o2) != 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const float other = __shfl_xor_sync(full, acc[e], o2);
+            acc[e] = upper ? other - acc[e] : acc[e] + other;
+        }
+    }
+    const int a = r / G, h = g * G + r % G;
+    float mt = -CUDART_INF_F, lt = 0.f, ot[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ot[e] = 0.f;
+    if (tK != nullptr) {
+        const int n = min(max(tlen[a], 0), tail_max);  // never read past the tail buffers
+        float q[EPL];
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) q[e] = bf2f(Q[((long long)a * Hq + h) * D + lane * EPL + e]);
+        const long long tb = ((long long)a * Hk + g) * tail_max;
+        for (int t = 0; t < n; ++t) {
+            float dot = 0.f;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) dot = fmaf(q[e], bf2f(tK[(tb + t) * D + lane * EPL + e]), dot);
+            dot = warp_sum(dot);
+            const float lg = __fmul_rn(dot, scale_log2);
+            const float mnew = fmaxf(mt, lg);
+            const float corr = exp2f(mt - mnew), p = exp2f(lg - mnew);
+            lt = lt * corr + p;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) ot[e] = ot[e] * corr + p * bf2f(tV[(tb + t) * D + lane * EPL + e]);
+            mt = mnew;
+        }
+    }
+    const float Mf = fmaxf(M, mt);
+    const float wp = (L > 0.f) ? exp2f(M - Mf) : 0.f;
+    const float wt = (lt > 0.f) ? exp2f(mt - Mf) : 0.f;
+    const float den = L * wp + lt * wt;
+    float* orow = out + ((long long)a * Hq + h) * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) orow[e] = (acc[e] * (1.0f / (float)D) * wp + ot[e] * wt) / den;
+}
+
 template <int D, int BITS>
 cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const AttendScratch& scr,
                 cudaStream_t st) {
@@ -257,18 +380,19 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
 
 cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
                                   int head_dim, const AttendArgs& a, cudaStream_t st) {
-    const long long R = a.rows;
-    if (head_dim == 64)
-        attend_combine_kernel<64><<<dim3(a.rows, kv_heads), 64, 0, st>>>(
-            part_acc, part_ml, parts, R, (long long)kv_heads * R, kv_heads, a.q_heads, a.group,
-            (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len, a.tail_max,
-            a.scale_log2, a.out);
-    else
-        attend_combine_kernel<128><<<dim3(a.rows, kv_heads), 128, 0, st>>>(
-            part_acc, part_ml, parts, R, (long long)kv_heads * R, kv_heads, a.q_heads, a.group,
-            (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len, a.tail_max,
-            a.scale_log2, a.out);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((a.rows + 7) / 8, kv_heads, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    auto kern = head_dim == 64 ? merge_rows_kernel<64> : merge_rows_kernel<128>;
+    return cudaLaunchKernelEx(&cfg, kern, part_acc, part_ml, parts, a.rows, kv_heads, a.q_heads, a.group,
+                              (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len,
+                              a.tail_max, a.scale_log2, a.out);
 }
 
 cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const AttendArgs& a,

@@ -103,8 +103,11 @@ struct Params {
     int* status;
     uint32_t tlo[4], thi[4];  // low / high bytes of fp16 lam * c[k], entry k in byte k % 4 of word k / 4
     float inv_lam;
-    float* part_ml;   // partial mode ([Hk][R][2] and [Hk][R][D]), else null
+    float* part_ml;   // partial mode ([nslice][Hk][R][2] and [nslice][Hk][R][D]), else null
     float* part_acc;
+    int rgn;          // row groups per KV head
+    int nslice;       // context slices per (KV head, row group): blockIdx.z = row group + rgn * slice;
+                      // slice s of a cluster of S CTAs covers tokens t0 + (s S + rank) tps ...
     const float* kscales;  // block-scaled K: [Hk][ctx_pad][D/32] (instances with KB), else unused
     // per-group V widths (instances with MIX): the width of each 32-token
     // group, its byte offset within a KV head's codes, the bytes per KV head,
@@ -425,10 +428,10 @@ __device__ __forceinline__ int nref_log2(const uint32_t* vnmax) {
 // and its accumulator in the rotated domain, in the units where the output is
 // H acc / (D L)
 template <int D>
-__device__ __forceinline__ void write_partial(const Params& p, int g, int row, int lane, float M, float L,
-                                              const float (&acc)[D / 32], float scale) {
+__device__ __forceinline__ void write_partial(const Params& p, int slice, int g, int row, int lane, float M,
+                                              float L, const float (&acc)[D / 32], float scale) {
     constexpr int EPL = D / 32;
-    const size_t base = (size_t)g * p.R + row;
+    const size_t base = ((size_t)slice * p.Hk + g) * p.R + row;
     float* dst = p.part_acc + base * D + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) dst[e] = acc[e] * scale;
@@ -527,10 +530,11 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     float* sO = reinterpret_cast<float*>(sm);      // epilogue: staging rows [128][ROWF]
 
     const int g = blockIdx.y;
-    const int row0 = blockIdx.z * p.RW;
+    const int slice = (int)blockIdx.z / p.rgn;
+    const int row0 = ((int)blockIdx.z - slice * p.rgn) * p.RW;
     const int nrows = min(p.RW, p.R - row0);  // a multiple of G
     const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
-    const int t_begin = p.t0 + crank * p.tps;
+    const int t_begin = p.t0 + (slice * S + crank) * p.tps;
     const int t_end = min(p.ctx, t_begin + p.tps);
     const int ntile = (t_end - t_begin + kTile - 1) / kTile;  // >= 1
     const long long head_tok = (long long)g * p.ctx_pad;
@@ -1099,6 +1103,27 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     }
     if (bad) atomicOr(p.status, kStTimeout);
 
+    // one CTA per context slice (workspace mode): the staged rows are the
+    // slice's partial states, written without a cluster merge
+    if (S == 1 && p.part_acc != nullptr) {
+        ptx::tc_fence_before();  // the tensor-memory reads of O come before its release
+        __syncthreads();
+        const float oscale = ldexpf(1.0f, *sNref) / (float)D * p.inv_lam;
+        for (int rr = warp; rr < nrows; rr += kThreads / 32) {
+            const float* src = sO + rr * ROWF;
+            const float m = src[D], l = src[D + 1];
+            float acc[EPL];
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) acc[e] = l > 0.f ? src[lane * EPL + e] : 0.f;
+            write_partial<D>(p, slice, g, row0 + rr, lane, l > 0.f ? m : -CUDART_INF_F, l, acc, oscale * (float)D);
+        }
+        if (warp == kWarpMma) {
+            ptx::tc_fence_after();
+            ptx::tmem_dealloc(tmem, kCols);
+        }
+        return;
+    }
+
     // this CTA is done with its stages (and has read O out of tensor memory):
     // other CTAs may write merge slots here once every CTA of the cluster has
     // arrived
@@ -1164,7 +1189,7 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 }
             }
             if (p.part_acc != nullptr) {  // partial mode: the slice's state, no rotation, no tail
-                write_partial<D>(p, g, row0 + rr, lane, M, L, acc, oscale * (float)D);
+                write_partial<D>(p, slice, g, row0 + rr, lane, M, L, acc, oscale * (float)D);
                 continue;
             }
             // inverse rotation H acc; lane holds EPL consecutive channels
@@ -1257,8 +1282,13 @@ int max_clusters(int S, size_t smem) {
     return n;
 }
 
+// ws_ctas > 0: workspace mode (partial results of many context slices, one
+// CTA each, at most ws_ctas CTAs in all); *nslice gets the slices per
+// (KV head, row group). ws_ctas = 0: clusters merge the whole slice
+// [t0, ctx) in distributed shared memory.
 template <int D, int BITS, bool TAIL, bool SPREAD, bool KB, bool MIX>
-cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, int RGN, cudaStream_t st) {
+cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, int RGN, int ws_ctas,
+                       int nslice_max, int* nslice, cudaStream_t st) {
     configure<D, BITS, TAIL, SPREAD, KB, MIX>();
     constexpr uint32_t kMaxSmem = 227 * 1024;
     const int rows_cta = std::min(prm.RW, prm.R);
@@ -1268,6 +1298,40 @@ cudaError_t launch_cfg(const CUtensorMap& kmap, Params prm, int ntiles, int Hk, 
     int max_nr = 3;
     while (max_nr > 1 && make_layout(D, BITS, max_nr, KB).total + 1024 > kMaxSmem) --max_nr;
     if (make_layout(D, BITS, max_nr, KB).total + 1024 > kMaxSmem) return cudaErrorInvalidConfiguration;
+    prm.rgn = RGN;
+    prm.nslice = 1;
+    if (ws_ctas > 0) {
+        // tiles per CTA: the fewest for which every slice fits in one wave
+        const long long jobs = (long long)Hk * RGN;
+        if (jobs > ws_ctas) return cudaErrorInvalidValue;
+        if (nslice_max < 1) return cudaErrorInvalidValue;
+        int per = (int)std::max(1LL, (jobs * ntiles + ws_ctas - 1) / ws_ctas);
+        while (jobs * ((ntiles + per - 1) / per) > ws_ctas || (ntiles + per - 1) / per > nslice_max) ++per;
+        prm.nslice = (ntiles + per - 1) / per;
+        prm.tps = per * kTile;
+        prm.own = agents_cta * prm.G;
+        prm.nraw = std::min(max_nr, per);
+        const Layout lay = make_layout(D, BITS, prm.nraw, KB);
+        if (staging_bytes(D, kM) + (size_t)prm.own * (D + 4) * 4 > lay.misc) return cudaErrorInvalidConfiguration;
+        if (max_clusters<D, BITS, TAIL, SPREAD, KB, MIX>(1, lay.total + 1024) < 1)
+            return cudaErrorInvalidConfiguration;
+        *nslice = prm.nslice;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, Hk, RGN * prm.nslice);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = lay.total + 1024;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        return cudaLaunchKernelEx(&cfg, attend_rows_kernel<D, BITS, TAIL, SPREAD, KB, MIX>, kmap, prm);
+    }
     // cluster size: fewest (waves x tiles per CTA), then the larger cluster;
     // the staging rows and the merge slots must fit in the stage area
     int bestS = 0;
@@ -1377,7 +1441,8 @@ cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const At
     const bool tail = prm.tK != nullptr;
     const bool kb = L.kscales != nullptr;
 #define KVP_ROWS_LAUNCH(DD, TT, SS, KK) \
-    launch_cfg<DD, BITS, TT, SS, KK, MIX>(km, prm, ntiles, s.kv_heads, RGN, st)
+    launch_cfg<DD, BITS, TT, SS, KK, MIX>(km, prm, ntiles, s.kv_heads, RGN, a.ws_ctas, a.ws_nslice_max, \
+                                          a.ws_nslice, st)
 // (MIX instances are block-scaled only: their second branch is the first)
 #define KVP_ROWS_KB(DD, TT, SS) (kb ? KVP_ROWS_LAUNCH(DD, TT, SS, true) : KVP_ROWS_LAUNCH(DD, TT, SS, MIX))
     if (D == 64) {

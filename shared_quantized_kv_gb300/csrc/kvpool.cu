@@ -508,8 +508,11 @@ int kvpool_layer_len(const kvpool_t* p, int layer) {
     return p->len[layer];
 }
 
-int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads,
-                  const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream) {
+namespace {
+
+// Validation shared by the attend calls: fills a (no slice, no partial mode).
+int attend_args(kvpool_t* p, int layer, const void* Q, int agents, int q_heads, const kvpool_tail_t* tail,
+                float* out, float softmax_scale, void* stream, kvp::AttendArgs& a) {
     int rc = check_layer(p, layer);
     if (rc) return rc;
     if (!Q || !out || agents < 1 || q_heads < p->kv_heads || q_heads % p->kv_heads)
@@ -524,7 +527,7 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
                                     (reinterpret_cast<uintptr_t>(tail->len) & 3)))
         return KVPOOL_ERR_INVALID_ARG;
     if (!p->compressed[layer]) return KVPOOL_ERR_STATE;
-    kvp::AttendArgs a{};
+    a = kvp::AttendArgs{};
     a.Q = Q;
     a.agents = agents;
     a.q_heads = q_heads;
@@ -541,8 +544,78 @@ int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads
     a.early = p->may_read_early(stream, layer) ? 1 : 0;
     a.t0 = 0;
     a.t1 = p->len[layer];
+    return KVPOOL_OK;
+}
+
+// Workspace of kvpool_attend_ws for rows query rows per KV head: the most
+// slices per (KV head, row group) one wave of CTAs can hold, and the byte
+// offset of the accumulators (after the (m, l) pairs).
+struct WsLayout {
+    long long nslice_max;
+    size_t acc_off, bytes;
+};
+WsLayout ws_layout(const kvpool* p, long long rows, int group) {
+    // row groups as the tensor-core launcher forms them (at most 64 rows in
+    // all: groups of <= 64 rows; else <= 128), whole agents each
+    const bool spread = rows <= 64;
+    const long long RW = ((spread ? 64 : 128) / group) * group;
+    WsLayout w{0, 0, 0};
+    if (RW < 1) return w;
+    const long long jobs = (long long)p->kv_heads * ((rows + RW - 1) / RW);
+    const long long ntiles = (p->ctx + kvp::kTokenPad - 1) / kvp::kTokenPad;
+    w.nslice_max = std::min(ntiles, (long long)p->sm_count / jobs);
+    if (w.nslice_max < 1) return w;
+    const size_t per = (size_t)p->kv_heads * rows;  // partial rows per slice
+    w.acc_off = align256((size_t)w.nslice_max * per * 2 * sizeof(float));
+    w.bytes = w.acc_off + (size_t)w.nslice_max * per * p->head_dim * sizeof(float);
+    return w;
+}
+
+}  // namespace
+
+int kvpool_attend(kvpool_t* p, int layer, const void* Q, int agents, int q_heads,
+                  const kvpool_tail_t* tail, float* out, float softmax_scale, void* stream) {
+    kvp::AttendArgs a;
+    const int rc = attend_args(p, layer, Q, agents, q_heads, tail, out, softmax_scale, stream, a);
+    if (rc) return rc;
     const cudaError_t e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), a, p->status, p->sm_count,
                                                 static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) p->wrote(stream, -1);
+    return map_cuda(e);
+}
+
+size_t kvpool_attend_ws_bytes(const kvpool_t* p, int agents, int q_heads) {
+    if (!p || agents < 1 || q_heads < p->kv_heads || q_heads % p->kv_heads) return 0;
+    const int group = q_heads / p->kv_heads;
+    if ((long long)agents * group > p->max_rows) return 0;
+    return ws_layout(p, (long long)agents * group, group).bytes;
+}
+
+int kvpool_attend_ws(kvpool_t* p, int layer, const void* Q, int agents, int q_heads, const kvpool_tail_t* tail,
+                     float* out, float softmax_scale, void* workspace, size_t workspace_bytes, void* stream) {
+    kvp::AttendArgs a;
+    const int rc = attend_args(p, layer, Q, agents, q_heads, tail, out, softmax_scale, stream, a);
+    if (rc) return rc;
+    const WsLayout w = ws_layout(p, a.rows, a.group);
+    if (w.bytes == 0) return KVPOOL_ERR_UNSUPPORTED;  // more row groups than one wave of CTAs
+    if (!workspace || !aligned16(workspace) || workspace_bytes < w.bytes) return KVPOOL_ERR_INVALID_ARG;
+    // slices of the context, one CTA each, their partial states into the
+    // workspace; then the log-sum-exp merge with the tails and the inverse FWHT
+    kvp::AttendArgs pa = a;
+    pa.tailK = pa.tailV = nullptr;
+    pa.tail_len = nullptr;
+    pa.tail_max = 0;
+    pa.part_ml = static_cast<float*>(workspace);
+    pa.part_acc = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + w.acc_off);
+    pa.ws_ctas = p->sm_count;  // one wave of CTAs
+    pa.ws_nslice_max = (int)w.nslice_max;
+    int nslice = 0;
+    pa.ws_nslice = &nslice;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), pa, p->status, p->sm_count, st);
+    if (e == cudaSuccess && (nslice < 1 || nslice > w.nslice_max)) e = cudaErrorInvalidValue;
+    if (e == cudaSuccess)
+        e = kvp::launch_merge_partials(nslice, pa.part_ml, pa.part_acc, p->kv_heads, p->head_dim, a, st);
     if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
 }

@@ -164,6 +164,13 @@ struct AttendArgs {
     // of the output (see kvpool_attend_partial); null otherwise
     float* part_ml;      // [Hk][rows][2]
     float* part_acc;     // [Hk][rows][D]
+    // workspace mode of the tensor-core kernel (ws_ctas > 0, partial mode
+    // only): the context in slices of one CTA each, at most ws_ctas CTAs;
+    // part_ml / part_acc then hold [nslice][Hk][rows] and *ws_nslice gets
+    // nslice
+    int ws_ctas;
+    int ws_nslice_max;  // the workspace holds at most this many slices
+    int* ws_nslice;
 };
 
 // Log-sum-exp merge of `parts` partial results laid out [parts][Hk][rows]

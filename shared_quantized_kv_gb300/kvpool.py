@@ -84,6 +84,10 @@ _SIGS = {
     "kvpool_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                               [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]),
+    "kvpool_attend_ws": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                        ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_float,
+                                        ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]),
+    "kvpool_attend_ws_bytes": (ctypes.c_size_t, [ctypes.c_void_p, ctypes.c_int, ctypes.c_int]),
     "kvpool_attend_partial": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                              ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]),
@@ -305,6 +309,33 @@ class KVPool:
         _check(_lib().kvpool_attend(self._h, layer, _dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, tp,
                                     _dev_ptr(out, torch.float32, "out"), softmax_scale,
                                     _stream_ptr(stream)), "kvpool_attend")
+        return out
+
+    def attend_ws_bytes(self, agents, q_heads) -> int:
+        """Workspace bytes kvpool_attend_ws needs for this many agents."""
+        return int(_lib().kvpool_attend_ws_bytes(self._h, int(agents), int(q_heads)))
+
+    def attend_ws(self, layer, Q, workspace=None, out=None, tail=None, softmax_scale=0.0, stream=None):
+        """kvpool_attend_ws: as attend, through a device workspace (uint8
+        tensor of at least attend_ws_bytes bytes; allocated here if None)."""
+        import torch
+
+        A, Hq, d = Q.shape
+        if out is None:
+            out = torch.empty((A, Hq, d), dtype=torch.float32, device=Q.device)
+        if workspace is None:
+            workspace = torch.empty(max(self.attend_ws_bytes(A, Hq), 16), dtype=torch.uint8, device=Q.device)
+        tp = None
+        if tail is not None:
+            Kt, Vt, lens = tail
+            self._tail = Tail(_dev_ptr(Kt, torch.bfloat16, "tail K").value,
+                              _dev_ptr(Vt, torch.bfloat16, "tail V").value,
+                              _dev_ptr(lens, torch.int32, "tail len").value, Kt.shape[2])
+            tp = ctypes.byref(self._tail)
+        _check(_lib().kvpool_attend_ws(self._h, layer, _dev_ptr(Q, torch.bfloat16, "Q"), A, Hq, tp,
+                                       _dev_ptr(out, torch.float32, "out"), softmax_scale,
+                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                       _stream_ptr(stream)), "kvpool_attend_ws")
         return out
 
     def attend_partial(self, layer, Q, t_begin, t_end, ml=None, acc=None, softmax_scale=0.0, stream=None):
