@@ -131,8 +131,9 @@ int kvpool_create(kvpool_t** out, int layers, int kv_heads, int head_dim, int ct
  * quantised values and scale as a pair of fp16 operands (about 22 significant
  * bits), the token's power-of-two range factor applied to its logit exactly.
  * kvpool_export_layer exports such a layer with *kscale = 1 and
- * kvpool_export_kscales copies its block scales; kvpool_import_layer returns
- * KVPOOL_ERR_UNSUPPORTED for these pools. Other k_block values:
+ * kvpool_export_kscales copies its block scales; such layers are loaded with
+ * kvpool_import_layer_blocks (kvpool_import_layer returns
+ * KVPOOL_ERR_UNSUPPORTED for these pools). Other k_block values:
  * KVPOOL_ERR_INVALID_ARG. */
 int kvpool_create_ex(kvpool_t** out, int layers, int kv_heads, int head_dim, int ctx,
                      const uint8_t* bits_per_layer, int max_rows, int k_block);
@@ -405,6 +406,25 @@ int kvpool_export_layer(const kvpool_t* pool, int layer, void* kq, void* vcodes,
  * KVPOOL_ERR_STATE if the layer already holds data. All four are required. */
 int kvpool_import_layer(kvpool_t* pool, int layer, const void* kq, const void* vcodes,
                         const void* vnorm, const void* kscale, void* stream);
+
+/* Load one layer of a block-scaled pool (kvpool_create_ex, k_block 32) from
+ * what kvpool_export_layer, kvpool_export_kscales and kvpool_layer_widths
+ * give for a layer of another block-scaled pool with the same kv_heads and
+ * head_dim: len tokens (1..ctx); kq int8 [kv_heads][len][head_dim]; vcodes
+ * the layer's code groups, per KV head back to back (kv_heads *
+ * sum_g head_dim * 4 * widths[g] bytes: kvpool_export_layer's layout);
+ * vnorm float [kv_heads][len]; kscales float [kv_heads][len][head_dim/32];
+ * widths: host uint8 [ceil(len/32)], each from 2 to this layer's create
+ * width (NULL: every group at the create width). The four buffers may be
+ * host or device memory; the copies are asynchronous on `stream` (host
+ * buffers should be pinned). Write-once: KVPOOL_ERR_STATE if the layer holds
+ * tokens. Afterwards the layer holds len tokens and takes appends if len is a
+ * multiple of 32. KVPOOL_ERR_UNSUPPORTED for per-tensor pools (they use
+ * kvpool_import_layer). Source: the QKVShare blog (mhpn.cn), section 3.1:
+ * the sender packs the quantised cache with its scales, and the receiver
+ * loads it. */
+int kvpool_import_layer_blocks(kvpool_t* pool, int layer, const void* kq, const void* vcodes, const void* vnorm,
+                               const void* kscales, const uint8_t* widths, int len, void* stream);
 
 /* Copy the library's float32 Lloyd-Max table for `bits` (2, 3 or 4) to host
  * arrays: 2^bits centroids (ascending) and 2^bits - 1 midpoints. The library

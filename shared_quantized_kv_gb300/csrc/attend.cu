@@ -254,8 +254,30 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     if (r >= R) return;
     const long long stride = (long long)Hk * R;  // between slices
     const long long b0 = (long long)g * R + r;
-    float M = -CUDART_INF_F;
-    for (int s = lane; s < nsplit; s += 32) {
+    // one round trip: lane s's (m, l) of slice s and the accumulators of the
+    // first kFirst slices are all requested before any is used
+    constexpr int kFirst = 16;
+    const float2 ml0 = lane < nsplit ? *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + lane * stride))
+                                     : make_float2(-CUDART_INF_F, 0.f);
+    float v[kFirst][EPL];
+#pragma unroll
+    for (int u = 0; u < kFirst; ++u) {
+        const float* src = part_acc + (b0 + (long long)u * stride) * D + lane * EPL;
+        if (u < nsplit) {
+            if constexpr (EPL == 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src);
+                v[u][0] = x.x, v[u][1] = x.y, v[u][2] = x.z, v[u][3] = x.w;
+            } else {
+                const float2 x = *reinterpret_cast<const float2*>(src);
+                v[u][0] = x.x, v[u][1] = x.y;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
+        }
+    }
+    float M = ml0.y > 0.f ? ml0.x : -CUDART_INF_F;
+    for (int s = lane + 32; s < nsplit; s += 32) {
         const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + s * stride));
         if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
@@ -264,41 +286,36 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     float acc[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) acc[e] = 0.f;
-    for (int s0 = 0; s0 < nsplit; s0 += 32) {
-        float w = 0.f;
-        if (s0 + lane < nsplit) {
-            const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + (s0 + lane) * stride));
-            if (ml.y > 0.f) {
-                w = exp2f(ml.x - M);
-                L += w * ml.y;
+    float w = ml0.y > 0.f ? exp2f(ml0.x - M) : 0.f;  // slice `lane`
+    L += w * ml0.y;
+#pragma unroll
+    for (int u = 0; u < kFirst; ++u) {
+        const float wu = __shfl_sync(full, w, u);  // 0 past nsplit
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+    }
+    // slices from kFirst on (more than kFirst slices), four at a time
+    for (int s0 = kFirst; s0 < nsplit; s0 += 4) {
+        float ww[4], x[4][EPL];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int s = s0 + u;
+            float wl = 0.f;
+            if (s < nsplit && s >= 32) {  // slices 16..31 have their weight in lane s
+                const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + s * stride));
+                wl = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
+                if (lane == 0) L += wl * ml.y;  // counted once
             }
+            ww[u] = s < 32 ? __shfl_sync(full, w, s & 31) : wl;
+            if (s >= nsplit) ww[u] = 0.f;
+            const float* src = part_acc + (b0 + (long long)s * stride) * D + lane * EPL;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[u][e] = ww[u] != 0.f ? src[e] : 0.f;
         }
-        const int n = min(32, nsplit - s0);
-        for (int k = 0; k < n; k += 4) {
-            float ww[4], v[4][EPL];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                ww[u] = __shfl_sync(full, w, (k + u) & 31);
-                if (k + u >= n) ww[u] = 0.f;
-                const float* src = part_acc + (b0 + (long long)(s0 + k + u) * stride) * D + lane * EPL;
-                if (ww[u] != 0.f) {  // the same for every lane
-                    if constexpr (EPL == 4) {
-                        const float4 x = *reinterpret_cast<const float4*>(src);
-                        v[u][0] = x.x, v[u][1] = x.y, v[u][2] = x.z, v[u][3] = x.w;
-                    } else {
-                        const float2 x = *reinterpret_cast<const float2*>(src);
-                        v[u][0] = x.x, v[u][1] = x.y;
-                    }
-                } else {
+        for (int u = 0; u < 4; ++u)
 #pragma unroll
-                    for (int e = 0; e < EPL; ++e) v[u][e] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-#pragma unroll
-                for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ww[u], v[u][e], acc[e]);
-        }
+            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ww[u], x[u][e], acc[e]);
     }
     L = warp_sum(L);
     // inverse rotation H acc / D: channel lane * EPL + e

@@ -841,6 +841,47 @@ int kvpool_import_layer(kvpool_t* p, int layer, const void* kq, const void* vcod
     return rc;
 }
 
+int kvpool_import_layer_blocks(kvpool_t* p, int layer, const void* kq, const void* vcodes, const void* vnorm,
+                               const void* kscales, const uint8_t* widths, int len, void* stream) {
+    int rc = check_layer(p, layer);
+    if (rc) return rc;
+    if (!p->k_block) return KVPOOL_ERR_UNSUPPORTED;
+    if (!kq || !vcodes || !vnorm || !kscales || len < 1 || len > p->ctx) return KVPOOL_ERR_INVALID_ARG;
+    if (p->compressed[layer] || p->len[layer] != 0) return KVPOOL_ERR_STATE;
+    const int ng = (len + 31) / 32;
+    std::vector<uint8_t> w(ng);
+    std::vector<uint32_t> off(ng);
+    size_t head_bytes = 0;  // the layer's code bytes per KV head
+    for (int g = 0; g < ng; ++g) {
+        w[g] = widths ? widths[g] : (uint8_t)p->bits[layer];
+        if (w[g] < 2 || w[g] > p->bits[layer]) return KVPOOL_ERR_INVALID_ARG;
+        off[g] = (uint32_t)head_bytes;
+        head_bytes += (size_t)p->head_dim * 4 * w[g];
+    }
+    const kvp::LayerBufs L = p->layer(layer);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t rows = (size_t)p->kv_heads, D = (size_t)p->head_dim, T = (size_t)len, Tp = (size_t)p->ctx_pad;
+    const size_t nb = D / (size_t)p->k_block;  // block scales per token
+    static const float kOne = 1.0f;  // the per-layer scale of a block-scaled layer
+    cudaError_t e = cudaMemcpy2DAsync(L.kq, Tp * D, kq, T * D, T * D, rows, cudaMemcpyDefault, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(L.vcodes, (size_t)L.vhead, vcodes, head_bytes, head_bytes, rows, cudaMemcpyDefault, st);
+    if (e == cudaSuccess) e = cudaMemcpy2DAsync(L.vnorm, Tp * 4, vnorm, T * 4, T * 4, rows, cudaMemcpyDefault, st);
+    if (e == cudaSuccess)
+        e = cudaMemcpy2DAsync(L.kscales, Tp * nb * 4, kscales, T * nb * 4, T * nb * 4, rows, cudaMemcpyDefault, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.kscale, &kOne, sizeof(float), cudaMemcpyHostToDevice, st);
+    // the group table (pageable host memory: staged before the calls return)
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.gbits, w.data(), (size_t)ng, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(L.goff, off.data(), (size_t)ng * 4, cudaMemcpyHostToDevice, st);
+    if (e == cudaSuccess) e = kvp::launch_norm_max({p->kv_heads, p->head_dim, len, p->ctx_pad}, L, st);
+    p->wrote(stream, layer);
+    if (e != cudaSuccess) return map_cuda(e);
+    p->gw[layer] = w;
+    p->len[layer] = len;
+    p->compressed[layer] = 1;
+    return KVPOOL_OK;
+}
+
 int kvpool_export_kscales(const kvpool_t* p, int layer, float* kscales, void* stream) {
     int rc = check_layer(p, layer);
     if (rc) return rc;

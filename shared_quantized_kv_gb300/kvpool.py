@@ -81,6 +81,8 @@ _SIGS = {
     "kvpool_codebook": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "kvpool_export_layer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
     "kvpool_import_layer": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5),
+    "kvpool_import_layer_blocks": (ctypes.c_int, [ctypes.c_void_p, ctypes.c_int] + [ctypes.c_void_p] * 5 +
+                                   [ctypes.c_int, ctypes.c_void_p]),
     "kvpool_attend_noalloc": (ctypes.c_int, [ctypes.c_void_p] * 5 + [ctypes.c_int] * 4 +
                               [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
                                ctypes.c_void_p, ctypes.c_float, ctypes.c_void_p]),
@@ -439,6 +441,18 @@ class KVPool:
         _check(_lib().kvpool_import_layer(self._h, layer, kq.data_ptr(), vcodes.data_ptr(),
                                           vnorm.data_ptr(), kscale.data_ptr(),
                                           _stream_ptr(stream)), "kvpool_import_layer")
+
+    def import_layer_blocks(self, layer, kq, vcodes, vnorm, kscales, widths=None, stream=None):
+        """Load a block-scaled layer: kq int8 [Hk, len, d], vcodes uint8 (the
+        layer's groups per head back to back), vnorm float32 [Hk, len],
+        kscales float32 [Hk, len, d/32] (device tensors); widths: list of the
+        groups' V widths (None: the layer's width)."""
+        buf = None
+        if widths is not None:
+            buf = (ctypes.c_uint8 * max(len(widths), 1))(*widths)
+        _check(_lib().kvpool_import_layer_blocks(self._h, layer, kq.data_ptr(), vcodes.data_ptr(), vnorm.data_ptr(),
+                                                 kscales.data_ptr(), buf, int(kq.shape[1]), _stream_ptr(stream)),
+               "kvpool_import_layer_blocks")
 
     def export_kscales(self, layer, stream=None):
         """Block scales of a block-scaled pool's layer: float32 [Hk, ctx, d/32]."""

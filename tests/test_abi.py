@@ -80,5 +80,8 @@ def test_null_pool_calls(kp):
     assert lib.kvpool_append(None, 0, None, None, 1, None) == -1
     assert lib.kvpool_append_bits(None, 0, None, None, 1, 3, None) == -1
     assert lib.kvpool_layer_widths(None, 0, None, 0) == -1
+    assert lib.kvpool_import_layer_blocks(None, 0, None, None, None, None, None, 1, None) == -1
+    assert lib.kvpool_attend_ws(None, 0, None, 1, 1, None, None, 0.0, None, 0, None) == -1
+    assert lib.kvpool_attend_ws_bytes(None, 1, 1) == 0
     assert lib.kvpool_layer_len(None, 0) == -1
     lib.kvpool_destroy(None)

@@ -179,3 +179,69 @@ def test_append_width_errors(kp):
         per_tensor.append(0, dK[:, :32].contiguous(), dV[:, :32].contiguous(), bits=2)
     assert e.value.code == ERR_UNSUPPORTED
     per_tensor.close()
+
+
+@pytest.mark.parametrize("host", [False, True])
+def test_handoff_of_a_grown_layer(kp, host):
+    """A block-scaled layer grown at widths 2, 4, 3 is exported (bytes, block
+    scales, widths) and loaded into a fresh pool (QKVShare blog, section 3.1:
+    the quantised cache travels with its scales): the same bytes, decompress
+    and attention against the oracle; the loaded layer then takes a further
+    append."""
+    import torch
+
+    w = wl.custom("mixw_handoff", 1, 2, 8, 128, 600, 3, "lognormal")
+    pool, K, V, Q, enc = _grow(kp, w, [128, 320, 416], [2, 4, 3], 4)
+    kq, vc, vn, _ = pool.export_layer(0)
+    ks = pool.export_kscales(0)
+    widths = pool.layer_widths(0)
+    if host:  # pinned host buffers
+        kq, vc, vn, ks = (t.cpu().pin_memory() for t in (kq, vc, vn, ks))
+    dst = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [4], max_rows=w.rows, k_block=32)
+    dst.import_layer_blocks(0, kq, vc, vn, ks, widths)
+    torch.cuda.synchronize()
+    assert dst.layer_len(0) == 416 and dst.layer_widths(0) == widths and dst.layer_view(0).mixed
+    check_encode(dst, 0, enc)
+    check_decompress(dst, 0, enc)
+    out = dst.attend(0, to_dev(Q))
+    assert dst.status() == 0
+    assert attention_error(out, enc, Q) <= TOL
+    with pytest.raises(kp.KVPoolError) as e:  # write-once
+        dst.import_layer_blocks(0, kq, vc, vn, ks, widths)
+    assert e.value.code == ERR_STATE
+    # the loaded layer grows on
+    dst.append(0, to_dev(np.ascontiguousarray(K[:, 416:600])), to_dev(np.ascontiguousarray(V[:, 416:600])), bits=2)
+    widths2 = widths + [2] * 6
+    enc2 = codec.encode_layer_groups(K[:, :600], V[:, :600], widths2)
+    check_encode(dst, 0, enc2)
+    out = dst.attend(0, to_dev(Q))
+    assert dst.status() == 0
+    assert attention_error(out, enc2, Q) <= TOL
+    dst.close()
+    pool.close()
+
+
+def test_import_blocks_errors(kp):
+    import torch
+
+    w = wl.custom("mixw_imp_err", 1, 2, 4, 64, 200, 2, "lognormal")
+    pool = kp.KVPool(1, 2, 64, 200, [3], k_block=32)
+    kq = torch.zeros((2, 64, 64), dtype=torch.int8, device="cuda")
+    vc = torch.zeros((2, 2 * 64 * 12), dtype=torch.uint8, device="cuda")
+    vn = torch.zeros((2, 64), dtype=torch.float32, device="cuda")
+    ks = torch.ones((2, 64, 2), dtype=torch.float32, device="cuda")
+    with pytest.raises(kp.KVPoolError) as e:  # a width above the create width
+        pool.import_layer_blocks(0, kq, vc, vn, ks, [3, 4])
+    assert e.value.code == ERR_INVALID_ARG
+    assert pool.layer_len(0) == 0
+    per_tensor = kp.KVPool(1, 2, 64, 200, [3])
+    with pytest.raises(kp.KVPoolError) as e:
+        per_tensor.import_layer_blocks(0, kq, vc, vn, ks, [3, 3])
+    assert e.value.code == ERR_UNSUPPORTED
+    per_tensor.close()
+    # all-zero codes and norms with unit scales: a layer of zeros, attended to zero output
+    pool.import_layer_blocks(0, kq, vc, vn, ks, [3, 3])
+    Q = to_dev(wl.layer_q(w, 0))
+    out = pool.attend(0, Q)
+    assert pool.status() == 0 and float(out.abs().max()) == 0.0
+    pool.close()
