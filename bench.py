@@ -1,14 +1,17 @@
 """Benchmark of the shared quantized KV pool hot path on GB300.
 
 The headline is the decode step of the method: every agent's queries attend
-over the resident compressed pool, layer after layer (one kvpool_attend call
-per layer: a layer's queries depend on the layer before). Workload: the
+over the resident compressed pool, layer after layer (one attention call per
+layer: a layer's queries depend on the layer before). The step calls
+kvpool_attend_ws (the context in one-CTA slices over every SM, partial states
+in a workspace allocated once before timing, one merge kernel); the
+cluster-merged kvpool_attend is timed beside it as the phase "attend". Workload: the
 Llama-3-8B-shaped pool (32 layers, 8 KV heads, 32 query heads, head_dim 128,
 4096 shared-context tokens, 15 agents x 1 decode query, int8 K, 3-bit V).
 
 value = agents x ranks / (max over ranks of the time of one decode step, all
-layers of kvpool_attend): agent-decode steps per second. The attend phase is
-captured as one CUDA graph and replayed; CUDA events around each replay give
+layers of kvpool_attend_ws): agent-decode steps per second. Each attention
+phase is captured as one CUDA graph and replayed; CUDA events around each replay give
 its device time, and L2 is flushed (a 512 MiB write) before every replay,
 outside the events. The write-once encode (kvpool_compress_layers, all layers
 in one call) and the per-agent materialisation baseline (kvpool_decompress_
@@ -69,7 +72,7 @@ def workload_config(w, ws, k_block):
     return {"workload": w.name, "k_scales": "per 32 elements" if k_block else "per layer",
             "layers": w.layers, "kv_heads": w.kv_heads, "q_heads": w.q_heads, "head_dim": w.head_dim,
             "ctx": w.ctx, "agents": w.agents, "v_bits": sorted(set(w.bits_list())), "tail": w.tail_max,
-            "step": "decode: kvpool_attend of every layer for every agent",
+            "step": "decode: kvpool_attend_ws of every layer for every agent (workspace allocated once)",
             "parallelism": "one GPU" if ws == 1 else
                            f"one pool, its KV heads split over {ws} ranks (no data-path collective)"}
 
@@ -78,7 +81,8 @@ def launches_per_step(w, k_block, per_layer_calls, batch=32):
     """The library's kernel launches in one step, by phase. Compress: a max|K|
     kernel and an encode kernel per layer, or, for all layers in one call, one
     max|K| kernel and one encode kernel per V width per 32 layers. Attend: the
-    tensor-core kernel per layer (per-tensor and block-scaled K alike).
+    tensor-core kernel per layer (per-tensor and block-scaled K alike);
+    attend_ws: that kernel in workspace mode and the merge kernel per layer.
     Decompress: one kernel per layer, or one per V width per 32 layers."""
     bits = w.bits_list()
     chunks = [bits[i:i + batch] for i in range(0, len(bits), batch)]
@@ -87,7 +91,7 @@ def launches_per_step(w, k_block, per_layer_calls, batch=32):
         comp, dec = 2 * len(bits), len(bits)
     else:
         comp, dec = len(chunks) + widths, widths
-    return {"compress": comp, "attend": len(bits), "decompress": dec}
+    return {"compress": comp, "attend": len(bits), "attend_ws": 2 * len(bits), "decompress": dec}
 
 
 def max_over_ranks(step_ms, ph_ms, phases, device=None):
@@ -252,7 +256,14 @@ def run_gpu(args):
         else:  # the whole shared context in one call
             pool.compress_layers(layers, K, V)
 
-    def attend():  # the decode step: layer l + 1's queries come from layer l's output
+    # the decode step's workspace, allocated once (like the pool)
+    wsbuf = torch.empty(max(pool.attend_ws_bytes(A, hk * G), 16), dtype=torch.uint8, device=dev)
+
+    def attend_ws():  # the decode step: layer l + 1's queries come from layer l's output
+        for l in layers:
+            pool.attend_ws(l, Q[l], wsbuf, out[l], tail[l] if tail else None)
+
+    def attend():  # the same step through the cluster-merged kvpool_attend
         for l in layers:
             pool.attend(l, Q[l], out[l], tail[l] if tail else None)
 
@@ -264,19 +275,20 @@ def run_gpu(args):
             pool.decompress_layers(layers, Kd, Vd)
 
     # eager once (state + correctness of the calls), then capture each phase
-    compress(); attend(); decompress()
+    compress(); attend(); attend_ws(); decompress()
     assert pool.status() == 0
     graphs = {}
     s = torch.cuda.Stream(device=dev)
     s.wait_stream(torch.cuda.current_stream())
-    for name, fn in (("compress", compress), ("attend", attend), ("decompress", decompress)):
+    for name, fn in (("compress", compress), ("attend_ws", attend_ws), ("attend", attend),
+                     ("decompress", decompress)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=s):
             fn()
         graphs[name] = g
     torch.cuda.synchronize()
 
-    phases = ("attend", "compress", "decompress")
+    phases = ("attend_ws", "attend", "compress", "decompress")
 
     def one_step(record):
         ev = []
@@ -324,7 +336,7 @@ def run_gpu(args):
             ph_ms[ph] += e0.elapsed_time(e1)
     ph_ms = {ph: v / args.steps for ph, v in ph_ms.items()}
     _, ph_ms = max_over_ranks(0.0, ph_ms, phases, dev if ws > 1 else None)
-    step_ms = ph_ms["attend"]  # the decode step: all layers of kvpool_attend
+    step_ms = ph_ms["attend_ws"]  # the decode step: all layers of kvpool_attend_ws
 
     launches = launches_per_step(w, args.k_block, args.per_layer_calls)
     # algorithmic bytes per layer (this rank's share of the heads)
@@ -333,7 +345,7 @@ def run_gpu(args):
     pool_layer = pool.pool_bytes() / L
     tail_bytes = 2 * A * hk * w.tail_len(w.decode_steps - 1) * w.head_dim * 2 if tail else 0
     algo = {"compress": kv_in + pool_layer, "attend": pool_layer + tail_bytes,
-            "decompress": pool_layer + kv_in}
+            "attend_ws": pool_layer + tail_bytes, "decompress": pool_layer + kv_in}
     peak, peak_kind = _peaks()
     ph_info = {}
     for ph in phases:
@@ -343,14 +355,18 @@ def run_gpu(args):
                        "algo_bytes_per_layer": int(algo[ph]), "GB_per_s": round(gbs, 1),
                        "hbm_frac": round(gbs / peak, 4), "launches_per_step": launches[ph]}
     ph_info["attend"]["agent_steps_per_s"] = round(A / (ph_ms["attend"] / 1e3), 1)
+    ph_info["attend_ws"]["agent_steps_per_s"] = round(A / (ph_ms["attend_ws"] / 1e3), 1)
+    ph_info["attend"]["note"] = "kvpool_attend: clusters merge the context splits in distributed shared memory"
+    ph_info["attend_ws"]["note"] = ("kvpool_attend_ws (the decode step): one-CTA context slices, partial states "
+                                    "in the workspace, a merge kernel per layer")
     ph_info["compress"]["note"] = "write-once encode of the shared context (once per pool, not per step)"
     ph_info["decompress"]["note"] = "per-agent materialisation baseline of the pages (not on the decode path)"
     att_file = "attend_rows.cuh"
 
     e2e = e2e_full = None
     if not args.no_e2e:
-        e2e = run_e2e_decode(args, pool, w, Q, tail, out)
-        e2e_full = run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd)
+        e2e = run_e2e_decode(args, pool, w, Q, tail, out, wsbuf)
+        e2e_full = run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd, wsbuf)
 
     value = A / (step_ms / 1e3)  # every agent's step over the whole (split) pool
     line = {
@@ -360,16 +376,17 @@ def run_gpu(args):
         "data": "synthetic (seeded; bf16 K/V with LogNormal(0,0.5) channel std and 1% x10 outlier "
                 "channels, Q ~ N(0,1))",
         "config": dict(workload_config(w, ws, args.k_block),
-                       calls="attend: one call per layer (the step); compress and decompress: all layers "
-                             "per call" + (" (one call per layer)" if args.per_layer_calls else ""),
+                       calls="attend_ws (the step) and attend: one call per layer; compress and decompress: "
+                             "all layers per call" + (" (one call per layer)" if args.per_layer_calls else ""),
                        l2="flushed (512 MiB write) before every timed graph replay, outside the events"),
         "phases": ph_info,
-        "roofline": {"bound": "hbm", "kernel": "attend", "achieved": ph_info["attend"]["GB_per_s"],
-                     "peak": peak, "unit": "GB/s", "frac": ph_info["attend"]["hbm_frac"],
+        "roofline": {"bound": "hbm", "kernel": "attend_ws", "achieved": ph_info["attend_ws"]["GB_per_s"],
+                     "peak": peak, "unit": "GB/s", "frac": ph_info["attend_ws"]["hbm_frac"],
                      "traffic": _traffic(att_file), "peak_source": peak_kind,
-                     "algo_bytes_per_launch": int(algo["attend"]),
-                     "how": "algorithmic bytes per layer (pool layer + tails) / (attend graph time / layers)"},
-        "gpu_launches": args.steps * launches["attend"],
+                     "algo_bytes_per_launch": int(algo["attend_ws"]),
+                     "how": "algorithmic bytes per layer (pool layer + tails) / (attend_ws graph time / layers: "
+                            "the attention kernel and its merge kernel)"},
+        "gpu_launches": args.steps * launches["attend_ws"],
         "gpu_launches_all_phases": args.steps * sum(launches.values()),
         "clocks": clocks,
         "wall_s_timed": round(t_wall, 3),
@@ -386,7 +403,7 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
-def run_e2e_decode(args, pool, w, Q, tail, out):
+def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
     """The decode step end to end: the pool stays resident; every step the
     queries of all layers (and, with tails, each agent's new tail token of
     every layer) are copied up from pinned host memory in one copy, the layers
@@ -436,7 +453,7 @@ def run_e2e_decode(args, pool, w, Q, tail, out):
                     tail[l][0][:, :, pos].copy_(nv[0])
                     tail[l][1][:, :, pos].copy_(nv[1])
                     t = tail[l]
-                pool.attend(l, q_dev[l], o_dev[l], t, stream=s_main)
+                pool.attend_ws(l, q_dev[l], wsbuf, o_dev[l], t, stream=s_main)
             ev_done[c].record(s_main)
         with torch.cuda.stream(s_out):
             for c, ls in enumerate(chunks):
@@ -472,7 +489,7 @@ def run_e2e_decode(args, pool, w, Q, tail, out):
                    f"downloaded {chunk} layers at a time on a second stream; one CUDA graph per step"}
 
 
-def run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd):
+def run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd, wsbuf):
     """The same step with inputs copied from pinned host memory and the results
     (attention outputs and the decompressed K/V) copied back, inside the timed
     region. Layers are independent, so the step is pipelined over three
@@ -532,7 +549,7 @@ def run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd):
                 o, kd, vd = kv_out[l]
                 pool.reset_layer(l)
                 pool.compress(l, k, v, stream=s_main)
-                pool.attend(l, q, o, tail[l] if tail else None, stream=s_main)
+                pool.attend_ws(l, q, wsbuf, o, tail[l] if tail else None, stream=s_main)
                 pool.decompress(l, kd, vd, stream=s_main)
             ev_done[c].record(s_main)
         with torch.cuda.stream(s_out):

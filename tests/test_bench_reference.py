@@ -37,9 +37,12 @@ def test_launch_count_by_call_structure():
     from shared_quantized_kv_gb300 import workloads as wl
 
     llama = wl.WORKLOADS["llama3_8b_4k"]  # 32 layers, all 3-bit
-    assert bench.launches_per_step(llama, 0, False) == {"compress": 2, "attend": 32, "decompress": 1}
-    assert bench.launches_per_step(llama, 0, True) == {"compress": 64, "attend": 32, "decompress": 32}
+    assert bench.launches_per_step(llama, 0, False) == {"compress": 2, "attend": 32, "attend_ws": 64,
+                                                         "decompress": 1}
+    assert bench.launches_per_step(llama, 0, True) == {"compress": 64, "attend": 32, "attend_ws": 64,
+                                                        "decompress": 32}
     assert bench.launches_per_step(llama, 32, False)["attend"] == 32  # block-scaled K: the same kernel
     qwen = wl.WORKLOADS["qwen3_32b_32k"]  # 64 layers, 2/3/4 bits: two launch chunks of 32 layers
     widths = sum(len(set(qwen.bits_list()[c:c + 32])) for c in (0, 32))
-    assert bench.launches_per_step(qwen, 0, False) == {"compress": 2 + widths, "attend": 64, "decompress": widths}
+    assert bench.launches_per_step(qwen, 0, False) == {"compress": 2 + widths, "attend": 64, "attend_ws": 128,
+                                                        "decompress": widths}
