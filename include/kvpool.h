@@ -308,8 +308,9 @@ int kvpool_attend_partial(kvpool_t* pool, int layer, const void* Q, int agents, 
  * o = H (sum_s 2^(m_s - M) acc_s) / head_dim joined with the tail tokens in
  * one softmax, divided by the total weight. part_ml: float [parts][kv_heads]
  * [agents * G][2]; part_acc: float [parts][kv_heads][agents * G][head_dim]
- * (the parts' buffers back to back), device. Q, tail, softmax_scale as in
- * kvpool_attend. Needs no pool. */
+ * (the parts' buffers back to back), device. A part whose l is not
+ * positive (an empty slice) counts for nothing; its m and accumulator are
+ * not used. Q, tail, softmax_scale as in kvpool_attend. Needs no pool. */
 int kvpool_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads, int head_dim,
                           const void* Q, int agents, int q_heads, const kvpool_tail_t* tail, float* out,
                           float softmax_scale, void* stream);

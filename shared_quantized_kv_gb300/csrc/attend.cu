@@ -290,9 +290,9 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     L += w * ml0.y;
 #pragma unroll
     for (int u = 0; u < kFirst; ++u) {
-        const float wu = __shfl_sync(full, w, u);  // 0 past nsplit
+        const float wu = __shfl_sync(full, w, u);  // 0 past nsplit and for empty slices
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) acc[e] = fmaf(wu, v[u][e], acc[e]);
+        for (int e = 0; e < EPL; ++e) acc[e] = wu != 0.f ? fmaf(wu, v[u][e], acc[e]) : acc[e];
     }
     // slices from kFirst on (more than kFirst slices), four at a time
     for (int s0 = kFirst; s0 < nsplit; s0 += 4) {
@@ -315,7 +315,7 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
 #pragma unroll
         for (int u = 0; u < 4; ++u)
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) acc[e] = fmaf(ww[u], x[u][e], acc[e]);
+            for (int e = 0; e < EPL; ++e) acc[e] = ww[u] != 0.f ? fmaf(ww[u], x[u][e], acc[e]) : acc[e];
     }
     L = warp_sum(L);
     // inverse rotation H acc / D: channel lane * EPL + e

@@ -158,3 +158,37 @@ def test_block_scaled_slices(kp):
     assert _row_err(out.cpu().numpy(), attention.attend_f64(Kh, Vh, Qh)) <= TOL
     assert pool.status() == 0
     pool.close()
+
+
+def test_merge_of_many_slices(kp):
+    """40 one-tile slices (more than one warp's lanes hold: the merge reads the
+    (m, l) of slices 32.. in its second loop), with some slices repeated as
+    empty parts (l = 0), merged with tails, against the oracle."""
+    import torch
+
+    Hk, Hq, d, ctx, A = 2, 8, 64, 40 * 128 - 50, 3
+    w = wl.custom("many_slices", 1, Hk, Hq, d, ctx, A, "lognormal", 6, 1, (3,))
+    pool, Kh, Vh, Qh, Q = _setup(kp, w, 3)
+    edges = list(range(0, ctx, 128)) + [ctx]
+    MLs, ACCs = [], []
+    for b, e in zip(edges[:-1], edges[1:]):
+        ml, acc = pool.attend_partial(0, Q, b, e)
+        MLs.append(ml)
+        ACCs.append(acc)
+    assert len(MLs) == 40
+    # three empty parts (l = 0) among them, one in the first 16: neither their
+    # m nor their accumulator (NaN here) may count
+    empty_ml = torch.zeros_like(MLs[0])
+    empty_ml[..., 0] = 1e30
+    for at in (5, 17, 36):
+        MLs.insert(at, empty_ml)
+        ACCs.insert(at, torch.full_like(ACCs[0], float("nan")))
+    ML, ACC = torch.stack(MLs), torch.stack(ACCs)
+    Kt, Vt = wl.layer_tail(w, 0)
+    lens = np.array([(a * 2) % (w.tail_max + 1) for a in range(A)])
+    dev_tail = (to_dev(Kt), to_dev(Vt), torch.from_numpy(lens.astype(np.int32)).cuda())
+    out = kp.merge_partials(ML, ACC, Q, Hk, dev_tail)
+    assert pool.status() == 0
+    ref = attention.attend_f64(Kh, Vh, Qh, (Kt, Vt, lens))
+    assert _row_err(out.cpu().numpy(), ref) <= TOL
+    pool.close()
