@@ -344,22 +344,67 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
 #pragma unroll
     for (int e = 0; e < EPL; ++e) ot[e] = 0.f;
     if (tK != nullptr) {
+        // the agent's tail, 32 tokens at a time: lane = token for the logits
+        // (the Q row in shared memory, read by every lane at once), then lane
+        // = channels for P.V; online softmax over the chunks
+        __shared__ float sq[8][D];
+        const int wi = threadIdx.x / 32;
         const int n = min(max(tlen[a], 0), tail_max);  // never read past the tail buffers
-        float q[EPL];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) q[e] = bf2f(Q[((long long)a * Hq + h) * D + lane * EPL + e]);
+        for (int e = 0; e < EPL; ++e) sq[wi][lane * EPL + e] = bf2f(Q[((long long)a * Hq + h) * D + lane * EPL + e]);
+        __syncwarp();
         const long long tb = ((long long)a * Hk + g) * tail_max;
-        for (int t = 0; t < n; ++t) {
-            float dot = 0.f;
+        for (int c0 = 0; c0 < n; c0 += 32) {
+            const int t = c0 + lane;
+            float lg = -CUDART_INF_F;
+            if (t < n) {
+                const uint4* kr = reinterpret_cast<const uint4*>(tK + (tb + t) * D);
+                float dot = 0.f;
+#pragma unroll 8
+                for (int cc = 0; cc < D / 8; ++cc) {
+                    const uint4 u = kr[cc];
+                    const float* qq = sq[wi] + cc * 8;
+                    dot = fmaf(qq[0], bf2f(u.x & 0xFFFF), dot);
+                    dot = fmaf(qq[1], bf2f(u.x >> 16), dot);
+                    dot = fmaf(qq[2], bf2f(u.y & 0xFFFF), dot);
+                    dot = fmaf(qq[3], bf2f(u.y >> 16), dot);
+                    dot = fmaf(qq[4], bf2f(u.z & 0xFFFF), dot);
+                    dot = fmaf(qq[5], bf2f(u.z >> 16), dot);
+                    dot = fmaf(qq[6], bf2f(u.w & 0xFFFF), dot);
+                    dot = fmaf(qq[7], bf2f(u.w >> 16), dot);
+                }
+                lg = __fmul_rn(dot, scale_log2);
+            }
+            const float mnew = fmaxf(mt, warp_max(lg));
+            const float corr = exp2f(mt - mnew);  // 0 on the first chunk
+            const float pt = t < n ? exp2f(lg - mnew) : 0.f;
+            lt = lt * corr + warp_sum(pt);
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) dot = fmaf(q[e], bf2f(tK[(tb + t) * D + lane * EPL + e]), dot);
-            dot = warp_sum(dot);
-            const float lg = __fmul_rn(dot, scale_log2);
-            const float mnew = fmaxf(mt, lg);
-            const float corr = exp2f(mt - mnew), p = exp2f(lg - mnew);
-            lt = lt * corr + p;
+            for (int e = 0; e < EPL; ++e) ot[e] *= corr;
+            const int nk = min(32, n - c0);
+            for (int k0 = 0; k0 < nk; k0 += 8) {  // eight V rows in flight at a time
+                float pk[8];
+                uint2 v[8];
 #pragma unroll
-            for (int e = 0; e < EPL; ++e) ot[e] = ot[e] * corr + p * bf2f(tV[(tb + t) * D + lane * EPL + e]);
+                for (int u = 0; u < 8; ++u) {
+                    pk[u] = __shfl_sync(full, pt, (k0 + u) & 31);  // 0 past the tail
+                    const uint16_t* vr = tV + (tb + c0 + k0 + u) * D + lane * EPL;
+                    v[u] = make_uint2(0u, 0u);
+                    if (k0 + u < nk) {
+                        if constexpr (EPL == 4) v[u] = *reinterpret_cast<const uint2*>(vr);
+                        else v[u].x = *reinterpret_cast<const uint32_t*>(vr);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    ot[0] = fmaf(pk[u], bf2f(v[u].x & 0xFFFF), ot[0]);
+                    ot[1] = fmaf(pk[u], bf2f(v[u].x >> 16), ot[1]);
+                    if constexpr (EPL == 4) {
+                        ot[2] = fmaf(pk[u], bf2f(v[u].y & 0xFFFF), ot[2]);
+                        ot[3] = fmaf(pk[u], bf2f(v[u].y >> 16), ot[3]);
+                    }
+                }
+            }
             mt = mnew;
         }
     }
