@@ -927,11 +927,10 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 const uint32_t tS = tmem + kColS + 128 * b + lane_off;
                 const int nval = t_end - (t_begin + i * kTile);  // valid tokens of the tile
                 if constexpr (KB) warp_wait(b_sig_full + 8 * (i & 1), (i >> 1) & 1, bad);
-                // chunk ch (32 tokens) of S for this lane (block-scaled: column t
-                // times sigma_t), tokens past the split at -inf
-                auto load_s = [&](int ch, uint32_t (&u)[32]) {
-                    ptx::tmem_ld32(tS + 32 * ch, u);
-                    ptx::tmem_wait_ld();
+                // chunk ch (32 tokens) of S as loaded for this lane, finished in
+                // place (block-scaled: column t times sigma_t; tokens past the
+                // split at -inf)
+                auto fix_s = [&](int ch, uint32_t (&u)[32]) {
                     if constexpr (KB) {
                         const float4* s4 = reinterpret_cast<const float4*>(sig + (i & 1) * 128 + 32 * ch);
 #pragma unroll
@@ -949,11 +948,15 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                             if (32 * ch + k >= nval) u[k] = __float_as_uint(-CUDART_INF_F);
                     }
                 };
+                auto load_s = [&](int ch, uint32_t (&u)[32]) {
+                    ptx::tmem_ld32(tS + 32 * ch, u);
+                    ptx::tmem_wait_ld();
+                    fix_s(ch, u);
+                };
+                // SPREAD: this lane's own chunk, kept from the max pass for P'
+                uint32_t uown[SPREAD ? 32 : 1];
                 float smax = -CUDART_INF_F;
-#pragma unroll
-                for (int c = 0; c < 2; ++c) {
-                    uint32_t u[32];
-                    load_s(2 * sg + c, u);
+                auto chunk_max = [&](const uint32_t (&u)[32]) {
                     float mm[4];
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -962,6 +965,26 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                                       fmaxf(fmaxf(__uint_as_float(u[k + 16]), __uint_as_float(u[k + 20])),
                                             fmaxf(__uint_as_float(u[k + 24]), __uint_as_float(u[k + 28]))));
                     smax = fmaxf(smax, fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])));
+                };
+                if constexpr (SPREAD) {
+                    // both chunks of the half under one wait; the lane keeps its own
+                    uint32_t u0[32], u1[32];
+                    ptx::tmem_ld32(tS + 32 * (2 * sg), u0);
+                    ptx::tmem_ld32(tS + 32 * (2 * sg + 1), u1);
+                    ptx::tmem_wait_ld();
+                    fix_s(2 * sg, u0);
+                    fix_s(2 * sg + 1, u1);
+                    chunk_max(u0);
+                    chunk_max(u1);
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) uown[k] = dup ? u1[k] : u0[k];
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        uint32_t u[32];
+                        load_s(2 * sg + c, u);
+                        chunk_max(u);
+                    }
                 }
                 pmax[(b * 2 + sg) * 128 + tl] = smax;
                 ptx::bar_sync(1 + q, 64);  // both halves read S; their maxima are published
@@ -1035,15 +1058,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 } else {
                     // lanes 0-15 take chunk 2 sg, lanes 16-31 chunk 2 sg + 1; each
                     // lane writes zeros over the other chunk of its row copy
-                    uint32_t u[32], hw[16], lw[16];
-                    {
-                        uint32_t u1[32];
-                        load_s(2 * sg, u);
-                        load_s(2 * sg + 1, u1);
-#pragma unroll
-                        for (int k = 0; k < 32; ++k) u[k] = dup ? u1[k] : u[k];
-                    }
-                    form(2 * sg + dup, u, hw, lw);
+                    uint32_t hw[16], lw[16];
+                    form(2 * sg + dup, uown, hw, lw);
                     uint32_t a[16];
 #pragma unroll
                     for (int k = 0; k < 16; ++k) a[k] = dup ? 0u : hw[k];
