@@ -979,12 +979,15 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 #pragma unroll
                     for (int k = 0; k < 32; ++k) uown[k] = dup ? u1[k] : u0[k];
                 } else {
-#pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t u[32];
-                        load_s(2 * sg + c, u);
-                        chunk_max(u);
-                    }
+                    // both chunks of the half under one wait (read again for P')
+                    uint32_t u0[32], u1[32];
+                    ptx::tmem_ld32(tS + 32 * (2 * sg), u0);
+                    ptx::tmem_ld32(tS + 32 * (2 * sg + 1), u1);
+                    ptx::tmem_wait_ld();
+                    fix_s(2 * sg, u0);
+                    fix_s(2 * sg + 1, u1);
+                    chunk_max(u0);
+                    chunk_max(u1);
                 }
                 pmax[(b * 2 + sg) * 128 + tl] = smax;
                 ptx::bar_sync(1 + q, 64);  // both halves read S; their maxima are published
@@ -1090,12 +1093,18 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             if constexpr (SPREAD) l += __shfl_xor_sync(0xffffffffu, l, 16);
             psum[sg * 128 + tl] = l;
             const bool stage = dup == 0 && r < nrows;
+            // the half row's columns, every 32-column read under one wait
+            constexpr int NO = HC >= 32 ? HC / 32 : 1;
+            uint32_t uo[NO][32];
+            if constexpr (HC >= 32) {
+#pragma unroll
+                for (int c = 0; c < NO; ++c) ptx::tmem_ld32(tmem + kColO + lane_off + sg * HC + 32 * c, uo[c]);
+                ptx::tmem_wait_ld();
+            }
 #pragma unroll
             for (int c0 = 0; c0 < HC; c0 += 32) {
                 if constexpr (HC >= 32) {
-                    uint32_t u[32];
-                    ptx::tmem_ld32(tmem + kColO + lane_off + sg * HC + c0, u);
-                    ptx::tmem_wait_ld();
+                    uint32_t (&u)[32] = uo[c0 / 32];
                     if constexpr (SPREAD) {
 #pragma unroll
                         for (int k = 0; k < 32; ++k)
