@@ -264,8 +264,9 @@ int kvpool_attend(kvpool_t* pool, int layer, const void* Q, int agents, int q_he
  * aligned; its contents need no initialisation and are scratch afterwards):
  * the context is cut into more slices than kvpool_attend's clusters can hold
  * (one CTA each, enough to fill every SM once), their partial states (the
- * kvpool_attend_partial quantities) go to the workspace, and a second kernel
- * merges them with the agents' tails exactly as kvpool_merge_partials. Same
+ * kvpool_attend_partial quantities) go to the workspace, the slices' CTAs
+ * also compute the agents' tails (each slice a share of the agents), and a
+ * second kernel merges all of it as kvpool_merge_partials does. Same
  * arguments, result and errors as kvpool_attend, plus
  * KVPOOL_ERR_INVALID_ARG for a missing, misaligned or short workspace and
  * KVPOOL_ERR_UNSUPPORTED when the (KV head, row group) pairs alone exceed

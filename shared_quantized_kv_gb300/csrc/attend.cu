@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(256)
 merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml, int nsplit, int R,
                   int Hk, int Hq, int G, const uint16_t* __restrict__ Q, const uint16_t* __restrict__ tK,
                   const uint16_t* __restrict__ tV, const int32_t* __restrict__ tlen, int tail_max,
-                  float scale_log2, float* __restrict__ out) {
+                  float scale_log2, float* __restrict__ out, const float* __restrict__ tail_ml) {
     constexpr int EPL = D / 32;
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x % 32;
@@ -343,7 +343,17 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     float mt = -CUDART_INF_F, lt = 0.f, ot[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) ot[e] = 0.f;
-    if (tK != nullptr) {
+    if (tail_ml != nullptr) {
+        // tails computed by the attention kernel: (m, l) here, the
+        // unnormalised accumulator in the output row
+        const float2 t = *reinterpret_cast<const float2*>(tail_ml + 2 * b0);
+        mt = t.x;
+        lt = t.y;
+        if (lt > 0.f) {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) ot[e] = out[((long long)a * Hq + h) * D + lane * EPL + e];
+        }
+    } else if (tK != nullptr) {
         // the agent's tail, 32 tokens at a time: lane = token for the logits
         // (the Q row in shared memory, read by every lane at once), then lane
         // = channels for P.V; online softmax over the chunks
@@ -454,7 +464,7 @@ cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* 
     auto kern = head_dim == 64 ? merge_rows_kernel<64> : merge_rows_kernel<128>;
     return cudaLaunchKernelEx(&cfg, kern, part_acc, part_ml, parts, a.rows, kv_heads, a.q_heads, a.group,
                               (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len,
-                              a.tail_max, a.scale_log2, a.out);
+                              a.tail_max, a.scale_log2, a.out, (const float*)a.ws_tail_ml);
 }
 
 cudaError_t launch_attend_split(const Shape& s, const LayerBufs& L, const AttendArgs& a,

@@ -105,6 +105,8 @@ struct Params {
     float inv_lam;
     float* part_ml;   // partial mode ([nslice][Hk][R][2] and [nslice][Hk][R][D]), else null
     float* part_acc;
+    float* ws_tail_ml;  // workspace mode with tails: the rows' tail (m, l), [Hk][R][2] (the
+                        // unnormalised tail accumulators go to `out`, as in the cluster path)
     int rgn;          // row groups per KV head
     int nslice;       // context slices per (KV head, row group): blockIdx.z = row group + rgn * slice;
                       // slice s of a cluster of S CTAs covers tokens t0 + (s S + rank) tps ...
@@ -617,7 +619,11 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
         ptx::grid_dep_wait();
         if (tid == 0)
             for (; first < min(ntile, NR); ++first) issue_tile(first);
-        tail_attention<D>(p, sm + (kNumOp == 2 ? lay.op : 0), tailml, S, crank, g, row0, nrows);
+        // the agents of this CTA: a mod S == rank in a cluster; a mod nslice
+        // == slice for the one-CTA slices of workspace mode
+        const bool ws = p.part_acc != nullptr;
+        tail_attention<D>(p, sm + (kNumOp == 2 ? lay.op : 0), tailml, ws ? p.nslice : S, ws ? slice : crank, g,
+                          row0, nrows);
     }
 
     bool bad = false;
@@ -1142,6 +1148,12 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
             for (int e = 0; e < EPL; ++e) acc[e] = l > 0.f ? src[lane * EPL + e] : 0.f;
             write_partial<D>(p, slice, g, row0 + rr, lane, l > 0.f ? m : -CUDART_INF_F, l, acc, oscale * (float)D);
         }
+        if constexpr (TAIL) {  // the tails of this CTA's agents, for the merge kernel
+            for (int rr = tid; rr < nrows; rr += kThreads)
+                if ((rr / p.G) % p.nslice == slice)
+                    *reinterpret_cast<float2*>(p.ws_tail_ml + 2 * ((size_t)g * p.R + row0 + rr)) =
+                        make_float2(tailml[2 * rr], tailml[2 * rr + 1]);
+        }
         if (warp == kWarpMma) {
             ptx::tc_fence_after();
             ptx::tmem_dealloc(tmem, kCols);
@@ -1426,6 +1438,7 @@ cudaError_t launch_attend_rows_bits(const Shape& s, const LayerBufs& L, const At
     prm.t0 = a.t0;
     prm.part_ml = a.part_ml;
     prm.part_acc = a.part_acc;
+    prm.ws_tail_ml = a.ws_tail_ml;
     prm.ctx_pad = s.ctx_pad;
     prm.Hk = s.kv_heads;
     prm.Q = (const uint16_t*)a.Q;

@@ -552,14 +552,14 @@ int attend_args(kvpool_t* p, int layer, const void* Q, int agents, int q_heads, 
 // offset of the accumulators (after the (m, l) pairs).
 struct WsLayout {
     long long nslice_max;
-    size_t acc_off, bytes;
+    size_t acc_off, tail_off, bytes;
 };
 WsLayout ws_layout(const kvpool* p, long long rows, int group) {
     // row groups as the tensor-core launcher forms them (at most 64 rows in
     // all: groups of <= 64 rows; else <= 128), whole agents each
     const bool spread = rows <= 64;
     const long long RW = ((spread ? 64 : 128) / group) * group;
-    WsLayout w{0, 0, 0};
+    WsLayout w{0, 0, 0, 0};
     if (RW < 1) return w;
     const long long jobs = (long long)p->kv_heads * ((rows + RW - 1) / RW);
     const long long ntiles = (p->ctx + kvp::kTokenPad - 1) / kvp::kTokenPad;
@@ -567,7 +567,9 @@ WsLayout ws_layout(const kvpool* p, long long rows, int group) {
     if (w.nslice_max < 1) return w;
     const size_t per = (size_t)p->kv_heads * rows;  // partial rows per slice
     w.acc_off = align256((size_t)w.nslice_max * per * 2 * sizeof(float));
-    w.bytes = w.acc_off + (size_t)w.nslice_max * per * p->head_dim * sizeof(float);
+    // then the rows' tail (m, l), for calls with tails
+    w.tail_off = align256(w.acc_off + (size_t)w.nslice_max * per * p->head_dim * sizeof(float));
+    w.bytes = w.tail_off + per * 2 * sizeof(float);
     return w;
 }
 
@@ -600,11 +602,13 @@ int kvpool_attend_ws(kvpool_t* p, int layer, const void* Q, int agents, int q_he
     if (w.bytes == 0) return KVPOOL_ERR_UNSUPPORTED;  // more row groups than one wave of CTAs
     if (!workspace || !aligned16(workspace) || workspace_bytes < w.bytes) return KVPOOL_ERR_INVALID_ARG;
     // slices of the context, one CTA each, their partial states into the
-    // workspace; then the log-sum-exp merge with the tails and the inverse FWHT
+    // workspace (and each slice's share of the agents' tails); then the
+    // log-sum-exp merge with the tails and the inverse FWHT
     kvp::AttendArgs pa = a;
-    pa.tailK = pa.tailV = nullptr;
-    pa.tail_len = nullptr;
-    pa.tail_max = 0;
+    if (a.tailK != nullptr) {
+        pa.ws_tail_ml = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + w.tail_off);
+        a.ws_tail_ml = pa.ws_tail_ml;
+    }
     pa.part_ml = static_cast<float*>(workspace);
     pa.part_acc = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + w.acc_off);
     pa.ws_ctas = p->sm_count;  // one wave of CTAs

@@ -171,6 +171,10 @@ struct AttendArgs {
     int ws_ctas;
     int ws_nslice_max;  // the workspace holds at most this many slices
     int* ws_nslice;
+    // workspace mode with tails: the slices' CTAs compute the agents' tails
+    // (accumulators into `out`, (m, l) here, [Hk][rows][2]) and the merge
+    // joins them; null otherwise (the merge computes the tails itself)
+    float* ws_tail_ml;
 };
 
 // Log-sum-exp merge of `parts` partial results laid out [parts][Hk][rows]
