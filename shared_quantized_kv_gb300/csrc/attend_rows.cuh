@@ -616,6 +616,10 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     // first tiles are in flight; the (last) operand stage is free until then
     int first = 0;  // loader: tiles requested before the role loops
     if constexpr (TAIL) {
+        // the layer's bytes may be requested before the grid-dependency wait
+        // unless the launch before this one wrote them (the tails and Q after it)
+        if (tid == 0 && p.early)
+            for (; first < min(ntile, NR); ++first) issue_tile(first);
         ptx::grid_dep_wait();
         if (tid == 0)
             for (; first < min(ntile, NR); ++first) issue_tile(first);
