@@ -966,15 +966,16 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 // SPREAD: this lane's own chunk, kept from the max pass for P'
                 uint32_t uown[SPREAD ? 32 : 1];
                 float smax = -CUDART_INF_F;
+                // three-input maxima: 16 instructions for 32 values and smax
                 auto chunk_max = [&](const uint32_t (&u)[32]) {
-                    float mm[4];
+                    auto f = [&](int k) { return __uint_as_float(u[k]); };
+                    float mm[11];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        mm[k] = fmaxf(fmaxf(fmaxf(__uint_as_float(u[k]), __uint_as_float(u[k + 4])),
-                                            fmaxf(__uint_as_float(u[k + 8]), __uint_as_float(u[k + 12]))),
-                                      fmaxf(fmaxf(__uint_as_float(u[k + 16]), __uint_as_float(u[k + 20])),
-                                            fmaxf(__uint_as_float(u[k + 24]), __uint_as_float(u[k + 28]))));
-                    smax = fmaxf(smax, fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3])));
+                    for (int k = 0; k < 10; ++k) mm[k] = ptx::max3(f(3 * k), f(3 * k + 1), f(3 * k + 2));
+                    mm[10] = ptx::max3(f(30), f(31), smax);
+                    const float a = ptx::max3(mm[0], mm[1], mm[2]), b = ptx::max3(mm[3], mm[4], mm[5]);
+                    const float c = ptx::max3(mm[6], mm[7], mm[8]);
+                    smax = ptx::max3(ptx::max3(a, b, c), mm[9], mm[10]);
                 };
                 if constexpr (SPREAD) {
                     // both chunks of the half under one wait; the lane keeps its own
@@ -1034,7 +1035,22 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 // P' = p * n_t / nref as fp16 hi + lo over the chunk's own S
                 // columns: hi in the first 16 columns, lo in the next 16
                 const float4* nn4 = reinterpret_cast<const float4*>(sm + e * lay.op + lay.op_n);
-                const float2 ns = make_float2(-s_ref, -s_ref), c2 = make_float2(cr, cr);
+                // While every row of the warp has |m_ref| <= 2^10 the exponent is
+                // one fused s * cr - m_ref (the product exact, one rounding):
+                // m_ref = fl(s_ref * cr) is then within 2^-14 of s_ref * cr, a
+                // factor within 2^(+-2^-14) common to the row's weights under
+                // that reference, and p stays below 2^(kLazy + 2^-13). Larger
+                // logits take the difference s - s_ref first (in place, `shift`)
+                // and then fl((s - s_ref) * cr + 0).
+                const bool fused = __all_sync(0xffffffffu, fabsf(m_ref) <= 1024.f);
+                const float2 c2 = make_float2(cr, cr);
+                const float2 nm = fused ? make_float2(-m_ref, -m_ref) : make_float2(0.f, 0.f);
+                auto shift = [&](uint32_t (&u)[32]) {
+                    if (!fused) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) u[k] = __float_as_uint(__fsub_rn(__uint_as_float(u[k]), s_ref));
+                    }
+                };
                 float2 l2 = make_float2(0.f, 0.f);
                 // P' of one 32-token chunk of S (this lane's S row), packed hi / lo
                 auto form = [&](int ch, const uint32_t (&u)[32], uint32_t (&hw)[16], uint32_t (&lw)[16]) {
@@ -1044,8 +1060,8 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
 #pragma unroll
                         for (int w2 = 0; w2 < 2; ++w2) {
                             const int k = k4 * 2 + w2;  // token pair (2k, 2k + 1) of the chunk
-                            const float2 d = __fmul2_rn(
-                                __fadd2_rn(make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1])), ns), c2);
+                            const float2 sv = make_float2(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
+                            const float2 d = __ffma2_rn(sv, c2, nm);
                             const float2 pv = make_float2(ptx::ex2(d.x), ptx::ex2(d.y));  // -inf -> 0
                             l2 = __fadd2_rn(l2, pv);
                             const float2 pp = __fmul2_rn(pv, w2 ? make_float2(nn.z, nn.w) : make_float2(nn.x, nn.y));
@@ -1064,6 +1080,7 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                         const int ch = 2 * sg + c;
                         uint32_t u[32], hw[16], lw[16];
                         load_s(ch, u);  // this chunk's own columns: nothing of it was overwritten yet
+                        shift(u);
                         form(ch, u, hw, lw);
                         ptx::tmem_st16(tS + 32 * ch, hw);
                         ptx::tmem_st16(tS + 32 * ch + 16, lw);
@@ -1072,6 +1089,7 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                     // lanes 0-15 take chunk 2 sg, lanes 16-31 chunk 2 sg + 1; each
                     // lane writes zeros over the other chunk of its row copy
                     uint32_t hw[16], lw[16];
+                    shift(uown);
                     form(2 * sg + dup, uown, hw, lw);
                     uint32_t a[16];
 #pragma unroll

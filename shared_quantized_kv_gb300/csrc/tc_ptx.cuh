@@ -307,5 +307,12 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// the largest of three floats (a NaN operand is passed over, as by fmaxf)
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 }  // namespace ptx
 }  // namespace kvp
