@@ -72,6 +72,26 @@ def test_extreme_magnitudes(kp, kexp, vexp):
     pool.close()
 
 
+@pytest.mark.parametrize("kexp", [6, 7])
+def test_logits_around_the_fused_exponent_bound(kp, kexp):
+    # K scaled so that the rows' largest logits (log2 units) lie around
+    # 2^10 (about 300 to 1100 for 2^6, 600 to 2200 for 2^7), where the
+    # softmax switches between its two exponent forms (one fused
+    # multiply-add, or the difference first); several tiles, so the
+    # reference moves between tiles of one row; both attention paths
+    w = wl.custom("bound", 1, 2, 16, 128, 1500, 6, "lognormal", bits=(3,))
+    K, V = wl.layer_kv(w, 0)
+    K = _bf16(codec.bf16_to_f32(K) * np.float32(2.0 ** kexp))
+    Q = wl.layer_q(w, 0)
+    pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [3], max_rows=w.rows)
+    enc = _check_layer(kp, pool, K, V, Q, 3)
+    out = pool.attend_ws(0, to_dev(Q))
+    assert pool.status() == 0
+    err = attention_error(out, enc, Q)
+    assert err <= TOL, err
+    pool.close()
+
+
 @pytest.mark.parametrize("where", ["k_inf", "v_nan"])
 def test_nonfinite_input_sets_status(kp, where):
     w = wl.custom("nonfinite", 1, 2, 4, 64, 100, 2, "lognormal")
