@@ -406,54 +406,85 @@ def run_gpu(args):
 def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
     """The decode step end to end: the pool stays resident; every step the
     queries of all layers (and, with tails, each agent's new tail token of
-    every layer) are copied up from pinned host memory in one copy, the layers
-    attend in order, and the attention outputs come back in chunks of eight
-    layers on a second stream, overlapping the later layers. One step is
-    captured as a CUDA graph and replayed."""
+    every layer) are copied up from pinned host memory on an input stream in
+    three pieces (layer 0, layers 1-3, the rest), so that layer 0 starts once
+    its own inputs are up. With tails, one copy kernel per piece writes the
+    new tokens of its layers into the agents' tails (the tails of all layers
+    live in one buffer). The layers attend in order, and the attention outputs
+    come back on a second stream in chunks that shrink towards the last layer
+    (8, 8, 8, 4, 2, 1, 1 layers for 32), overlapping the later layers. One
+    step is captured as a CUDA graph and replayed."""
     import torch
 
     L, A = w.layers, w.agents
     dev = Q[0].device
     q_bytes = Q[0].numel() * Q[0].element_size()
-    nt_shape = (2, A, w.kv_heads, w.head_dim)  # one new tail token per agent and KV head
-    nt_bytes = 2 * A * w.kv_heads * w.head_dim * 2 if tail else 0
-    per_in = q_bytes + nt_bytes
-    d_in = torch.empty(L * per_in, dtype=torch.uint8, device=dev)
-    h_in = torch.empty(L * per_in, dtype=torch.uint8).pin_memory()
-    q_dev, nt_dev = [], []
+    nt_bytes = 0
+    if tail:
+        # every layer's tails in one buffer [L][2][A][Hk][T_max][d], so that one
+        # copy kernel appends the step's tokens of several layers
+        tshape = tuple(tail[0][0].shape)  # [A, Hk, T_max, d]
+        tail_all = torch.empty((L, 2) + tshape, dtype=torch.bfloat16, device=dev)
+        for l in range(L):
+            tail_all[l, 0].copy_(tail[l][0])
+            tail_all[l, 1].copy_(tail[l][1])
+        t_e2e = [(tail_all[l, 0], tail_all[l, 1], tail[l][2]) for l in range(L)]
+        pos = w.tail_len(w.decode_steps - 1) - 1  # the step's token
+        nt_shape = (L, 2, tshape[0], tshape[1], tshape[3])  # one new token per agent and KV head
+        nt_bytes = 2 * tshape[0] * tshape[1] * tshape[3] * 2
+    d_in = torch.empty(L * (q_bytes + nt_bytes), dtype=torch.uint8, device=dev)
+    h_in = torch.empty(L * (q_bytes + nt_bytes), dtype=torch.uint8).pin_memory()
+    q_dev = [d_in[l * q_bytes:(l + 1) * q_bytes].view(torch.bfloat16).view(Q[l].shape) for l in range(L)]
     for l in range(L):
-        off = l * per_in
-        qv = d_in[off:off + q_bytes].view(torch.bfloat16).view(Q[l].shape)
-        qv.copy_(Q[l])
-        q_dev.append(qv)
-        if tail:
-            nv = d_in[off + q_bytes:off + per_in].view(torch.bfloat16).view(nt_shape)
-            pos = w.tail_len(w.decode_steps - 1) - 1  # the step's token
-            nv[0].copy_(tail[l][0][:, :, pos])
-            nv[1].copy_(tail[l][1][:, :, pos])
-            nt_dev.append((nv, pos))
+        q_dev[l].copy_(Q[l])
+    if tail:
+        nt_all = d_in[L * q_bytes:].view(torch.bfloat16).view(nt_shape)
+        for l in range(L):
+            nt_all[l, 0].copy_(tail[l][0][:, :, pos])
+            nt_all[l, 1].copy_(tail[l][1][:, :, pos])
     h_in.copy_(d_in.cpu())
     o_bytes = out[0].numel() * out[0].element_size()
     d_out = torch.empty(L * o_bytes, dtype=torch.uint8, device=dev)
     o_dev = [d_out[l * o_bytes:(l + 1) * o_bytes].view(torch.float32).view(out[l].shape) for l in range(L)]
     h_out = torch.empty(L * o_bytes, dtype=torch.uint8).pin_memory()
-    chunk = 8
-    chunks = [list(range(c, min(L, c + chunk))) for c in range(0, L, chunk)]
-    s_main, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    # download chunks: eight layers at a time, then shrinking, so that little
+    # is left to copy after the last layer
+    sizes, left = [], L
+    while left > 0:
+        n = 8 if left > 16 else max(1, left // 2)
+        sizes.append(n)
+        left -= n
+    chunks, c0 = [], 0
+    for n in sizes:
+        chunks.append(list(range(c0, c0 + n)))
+        c0 += n
+    # upload pieces: layer 0, layers 1-3, the rest (each waited for before its
+    # first layer)
+    pieces = [p for p in ((0, 1), (1, min(4, L)), (min(4, L), L)) if p[0] < p[1]]
+    s_main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_done = [torch.cuda.Event() for _ in chunks]
+    ev_in = [torch.cuda.Event() for _ in pieces]
+    piece_of = {p[0]: i for i, p in enumerate(pieces)}
 
     def step():
-        d_in.copy_(h_in, non_blocking=True)
+        s_in.wait_stream(s_main)
         s_out.wait_stream(s_main)
+        with torch.cuda.stream(s_in):
+            for i, (a, b) in enumerate(pieces):
+                d_in[a * q_bytes:b * q_bytes].copy_(h_in[a * q_bytes:b * q_bytes], non_blocking=True)
+                if tail:
+                    o0 = L * q_bytes
+                    d_in[o0 + a * nt_bytes:o0 + b * nt_bytes].copy_(h_in[o0 + a * nt_bytes:o0 + b * nt_bytes],
+                                                                    non_blocking=True)
+                ev_in[i].record(s_in)
         for c, ls in enumerate(chunks):
             for l in ls:
-                t = None
-                if tail:
-                    nv, pos = nt_dev[l]
-                    tail[l][0][:, :, pos].copy_(nv[0])
-                    tail[l][1][:, :, pos].copy_(nv[1])
-                    t = tail[l]
-                pool.attend_ws(l, q_dev[l], wsbuf, o_dev[l], t, stream=s_main)
+                if l in piece_of:
+                    s_main.wait_event(ev_in[piece_of[l]])
+                    if tail:  # the piece's new tokens into the tails
+                        a, b = pieces[piece_of[l]]
+                        tail_all[a:b, :, :, :, pos].copy_(nt_all[a:b])
+                pool.attend_ws(l, q_dev[l], wsbuf, o_dev[l], t_e2e[l] if tail else None, stream=s_main)
             ev_done[c].record(s_main)
         with torch.cuda.stream(s_out):
             for c, ls in enumerate(chunks):
@@ -461,6 +492,7 @@ def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
                 a, b = ls[0] * o_bytes, (ls[-1] + 1) * o_bytes
                 h_out[a:b].copy_(d_out[a:b], non_blocking=True)
         s_main.wait_stream(s_out)
+        s_main.wait_stream(s_in)
 
     s_main.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(s_main):
@@ -484,9 +516,11 @@ def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
     assert torch.equal(h_out.view(torch.float32)[:out[0].numel()].view(out[0].shape).to(dev), o_dev[0])
     return {"value": round(w.agents / (ms / 1e3), 2), "unit": UNIT, "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": int(h_in.numel()), "d2h_bytes_per_step": int(h_out.numel()),
-            "how": "decode step through the C-ABI, pool resident: one upload of every layer's queries"
-                   + (" and new tail tokens" if tail else "") + ", attend layer by layer, outputs "
-                   f"downloaded {chunk} layers at a time on a second stream; one CUDA graph per step"}
+            "how": "decode step through the C-ABI, pool resident: every layer's queries"
+                   + (" and new tail tokens (appended by one copy kernel per piece)" if tail else "")
+                   + f" uploaded in {len(pieces)} pieces on an input stream (layer 0 first), attend layer by "
+                   "layer, outputs "
+                   f"downloaded on a second stream in chunks of {sizes} layers; one CUDA graph per step"}
 
 
 def run_e2e_full(args, pool, w, K, V, Q, tail, out, Kd, Vd, wsbuf):
