@@ -238,7 +238,12 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
 // read by the lanes at once, their accumulators four slices at a time; one
 // inverse FWHT per row in registers and shuffles; then the agent's tail
 // tokens (online softmax) and the final normalisation. Launched as a
-// programmatic dependent of the kernel that wrote the partials.
+// programmatic dependent of the kernel that wrote the partials. It releases
+// its own dependents before its grid-dependency wait: the next layer's
+// attention CTAs then start while this merge waits, and reach their own wait
+// with their pool tiles already requested. Their wait still covers this
+// kernel's completion, which follows the partials' writer; what they read
+// before it (pool bytes) neither kernel writes.
 template <int D>
 __global__ void __launch_bounds__(256)
 merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml, int nsplit, int R,
@@ -249,8 +254,8 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x % 32;
     const int r = blockIdx.x * 8 + threadIdx.x / 32, g = blockIdx.y;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     if (r >= R) return;
     const long long stride = (long long)Hk * R;  // between slices
     const long long b0 = (long long)g * R + r;

@@ -195,9 +195,10 @@ struct kvpool {
     // -1 for none, kWroteMany for several (a multi-layer compress). An attend
     // may read its layer before the grid-dependency wait (programmatic
     // dependent launch) unless the launch right before it on the same stream
-    // wrote that layer: only the immediately preceding kernel can still be
-    // running when it starts, and that one cannot have started before the
-    // kernels ahead of it finished.
+    // wrote that layer. The kernels that write a layer (the encode) never
+    // release their dependents before they finish, so once any later launch
+    // has started, the writer is complete; only a writer launched right
+    // before the attend can be finishing as the attend starts.
     static constexpr int kWroteMany = -2;
     std::unordered_map<void*, int> last_write;
     std::mutex mu;  // last_write: attends may come from several host threads
