@@ -456,7 +456,7 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
 }  // namespace
 
 cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
-                                  int head_dim, const AttendArgs& a, cudaStream_t st) {
+                                  int head_dim, const AttendArgs& a, cudaStream_t st, int sm_count) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((a.rows + 7) / 8, kv_heads, 1);
     cfg.blockDim = dim3(256, 1, 1);
@@ -467,6 +467,26 @@ cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     auto kern = head_dim == 64 ? merge_rows_kernel<64> : merge_rows_kernel<128>;
+    // The merge starts early, while the attention kernel still holds most
+    // SMs: its CTAs would all land on the few SMs left free and share their
+    // load bandwidth for the partial states. When the grid fits one wave and
+    // the partial states are large (1 MiB or more), each CTA reserves more
+    // than half of an SM's shared memory (unused), so at most one CTA runs
+    // per SM and the rest start on the SMs the attention CTAs release. (With
+    // small partial states the free SMs load them fast enough, and the CTAs
+    // that would wait for a released SM only start later.)
+    constexpr int kSpreadSmem = 120 * 1024;
+    const size_t part_bytes = (size_t)parts * kv_heads * a.rows * (head_dim + 2) * sizeof(float);
+    if (sm_count > 0 && (long long)cfg.gridDim.x * cfg.gridDim.y <= sm_count && part_bytes >= (size_t(1) << 20)) {
+        // opted in once per instance (a static initialiser: thread-safe)
+        static const cudaError_t opt64 =
+            cudaFuncSetAttribute(merge_rows_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmem);
+        static const cudaError_t opt128 =
+            cudaFuncSetAttribute(merge_rows_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSpreadSmem);
+        const cudaError_t opt = head_dim == 64 ? opt64 : opt128;
+        if (opt != cudaSuccess) return opt;
+        cfg.dynamicSmemBytes = kSpreadSmem;
+    }
     return cudaLaunchKernelEx(&cfg, kern, part_acc, part_ml, parts, a.rows, kv_heads, a.q_heads, a.group,
                               (const uint16_t*)a.Q, (const uint16_t*)a.tailK, (const uint16_t*)a.tailV, a.tail_len,
                               a.tail_max, a.scale_log2, a.out, (const float*)a.ws_tail_ml);

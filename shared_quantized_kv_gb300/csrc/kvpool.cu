@@ -620,7 +620,8 @@ int kvpool_attend_ws(kvpool_t* p, int layer, const void* Q, int agents, int q_he
     cudaError_t e = kvp::launch_attend_tc(p->shape_of(layer), p->layer(layer), pa, p->status, p->sm_count, st);
     if (e == cudaSuccess && (nslice < 1 || nslice > w.nslice_max)) e = cudaErrorInvalidValue;
     if (e == cudaSuccess)
-        e = kvp::launch_merge_partials(nslice, pa.part_ml, pa.part_acc, p->kv_heads, p->head_dim, a, st);
+        e = kvp::launch_merge_partials(nslice, pa.part_ml, pa.part_acc, p->kv_heads, p->head_dim, a, st,
+                                       p->sm_count);
     if (e == cudaSuccess) p->wrote(stream, -1);
     return map_cuda(e);
 }
