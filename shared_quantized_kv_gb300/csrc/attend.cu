@@ -245,7 +245,7 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
 // kernel's completion, which follows the partials' writer; what they read
 // before it (pool bytes) neither kernel writes.
 template <int D>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(512)
 merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ part_ml, int nsplit, int R,
                   int Hk, int Hq, int G, const uint16_t* __restrict__ Q, const uint16_t* __restrict__ tK,
                   const uint16_t* __restrict__ tV, const int32_t* __restrict__ tlen, int tail_max,
@@ -253,7 +253,7 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     constexpr int EPL = D / 32;
     const unsigned full = 0xffffffffu;
     const int lane = threadIdx.x % 32;
-    const int r = blockIdx.x * 8 + threadIdx.x / 32, g = blockIdx.y;
+    const int r = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32, g = blockIdx.y;
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     if (r >= R) return;
@@ -362,7 +362,7 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
         // the agent's tail, 32 tokens at a time: lane = token for the logits
         // (the Q row in shared memory, read by every lane at once), then lane
         // = channels for P.V; online softmax over the chunks
-        __shared__ float sq[8][D];
+        __shared__ float sq[16][D];
         const int wi = threadIdx.x / 32;
         const int n = min(max(tlen[a], 0), tail_max);  // never read past the tail buffers
 #pragma unroll
@@ -457,9 +457,15 @@ cudaError_t run(const Shape& s, const LayerBufs& Lb, const AttendArgs& a, const 
 
 cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
                                   int head_dim, const AttendArgs& a, cudaStream_t st, int sm_count) {
+    // 8 warps (rows) per CTA; 16 where that puts a grid of more than one
+    // wave into one
+    int wpc = 8;
+    if (sm_count > 0 && (long long)((a.rows + 7) / 8) * kv_heads > sm_count &&
+        (long long)((a.rows + 15) / 16) * kv_heads <= sm_count)
+        wpc = 16;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((a.rows + 7) / 8, kv_heads, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.gridDim = dim3((a.rows + wpc - 1) / wpc, kv_heads, 1);
+    cfg.blockDim = dim3(32 * wpc, 1, 1);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
