@@ -179,9 +179,11 @@ struct AttendArgs {
 
 // Log-sum-exp merge of `parts` partial results laid out [parts][Hk][rows]
 // (see kvpool_merge_partials), one inverse FWHT per row, the agents' tails,
-// and the final normalisation into a.out. sm_count > 0: when the grid fits
-// one wave on that many SMs, each CTA reserves more than half of an SM's
-// shared memory, so that the CTAs spread one per SM (see attend.cu).
+// and the final normalisation into a.out. sm_count > 0 (the workspace path)
+// shapes the grid for that many SMs: CTAs of 16 warps where that fits a grid
+// of more than one wave into one, and for a one-wave grid over 1 MiB of
+// partial states a shared-memory reservation that spreads the CTAs one per
+// SM (see attend.cu).
 cudaError_t launch_merge_partials(int parts, const float* part_ml, const float* part_acc, int kv_heads,
                                   int head_dim, const AttendArgs& a, cudaStream_t st, int sm_count = 0);
 
