@@ -530,6 +530,9 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     const uint32_t b_sig_full = b_m + 8;           // KB: [2] sigma_t of a tile is written
     const uint32_t b_sig_empty = b_sig_full + 16;  // KB: [2] the softmax is done with the slot
     float* sO = reinterpret_cast<float*>(sm);      // epilogue: staging rows [128][ROWF]
+    // one-CTA slices of at most 64 rows (SPREAD) write their partial states
+    // straight from the softmax threads' registers, without staging rows
+    const bool direct = SPREAD && S == 1 && p.part_acc != nullptr;
 
     const int g = blockIdx.y;
     const int slice = (int)blockIdx.z / p.rgn;
@@ -1139,7 +1142,17 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                             u[k] = __float_as_uint(__uint_as_float(u[k]) +
                                                    __uint_as_float(__shfl_xor_sync(0xffffffffu, u[k], 16)));
                     }
-                    if (stage) {
+                    if (stage && direct) {
+                        // the slice's accumulator row, in the units of
+                        // write_partial (scale 2^nref / lam)
+                        const float sc = ldexpf(1.0f, *sNref) * p.inv_lam;
+                        float* dst = p.part_acc + (((size_t)slice * p.Hk + g) * p.R + row0 + r) * D + sg * HC + c0;
+#pragma unroll
+                        for (int c4 = 0; c4 < 32; c4 += 4)
+                            *reinterpret_cast<float4*>(dst + c4) =
+                                make_float4(__uint_as_float(u[c4]) * sc, __uint_as_float(u[c4 + 1]) * sc,
+                                            __uint_as_float(u[c4 + 2]) * sc, __uint_as_float(u[c4 + 3]) * sc);
+                    } else if (stage) {
                         float* dst = sO + r * ROWF + sg * HC + c0;
 #pragma unroll
                         for (int c4 = 0; c4 < 32; c4 += 4)
@@ -1148,7 +1161,12 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
                 }
             }
             ptx::bar_sync(1 + q, 64);  // both halves' row sums
-            if (sg == 0 && stage) {
+            if (sg == 0 && stage && direct) {
+                const float lt = psum[tl] + psum[128 + tl];
+                const size_t base = ((size_t)slice * p.Hk + g) * p.R + row0 + r;
+                p.part_ml[2 * base] = lt > 0.f ? m_ref : -CUDART_INF_F;
+                p.part_ml[2 * base + 1] = lt;
+            } else if (sg == 0 && stage) {
                 sO[r * ROWF + D] = m_ref;
                 sO[r * ROWF + D + 1] = psum[tl] + psum[128 + tl];
             }
@@ -1157,12 +1175,13 @@ attend_rows_kernel(const __grid_constant__ CUtensorMap kmap, const Params p) {
     if (bad) atomicOr(p.status, kStTimeout);
 
     // one CTA per context slice (workspace mode): the staged rows are the
-    // slice's partial states, written without a cluster merge
+    // slice's partial states, written without a cluster merge (SPREAD: the
+    // softmax threads have written them already)
     if (S == 1 && p.part_acc != nullptr) {
         ptx::tc_fence_before();  // the tensor-memory reads of O come before its release
         __syncthreads();
         const float oscale = ldexpf(1.0f, *sNref) / (float)D * p.inv_lam;
-        for (int rr = warp; rr < nrows; rr += kThreads / 32) {
+        for (int rr = warp; !direct && rr < nrows; rr += kThreads / 32) {
             const float* src = sO + rr * ROWF;
             const float m = src[D], l = src[D + 1];
             float acc[EPL];
