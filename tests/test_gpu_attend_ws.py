@@ -151,3 +151,33 @@ def test_workspace_errors(kp):
         big.attend_ws(0, to_dev(wl.layer_q(wb, 0)), torch.empty(1024, dtype=torch.uint8, device="cuda"))
     assert e.value.code == ERR_UNSUPPORTED
     big.close()
+
+
+def test_recompress_right_after_attention_same_stream(kp):
+    # attend_ws, then the same layer re-armed and compressed with other data,
+    # then attend_ws again, all queued on one stream with no host sync: the
+    # writers of the layer must not start before the first attention (and
+    # the merge that releases its dependents early) is done with it. Full
+    # Llama-4K-shaped layer, so the merge takes the spread launch.
+    import torch
+
+    w = wl.WORKLOADS["llama3_8b_4k"]
+    pool = kp.KVPool(1, w.kv_heads, w.head_dim, w.ctx, [3], max_rows=w.rows)
+    data = [wl.layer_kv(w, l) for l in (0, 1)]
+    Q = wl.layer_q(w, 0, 0)
+    Qd = to_dev(Q)
+    outs = []
+    for rep in range(2):
+        for K, V in data:
+            pool.reset_layer(0)
+            pool.compress(0, to_dev(K), to_dev(V))
+            outs.append(pool.attend_ws(0, Qd))
+    torch.cuda.synchronize()
+    assert pool.status() == 0
+    rows = _rows(w, 24, seed=3)
+    for i, out in enumerate(outs):
+        K, V = data[i % 2]
+        enc = codec.encode_layer(K, V, 3)
+        err = attention_error(out, enc, Q, None, rows=rows)
+        assert err <= TOL, (i, err)
+    pool.close()
