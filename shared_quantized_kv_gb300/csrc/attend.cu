@@ -261,7 +261,7 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
     const long long b0 = (long long)g * R + r;
     // one round trip: lane s's (m, l) of slice s and the accumulators of the
     // first kFirst slices are all requested before any is used
-    constexpr int kFirst = 16;
+    constexpr int kFirst = 20;
     const float2 ml0 = lane < nsplit ? *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + lane * stride))
                                      : make_float2(-CUDART_INF_F, 0.f);
     float v[kFirst][EPL];
@@ -306,7 +306,7 @@ merge_rows_kernel(const float* __restrict__ part_acc, const float* __restrict__ 
         for (int u = 0; u < 4; ++u) {
             const int s = s0 + u;
             float wl = 0.f;
-            if (s < nsplit && s >= 32) {  // slices 16..31 have their weight in lane s
+            if (s < nsplit && s >= 32) {  // slices below 32 have their weight in lane s
                 const float2 ml = *reinterpret_cast<const float2*>(part_ml + 2 * (b0 + s * stride));
                 wl = ml.y > 0.f ? exp2f(ml.x - M) : 0.f;
                 if (lane == 0) L += wl * ml.y;  // counted once
