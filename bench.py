@@ -403,6 +403,24 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def e2e_download_sizes(L: int) -> list:
+    """Layers per download chunk of the end-to-end decode step: eight at a
+    time, then halving, so that little is left to copy after the last layer
+    (32 layers: 8, 8, 8, 4, 2, 1, 1)."""
+    sizes, left = [], L
+    while left > 0:
+        n = 8 if left > 16 else max(1, left // 2)
+        sizes.append(n)
+        left -= n
+    return sizes
+
+
+def e2e_upload_pieces(L: int) -> list:
+    """Layer ranges [a, b) uploaded as one copy each: layer 0, layers 1-3,
+    the rest; each is waited for before its first layer attends."""
+    return [p for p in ((0, 1), (1, min(4, L)), (min(4, L), L)) if p[0] < p[1]]
+
+
 def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
     """The decode step end to end: the pool stays resident; every step the
     queries of all layers (and, with tails, each agent's new tail token of
@@ -447,20 +465,12 @@ def run_e2e_decode(args, pool, w, Q, tail, out, wsbuf):
     d_out = torch.empty(L * o_bytes, dtype=torch.uint8, device=dev)
     o_dev = [d_out[l * o_bytes:(l + 1) * o_bytes].view(torch.float32).view(out[l].shape) for l in range(L)]
     h_out = torch.empty(L * o_bytes, dtype=torch.uint8).pin_memory()
-    # download chunks: eight layers at a time, then shrinking, so that little
-    # is left to copy after the last layer
-    sizes, left = [], L
-    while left > 0:
-        n = 8 if left > 16 else max(1, left // 2)
-        sizes.append(n)
-        left -= n
+    sizes = e2e_download_sizes(L)
     chunks, c0 = [], 0
     for n in sizes:
         chunks.append(list(range(c0, c0 + n)))
         c0 += n
-    # upload pieces: layer 0, layers 1-3, the rest (each waited for before its
-    # first layer)
-    pieces = [p for p in ((0, 1), (1, min(4, L)), (min(4, L), L)) if p[0] < p[1]]
+    pieces = e2e_upload_pieces(L)
     s_main, s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
     ev_done = [torch.cuda.Event() for _ in chunks]
     ev_in = [torch.cuda.Event() for _ in pieces]
