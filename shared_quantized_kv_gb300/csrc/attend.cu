@@ -235,7 +235,8 @@ attend_combine_kernel(const float* __restrict__ part_acc, const float* __restric
 
 // kvpool_merge_partials and the merge of kvpool_attend_ws: one warp per
 // (row, KV head), lane = D/32 consecutive channels. The slices' (m, l) are
-// read by the lanes at once, their accumulators four slices at a time; one
+// read by the lanes at once with the first 20 slices' accumulators, the
+// accumulators of any further slices four at a time; one
 // inverse FWHT per row in registers and shuffles; then the agent's tail
 // tokens (online softmax) and the final normalisation. Launched as a
 // programmatic dependent of the kernel that wrote the partials. It releases
